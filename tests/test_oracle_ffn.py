@@ -1,0 +1,214 @@
+"""Pins for the oracle's expert FFN, bucketing, RMS chaining and FP8 GEMV
+(CPU only)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp4_softmax_gb300 import synth
+from conftest import golden
+from oracle import oracle as O
+
+E2M1 = {int(r[0]): float(r[1]) for r in golden("e2m1_codes.txt")}
+
+
+def _bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _e4m3(b):
+    return float(torch.tensor([b], dtype=torch.uint8).view(torch.float8_e4m3fn).float())
+
+
+def _brute_dequant(rec, off, soff, rows, K, fmt):
+    """Element-by-element decode straight from the record bytes."""
+    Gs = 16 if fmt == O.FMT_NVFP4 else 32
+    out = [[0.0] * K for _ in range(rows)]
+    for r in range(rows):
+        for c in range(K):
+            byte = int(rec[off + (r * K + c) // 2])
+            code = byte & 0xF if c % 2 == 0 else byte >> 4
+            sb = int(rec[soff + (r * K + c) // Gs])
+            s = _e4m3(sb) if fmt == O.FMT_NVFP4 else 2.0 ** (sb - 127)
+            out[r][c] = E2M1[code] * s
+    return out
+
+
+def _brute_layer(xb, idx, w, recs, H, I, fmt):
+    lay = O.record_layout(H, I, fmt)
+    x = [[float(v) for v in row] for row in O.bf16_bits_to_f32(xb)]
+    T, k = idx.shape
+    y = [[0.0] * H for _ in range(T)]
+    for t in range(T):
+        for j in range(k):
+            rec = recs[int(idx[t, j])]
+            Wg = _brute_dequant(rec, lay["gate"], lay["gate_s"], I, H, fmt)
+            Wu = _brute_dequant(rec, lay["up"], lay["up_s"], I, H, fmt)
+            Wd = _brute_dequant(rec, lay["down"], lay["down_s"], H, I, fmt)
+            g = [math.fsum(Wg[i][h] * x[t][h] for h in range(H)) for i in range(I)]
+            u = [math.fsum(Wu[i][h] * x[t][h] for h in range(H)) for i in range(I)]
+            hh = [g[i] / (1.0 + math.exp(-g[i])) * u[i] for i in range(I)]
+            for n in range(H):
+                y[t][n] += w[t, j] * math.fsum(Wd[n][i] * hh[i] for i in range(I))
+    return np.array(y)
+
+
+def _pool(E, H, I, fmt, seed):
+    recs = []
+    for e in range(E):
+        g, u, d = synth.expert_weights(H, I, seed + e, std=0.5)
+        recs.append(O.pack_expert(g.numpy(), u.numpy(), d.numpy(), fmt))
+    return recs
+
+
+@pytest.mark.parametrize("fmt", [O.FMT_NVFP4, O.FMT_MXFP4])
+def test_decode_layer_matches_brute_force(fmt):
+    H, I, E, k, T = 32, 32, 6, 3, 2
+    recs = _pool(E, H, I, fmt, 100)
+    xb = _bits(synth.activations(T, H, 21))
+    idx = np.array([[4, 0, 2], [1, 5, 3]], dtype=np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.6, 0.25, 0.15]])
+    got = O.moe_layer_decode(xb, idx, w, recs, H, I, fmt)
+    want = _brute_layer(xb, idx, w, recs, H, I, fmt)
+    assert O.rel_l2(got, want) < 1e-7
+
+
+def test_pointer_table_permutation_invariance_and_zero_record():
+    H, I, E = 64, 32, 5
+    recs = _pool(E, H, I, O.FMT_NVFP4, 200)
+    xb = _bits(synth.activations(3, H, 22))
+    idx = np.array([[0, 1], [2, 3], [4, 0]], dtype=np.int32)
+    w = np.array([[0.7, 0.3], [0.5, 0.5], [0.9, 0.1]])
+    base = O.moe_layer_decode(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+    perm = [3, 0, 4, 1, 2]                       # slot s holds expert perm[s]
+    table = {perm[s]: recs[perm[s]] for s in range(E)}
+    assert np.array_equal(O.moe_layer_decode(xb, idx, w, table, H, I, O.FMT_NVFP4), base)
+    zero = dict(enumerate(recs))
+    zero[4] = np.zeros_like(recs[4])
+    y = O.moe_layer_decode(xb, idx, w, zero, H, I, O.FMT_NVFP4)
+    only0 = O.moe_layer_decode(xb[2:3], np.array([[0]]), np.array([[0.1]]), recs, H, I, O.FMT_NVFP4)
+    assert np.allclose(y[2], only0[0], rtol=1e-6, atol=0)
+
+
+def test_k1_weight1_is_single_expert_ffn():
+    H, I = 64, 32
+    g, u, d = synth.expert_weights(H, I, 300, std=0.5)
+    rec = O.pack_expert(g.numpy(), u.numpy(), d.numpy(), O.FMT_NVFP4)
+    Wg, Wu, Wd = O.unpack_expert(rec, H, I, O.FMT_NVFP4)
+    xb = _bits(synth.activations(1, H, 23))
+    x = O.bf16_bits_to_f32(xb)[0].astype(np.float64)
+    gg, uu = Wg @ x, Wu @ x
+    want = Wd @ (gg * uu * scipy_expit(gg))
+    y = O.moe_layer_decode(xb, np.array([[0]]), np.array([[1.0]]), [rec], H, I, O.FMT_NVFP4)
+    assert np.allclose(y[0], want, rtol=1e-6, atol=1e-12)
+
+
+def scipy_expit(v):
+    import scipy.special
+    return scipy.special.expit(v)
+
+
+def _controls_setup():
+    H, I, E = 64, 32, 4
+    recs = _pool(E, H, I, O.FMT_NVFP4, 400)
+    xb = _bits(synth.activations(2, H, 24))
+    idx = np.array([[0, 1], [2, 3]], dtype=np.int32)
+    w = np.array([[0.6, 0.4], [0.8, 0.2]])
+    return H, I, recs, xb, idx, w
+
+
+def test_negative_control_nibble_swap_breaks_output():
+    H, I, recs, xb, idx, w = _controls_setup()
+    base = O.moe_layer_decode(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+    lay = O.record_layout(H, I, O.FMT_NVFP4)
+    bad = []
+    for r in recs:
+        r = r.copy()
+        c = r[: lay["gate_s"]]
+        r[: lay["gate_s"]] = ((c & 0xF) << 4) | (c >> 4)
+        bad.append(r)
+    assert O.rel_l2(O.moe_layer_decode(xb, idx, w, bad, H, I, O.FMT_NVFP4), base) > 0.1
+
+
+def test_negative_control_gate_up_swap_breaks_output():
+    H, I, recs, xb, idx, w = _controls_setup()
+    base = O.moe_layer_decode(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+    lay = O.record_layout(H, I, O.FMT_NVFP4)
+    bad = []
+    for r in recs:
+        r = r.copy()
+        a = r[lay["gate"]:lay["up"]].copy()
+        r[lay["gate"]:lay["up"]] = r[lay["up"]:lay["down"]]
+        r[lay["up"]:lay["down"]] = a
+        bad.append(r)
+    assert O.rel_l2(O.moe_layer_decode(xb, idx, w, bad, H, I, O.FMT_NVFP4), base) > 0.1
+
+
+def test_negative_control_wrong_scale_format_breaks_output():
+    H, I, recs, xb, idx, w = _controls_setup()
+    base = O.moe_layer_decode(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+    Wg, Wu, Wd = O.unpack_expert(recs[0], H, I, O.FMT_NVFP4)
+    lay = O.record_layout(H, I, O.FMT_NVFP4)
+    c = recs[0][lay["gate"]:lay["up"]].reshape(I, H // 2)
+    s = recs[0][lay["gate_s"]:lay["up_s"]].reshape(I, H // 16)
+    as_ue8m0 = O.e2m1_decode(np.stack([c & 0xF, c >> 4], -1).reshape(I, H)) * \
+        np.repeat(O.ue8m0_decode(s), 16, axis=1)
+    assert O.rel_l2(as_ue8m0, Wg) > 0.5
+
+
+def test_grouped_k1_close_to_decode_and_by_expert_equal():
+    H, I, E = 64, 64, 4
+    recs = _pool(E, H, I, O.FMT_NVFP4, 500)
+    xb = _bits(synth.activations(6, H, 25))
+    idx = np.array([[0], [1], [2], [3], [0], [1]], dtype=np.int32)
+    w = np.ones((6, 1))
+    dec = O.moe_layer_decode(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+    grp = O.moe_layer_grouped(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+    assert O.rel_l2(grp, dec) < 2e-3
+    assert O.rel_l2(grp, dec) > 0          # the BF16 rounding of h is visible
+    idx2 = np.array([[0, 1], [1, 2], [2, 3], [3, 0], [0, 2], [1, 3]], dtype=np.int32)
+    w2 = np.full((6, 2), 0.5)
+    a = O.moe_layer_grouped(xb, idx2, w2, recs, H, I, O.FMT_NVFP4)
+    b = O.moe_layer_grouped_by_expert(xb, idx2, w2, recs, H, I, O.FMT_NVFP4)
+    assert O.rel_l2(a, b) < 1e-6
+
+
+def test_bucketing_brute_force():
+    rng = np.random.default_rng(9)
+    T, k, E = 37, 4, 11
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, pairs = O.bucket_by_expert(idx, E)
+    want = []
+    for e in range(E):
+        grp = [t * k + j for t in range(T) for j in range(k) if idx[t, j] == e]
+        assert counts[e] == len(grp)
+        assert offsets[e] == len(want)
+        want += grp
+    assert offsets[E] == T * k
+    assert list(pairs) == want
+
+
+def test_rmsnorm_matches_torch_then_bf16():
+    rng = np.random.default_rng(10)
+    y = (rng.standard_normal((4, 256)) * 0.3).astype(np.float32)
+    got = O.rmsnorm_bf16(y, 1e-6)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(y).double(), (256,), eps=1e-6)
+    want = O.bf16_round_bits(ref.numpy())
+    assert np.array_equal(got, want)
+    xs = O.bf16_bits_to_f32(got).astype(np.float64)
+    assert np.allclose(np.sqrt(np.mean(xs * xs, axis=1)), 1.0, atol=1e-2)
+
+
+def test_fp8_gemv_brute_force():
+    rng = np.random.default_rng(11)
+    M, K = 9, 48
+    W = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    W[(W & 0x7F) == 0x7F] = 0x11                 # no NaN codes
+    s = rng.uniform(0.5, 2.0, M).astype(np.float32)
+    xb = _bits(synth.activations(1, K, 26))[0]
+    got = O.fp8_rowscale_gemv(W, s, xb)
+    x = O.bf16_bits_to_f32(xb)
+    for m in range(M):
+        want = float(s[m]) * math.fsum(_e4m3(int(W[m, c])) * float(x[c]) for c in range(K))
+        assert np.float32(want) == got[m] or abs(want - got[m]) <= 1e-6 * abs(want)

@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the routed-MoE FFN with block-scaled FP4 experts on GB300.
+
+Default workload: the Qwen-shaped decode stack -- 48 layers, each with 512
+NVFP4 experts (H=2560, I=640, 2,764,800-byte records, ~68 GB resident in
+HBM), top-10 routing, one token per step; each layer's input is the previous
+layer's output, RMS-normalised.  A step runs router -> experts -> RMS chaining
+for all 48 layers.  The metric is expert GB/s: the bytes of the records the
+step selects divided by the step time, and its fraction of the HBM roofline.
+
+``--impl reference`` times the CPU oracle (float64 numpy) on a bounded sample
+of the same workload instead.
+
+One JSON line is printed by rank 0.  Multi-GPU runs (torchrun) are independent
+replicas: each rank decodes its own tokens, no data-path collective.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "expert GB/s & fraction of HBM peak (decode); tokens/s per MoE layer (prompt)"
+H, I, E, K_TOP, LAYERS = 2560, 640, 512, 10, 48
+WORKLOAD_ID = 1
+UNIQUE_EXPERTS = 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the decode-stack workload on the GPU
+# ---------------------------------------------------------------------------
+class DecodeStack:
+    def __init__(self, torch, moe, synth, device, rank: int, steps_total: int):
+        self.torch, self.moe, self.synth = torch, moe, synth
+        self.dev = device
+        self.s = moe.shape(H, I, moe.FMT_NVFP4)
+        self.rec_bytes = moe.moe_expert_record_bytes(self.s)
+        t0 = time.time()
+        uniq = torch.empty(UNIQUE_EXPERTS, self.rec_bytes, dtype=torch.uint8, device=device)
+        for u in range(UNIQUE_EXPERTS):
+            g, up, d = synth.expert_weights(H, I, synth.expert_seed(WORKLOAD_ID, 0, u), device=device)
+            moe.fp4_pack_expert(g, up, d, self.s, record=uniq[u])
+        # 48 x 512 slots, each its own physical copy of a seeded choice of record
+        self.slots = torch.empty(LAYERS, E, self.rec_bytes, dtype=torch.uint8, device=device)
+        self.choice = []
+        for L in range(LAYERS):
+            rng = np.random.default_rng(synth.seed_of(WORKLOAD_ID, L, synth.T_PERM))
+            ch = rng.permutation(UNIQUE_EXPERTS)[:E]
+            self.choice.append(ch)
+            for e in range(E):  # one contiguous device-to-device copy per slot
+                self.slots[L, e].copy_(uniq[int(ch[e])])
+        del uniq
+        self.ptrs = [moe.pointer_table([self.slots[L, e] for e in range(E)]) for L in range(LAYERS)]
+        self.wr = torch.stack([synth.router_weights(E, H, synth.seed_of(WORKLOAD_ID, L, synth.T_ROUTER),
+                                                    device=device) for L in range(LAYERS)])
+        # one input token per step (distinct tokens, seeded)
+        self.x0 = torch.cat([synth.activations(1, H, synth.seed_of(WORKLOAD_ID, 100 + s, synth.T_X),
+                                               device=device) for s in range(steps_total)])
+        self.x = torch.empty(1, H, dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty(1, K_TOP, dtype=torch.int32, device=device)
+        self.w = torch.empty(1, K_TOP, dtype=torch.float32, device=device)
+        self.logits = torch.empty(1, E, dtype=torch.float32, device=device)
+        self.y = torch.empty(1, H, dtype=torch.float32, device=device)
+        self.ws = torch.zeros(moe.moe_experts_decode_workspace(1, K_TOP, self.s), dtype=torch.uint8,
+                              device=device)
+        self.st = torch.zeros(1, dtype=torch.int32, device=device)
+        self.setup_s = time.time() - t0
+        self.kernels_per_step = LAYERS * 5 - 1
+        self.ev = None
+
+    def expert_bytes_per_step(self):
+        return LAYERS * K_TOP * self.rec_bytes
+
+    def run_layers(self, timing_events=None):
+        moe = self.moe
+        for L in range(LAYERS):
+            moe.moe_router_topk(self.x, self.wr[L], None, K_TOP, self.idx, self.w, self.logits)
+            if timing_events is not None:
+                timing_events[L][0].record()
+            moe.moe_experts_decode(self.x, self.idx, self.w, self.ptrs[L], self.s, self.y, self.ws,
+                                   self.st)
+            if timing_events is not None:
+                timing_events[L][1].record()
+            if L + 1 < LAYERS:
+                moe.moe_rmsnorm_bf16(self.y, 1e-6, self.x)
+
+    def capture(self, with_events: bool):
+        torch = self.torch
+        self.x.copy_(self.x0[0:1])
+        self.run_layers()  # warm, sets kernel attributes outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        ev = None
+        if with_events:
+            ev = [(torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True)) for _ in range(LAYERS)]
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self.run_layers(ev)
+        return g, ev
+
+
+def _hash_sources():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_scaled_fp4_softmax_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profiles(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d.get(kernel_key)
+        if ent and ent.get("sources") == _hash_sources():
+            return ent["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from block_scaled_fp4_softmax_gb300 import build, moe, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    moe.load()
+
+    steps, warm = args.steps, args.warmup
+    wl = DecodeStack(torch, moe, synth, dev, rank, steps + warm)
+    graph, _ = wl.capture(with_events=False)
+    stream = torch.cuda.current_stream()
+
+    def one_step(s):
+        wl.x.copy_(wl.x0[s:s + 1])
+        graph.replay()
+
+    for s in range(warm):
+        one_step(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(steps):
+        one_step(warm + s)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end) / steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    st = int(wl.st.item())
+
+    # dominant kernel (the expert pass) timed with events inside the graph
+    kern_ms = None
+    try:
+        g2, ev = wl.capture(with_events=True)
+        samples = []
+        for s in range(steps):
+            wl.x.copy_(wl.x0[(warm + s) % (steps + warm):(warm + s) % (steps + warm) + 1])
+            g2.replay()
+            torch.cuda.synchronize()
+            samples += [a.elapsed_time(b) for a, b in ev]
+        kern_ms = statistics.mean(samples)
+        del g2
+    except Exception as exc:  # events inside graphs unsupported: time eagerly
+        print(f"# graph events unavailable ({exc}); timing the expert pass eagerly", file=sys.stderr)
+        samples = []
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for s in range(steps):
+            L = s % LAYERS
+            torch.ops.aten.fill_(flush, s & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            moe.moe_experts_decode(wl.x, wl.idx, wl.w, wl.ptrs[L], wl.s, wl.y, wl.ws, wl.st)
+            b.record()
+            torch.cuda.synchronize()
+            samples.append(a.elapsed_time(b))
+        kern_ms = statistics.mean(samples)
+
+    # end to end through the C ABI with host buffers: H2D of the token, all
+    # 48 layers as separate library calls, D2H of the output
+    e2e = None
+    if not args.no_e2e:
+        x_host = wl.x0.cpu().pin_memory()
+        y_host = torch.empty(1, H, dtype=torch.float32).pin_memory()
+        e_steps = max(3, min(steps, 20))
+        for s in range(2):
+            wl.x.copy_(x_host[s:s + 1], non_blocking=True)
+            wl.run_layers()
+            y_host.copy_(wl.y, non_blocking=True)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record()
+        for s in range(e_steps):
+            wl.x.copy_(x_host[s % x_host.shape[0]:s % x_host.shape[0] + 1], non_blocking=True)
+            wl.run_layers()
+            y_host.copy_(wl.y, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) / e_steps
+        e2e = {"value": round(wl.expert_bytes_per_step() / wall / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4,
+               "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 240 per token"}
+
+    peak, peak_kind = _peaks()
+    value = wl.expert_bytes_per_step() * world / (ms / 1e3) / 1e9
+    per_launch_bytes = K_TOP * wl.rec_bytes + H * 2 + H * 4 + K_TOP * I * 4 * 2
+    achieved = per_launch_bytes / (kern_ms / 1e3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1+e4m3 weights, bf16 activations, f32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) FP32 experts packed to NVFP4 on device; "
+                "1024 distinct experts copied into 24,576 physical slots)",
+        "config": {"workload": "qwen_decode_stack: 48 layers x 512 NVFP4 experts "
+                               "(H=2560, I=640, 2,764,800 B each, 68 GB resident), top-10, 1 token/step, "
+                               "RMS-chained layers",
+                   "tokens_per_step": 1, "layers": LAYERS, "experts": E, "top_k": K_TOP,
+                   "expert_bytes_per_step": wl.expert_bytes_per_step(),
+                   "l2": "inputs larger than L2: 1.33 GB of distinct expert records per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "CUDA graph of 239 kernel launches per step"},
+        "tokens_per_s": round(world * 1e3 / ms, 2),
+        "hbm_frac": {"of_measured": round(value / world / peak, 4), "measured_gbs": peak,
+                     "of_nominal_8000": round(value / world / 8000.0, 4)},
+        "roofline": {"bound": "hbm", "kernel": "moe_experts_decode (gate/up + down kernels)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "peak_kind": peak_kind + " (burst copy)",
+                     "frac": round(achieved / peak, 4),
+                     "bytes_per_launch": per_launch_bytes, "avg_launch_us": round(kern_ms * 1e3, 3),
+                     "traffic": _traffic_from_profiles("moe_experts_decode")},
+        "gpu_launches": wl.kernels_per_step * steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "dev_status": st,
+        "setup_s": round(wl.setup_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+def _oracle_sample(budget_s: float, max_layers: int = LAYERS):
+    """Run the oracle through the decode stack for one token until the time
+    budget is used; returns (expert bytes processed, seconds, layers)."""
+    import torch
+
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    rec_bytes = O.record_bytes(H, I, O.FMT_NVFP4)
+    x = bits(synth.activations(1, H, synth.seed_of(WORKLOAD_ID, 100, synth.T_X)))
+    done_bytes, busy, layers = 0, 0.0, 0
+    for L in range(max_layers):
+        wr = bits(synth.router_weights(E, H, synth.seed_of(WORKLOAD_ID, L, synth.T_ROUTER)))
+        rng = np.random.default_rng(synth.seed_of(WORKLOAD_ID, L, synth.T_PERM))
+        choice = rng.permutation(UNIQUE_EXPERTS)[:E]
+        t0 = time.perf_counter()
+        idx, w = O.topk_softmax(O.router_logits(x, wr), K_TOP)
+        busy += time.perf_counter() - t0
+        recs = {}
+        for e in idx.ravel():          # records are inputs: pack them untimed
+            g, u, d = synth.expert_weights(H, I, synth.expert_seed(WORKLOAD_ID, 0, int(choice[e])))
+            recs[int(e)] = O.pack_expert(g.numpy(), u.numpy(), d.numpy(), O.FMT_NVFP4)
+        t0 = time.perf_counter()
+        y = O.moe_layer_decode(x, idx, w, recs, H, I, O.FMT_NVFP4)
+        x = O.rmsnorm_bf16(y, 1e-6)
+        busy += time.perf_counter() - t0
+        done_bytes += K_TOP * rec_bytes
+        layers += 1
+        if busy >= budget_s:
+            break
+    return done_bytes, busy, layers
+
+
+def _cores():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s: float):
+    nbytes, secs, layers = _oracle_sample(budget_s)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"{layers} layers of the decode stack for 1 token (router + 10 experts + "
+                      f"RMS chaining per layer), float64 numpy; record packing untimed",
+            "seconds": round(secs, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    steps, warm = args.steps, args.warmup
+    per_step_budget = max(0.5, args.cpu_seconds / max(1, steps))
+    for _ in range(min(warm, 1)):
+        _oracle_sample(0.0, max_layers=1)
+    t_bytes, t_secs, t_layers = 0, 0.0, 0
+    for _ in range(steps):
+        b, s, l = _oracle_sample(per_step_budget, max_layers=2)
+        t_bytes += b
+        t_secs += s
+        t_layers += l
+    value = t_bytes / t_secs / 1e9
+    cores = _cores()
+    sample = (f"{t_layers} layers over {steps} steps of the decode stack for 1 token, "
+              f"float64 numpy oracle")
+    out = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+           "steps": steps, "warmup": warm, "ms_per_step": round(t_secs / steps * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": "qwen_decode_stack (bounded sample on host cores)"},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                            "cores": cores, "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

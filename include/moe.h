@@ -1,0 +1,202 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed mixture-of-experts FFN with
+ * block-scaled FP4 experts.
+ *
+ * The operation is one routed-MoE feed-forward layer as the pages on
+ * streaming experts describe it: a router picks the top-k experts of a token
+ * ("Running a 133 GB MoE model on an 8 GB GPU at 11 tokens/s by streaming
+ * experts from NVMe", section "Why this model": top-10 of 512; "Running the
+ * 510 GB DeepSeek-V4.1-Flash on an 8 GB GPU, and three bugs that never raise
+ * an error", section "Bytes per token decide everything": 6 of 384); every
+ * selected expert is one contiguous record gate | up | down | gate_scale |
+ * up_scale | down_scale of FP4 (e2m1) codes with block scales (first page,
+ * section "The engine", item 1); the expert computes SwiGLU
+ * down(silu(gate x) * up x) (first page, "The engine", item 4); the outputs
+ * are summed with the router weights.
+ *
+ * Conventions shared by every entry point:
+ *  - All data pointers are DEVICE pointers owned by the caller, unless a
+ *    comment says otherwise.  The library keeps no state between calls and
+ *    allocates no memory.
+ *  - BF16 tensors are passed as uint16_t bit patterns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous on that stream.
+ *  - The return value is a moe_status: host-side argument checks and launch
+ *    errors only.  Errors found while a kernel runs (a bad expert index, a
+ *    NULL or misaligned record, a wait that ran out) are OR-ed into the
+ *    optional device word `dev_status` (MOE_DEV_* bits); the kernel skips
+ *    the bad item, never traps, and the caller reads the word after its own
+ *    synchronisation.
+ *  - Matrices are row-major [out x in] with the input dimension K contiguous:
+ *    gate and up are [I x H], down is [H x I].
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* NULL pointer, negative or zero size, k > E ... */
+  MOE_ERR_ALIGNMENT = 2,           /* a pointer is not 16-byte aligned */
+  MOE_ERR_UNSUPPORTED = 3,         /* shape outside what the kernels handle */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the *_workspace() size */
+  MOE_ERR_CUDA = 5                 /* a CUDA launch or runtime call failed */
+} moe_status;
+
+/* Record formats. */
+enum {
+  MOE_FMT_NVFP4 = 0, /* e2m1 codes + one FP8 E4M3 scale per 16 elements */
+  MOE_FMT_MXFP4 = 1  /* e2m1 codes + one UE8M0 scale (2^(s-127)) per 32 elements */
+};
+
+/* Bits of the device status word. */
+enum {
+  MOE_DEV_NULL_EXPERT = 1, /* a selected expert's record pointer was NULL */
+  MOE_DEV_MISALIGNED = 2,  /* a selected expert's record was not 16-byte aligned */
+  MOE_DEV_BAD_INDEX = 4,   /* an expert index was outside [0, E) */
+  MOE_DEV_TIMEOUT = 8      /* a bounded wait inside a kernel gave up */
+};
+
+/* Expert shape: hidden size H, intermediate size I, record format.
+ * Supported: H and I multiples of 64, H <= 16384, I <= 8192. */
+typedef struct {
+  int32_t hidden;
+  int32_t inter;
+  int32_t format;
+} moe_expert_shape;
+
+/* Byte size of one expert record (first page, "The engine", item 1: one
+ * 2,764,800-byte block for H=2560, I=640, NVFP4; second page, "The
+ * approach": 17.7 MB of codes + 1.1 MB of scales for the DeepSeek shape).
+ * Layout, all parts back to back, no padding:
+ *   gate codes [I x H/2] | up codes [I x H/2] | down codes [H x I/2] |
+ *   gate scales [I x H/G] | up scales [I x H/G] | down scales [H x I/G]
+ * G = 16 (NVFP4) or 32 (MXFP4).  Codes hold two elements per byte, element
+ * 2i in the low nibble.  Returns 0 for an unsupported shape. */
+size_t moe_expert_record_bytes(moe_expert_shape s);
+
+/* Byte offsets of the six parts plus the total, written to offsets[0..6]
+ * (host array) in the order gate, up, down, gate_s, up_s, down_s, total. */
+int moe_expert_record_offsets(moe_expert_shape s, size_t* offsets);
+
+/* Quantise one expert from FP32 and pack its record (first page, "The
+ * engine", item 1: the repacked one-block-per-expert format).
+ * gate [I x H], up [I x H], down [H x I]: FP32 device arrays.
+ * record: device buffer of moe_expert_record_bytes(s) bytes, 16-B aligned.
+ * NVFP4 block of 16: s = E4M3_rn_satfinite(amax / 6) (FP32 divide); if the
+ * decoded s is 0 every code is +0, else code = e2m1_rn_satfinite(x / s).
+ * MXFP4 block of 32: s = clamp(E + 127, 0, 254) for the smallest E with
+ * 6 * 2^E >= amax (s = 0 when amax = 0); code = e2m1_rn_satfinite(x * 2^(127-s)).
+ * Round to nearest, ties to even; the sign of zero results is kept. */
+int fp4_pack_expert(const float* gate, const float* up, const float* down,
+                    moe_expert_shape s, void* record, void* stream);
+
+/* Router: logits, top-k and renormalised softmax weights (first page, "Why
+ * this model": top-10 routing; "Where the time actually goes": the router's
+ * answer gates the expert work).
+ * x_bf16 [T x H], wr_bf16 [E x H]: BF16, 16-B aligned, H % 8 == 0.
+ * bias [E] FP32 or NULL.
+ * logits [T x E] FP32 output (required): logit[t,e] = sum_h x[t,h] W_r[e,h]
+ *   (+ bias[e]) summed in FP32 in a fixed order: the K axis is cut into
+ *   chunks of 8; chunk c goes to slot c mod 32; each slot sums its chunks in
+ *   ascending order from +0; the 32 slots are combined pairwise, slot i with
+ *   slot i xor d for d = 16, 8, 4, 2, 1; the bias is added last.
+ * idx [T x k] int32 output: the k largest logits, larger first, ties to the
+ *   lower expert index, NaN last.
+ * weights [T x k] FP32 output: exp(l_j - l_0) / sum_i exp(l_i - l_0) over
+ *   the selected k (sums to 1).
+ * Limits: 1 <= k <= min(E, 32), E <= 4096. */
+int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, const float* bias,
+                    int T, int H, int E, int k,
+                    int32_t* idx, float* weights, float* logits, void* stream);
+
+/* Layer chaining for stacked decode: x[t] = BF16(y[t] / sqrt(mean(y[t]^2) +
+ * eps)), no learnable weight; the mean and the division are done in FP64 and
+ * the result is rounded once to BF16 (ties to even).
+ * y [T x H] FP32 input, x_bf16 [T x H] output. */
+int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16_t* x_bf16,
+                     void* stream);
+
+/* Workspace bytes moe_experts_decode needs for T tokens, k experts each.
+ * The workspace holds the FP32 SwiGLU intermediate and, at its end, the words
+ * of a grid barrier: it must be zero-filled before its first use.  Every call
+ * that completes leaves those words at zero again, so one zeroed workspace
+ * serves any number of calls on one stream; calls that overlap in time need
+ * separate workspaces.  After a call that reported MOE_DEV_TIMEOUT, zero it
+ * again. */
+size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s);
+
+/* Decode path: the experts of T tokens (T*k small, GEMV shaped), HBM bound
+ * (first page, "The engine", item 4: the single-token NVFP4 SwiGLU expert
+ * kernel).  For T*k <= 64 (and T*H, T*k*I within 24K floats) this is one
+ * persistent kernel with a grid barrier between gate/up and down; larger
+ * calls use two kernels.  Results are bit-identical between repeated calls.
+ * x_bf16 [T x H]; idx, weights [T x k] as moe_router_topk writes them.
+ * expert_ptrs: device array of E device pointers, one record per expert;
+ *   entries may point anywhere (arbitrary slots), 16-B aligned; an entry may
+ *   be NULL if that expert is never selected.
+ * y [T x H] FP32 output, overwritten:
+ *   y[t] = sum_j weights[t,j] * down_e(silu(gate_e x_t) * up_e x_t),
+ *   e = idx[t,j], with FP32 accumulation and an FP32 SwiGLU intermediate,
+ *   summed in a fixed order (bit-reproducible).
+ * workspace: device scratch of at least moe_experts_decode_workspace() bytes.
+ * dev_status: device int32 or NULL; MOE_DEV_* bits are OR-ed into it.
+ * Limits: T*k <= 4096. */
+int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
+                       int T, int k, const void* const* expert_ptrs, int E,
+                       moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
+                       int32_t* dev_status, void* stream);
+
+/* Bucketing of routed pairs by expert (first page, "The engine", item 5:
+ * the whole prompt runs through a layer at once; second page, "v3": each
+ * expert's tokens are found by comparing the index tensor with the expert).
+ * idx [T x k] int32 input.  counts [E], offsets [E+1] (exclusive scan of
+ * counts), pairs [T*k]: the pair ids p = t*k + j grouped by expert, ascending
+ * p inside each group.  Bit-reproducible.  An index outside [0, E) sets
+ * MOE_DEV_BAD_INDEX in dev_status (if given) and the pair is dropped.
+ * workspace: at least moe_bucket_workspace(T, k, E) bytes. */
+size_t moe_bucket_workspace(int T, int k, int E);
+int moe_bucket_by_expert(const int32_t* idx, int T, int k, int E, int32_t* counts,
+                         int32_t* offsets, int32_t* pairs, void* workspace,
+                         size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Workspace bytes moe_experts_grouped needs. */
+size_t moe_experts_grouped_workspace(int T, int k, int E, moe_expert_shape s);
+
+/* Prompt path: the same layer for many tokens as a grouped contraction on
+ * the tensor cores (tcgen05, BF16 operands, FP32 accumulation in TMEM).
+ * Same arguments and output as moe_experts_decode, except:
+ *  - the SwiGLU intermediate silu(g) * u is rounded to BF16 before the down
+ *    projection (it is a BF16 MMA operand);
+ *  - the k contributions to y[t] are accumulated with FP32 atomic adds, so
+ *    the order of the additions (and the last bits of y) may vary between
+ *    runs.
+ * Only MOE_FMT_NVFP4 and MOE_FMT_MXFP4 records with H % 128 == 0 and
+ * I % 128 == 0 are accepted. */
+int moe_experts_grouped(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
+                        int T, int k, const void* const* expert_ptrs, int E,
+                        moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
+                        int32_t* dev_status, void* stream);
+
+/* FP8 row-scaled matrix-vector (first page, "Why this model": large matrices
+ * stored in FP8 with one scale per row; "The engine", item 4: their own GEMV
+ * kernel).  w_e4m3 [M x K] E4M3FN bytes, row_scale [M] FP32, x_bf16 [K];
+ * y[m] = row_scale[m] * sum_k e4m3(w[m,k]) * x[k], FP32 accumulation.
+ * K % 16 == 0; w and x 16-B aligned. */
+int fp8_rowscale_gemv(const uint8_t* w_e4m3, const float* row_scale, const uint16_t* x_bf16,
+                      int M, int K, float* y, void* stream);
+
+/* Static text for a moe_status value. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

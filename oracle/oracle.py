@@ -81,17 +81,18 @@ def ue8m0_decode(b) -> np.ndarray:
 
 def _rn_even_on_grid(mag: np.ndarray, grid: np.ndarray) -> np.ndarray:
     """Index into an ascending non-negative grid of the nearest point to
-    ``mag`` (float64, >= 0), ties going to the even index; values above the
-    top of the grid saturate to the top (satfinite)."""
-    mag = np.asarray(mag, dtype=np.float64)
-    top = len(grid) - 1
-    lo = np.clip(np.searchsorted(grid, mag, side="right") - 1, 0, top)
-    hi = np.minimum(lo + 1, top)
-    dlo = mag - grid[lo]
-    dhi = grid[hi] - mag
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0) & (hi != lo))
-    out = np.where(pick_hi, hi, lo)
-    return np.where(mag >= grid[top], top, out)
+    ``mag`` (>= 0), ties going to the even index; values above the top of the
+    grid saturate to the top (satfinite).
+
+    With mid[m] = (grid[m] + grid[m+1]) / 2 (exact in binary), the nearest
+    index is the number of midpoints strictly below ``mag``; when ``mag``
+    equals a midpoint the two neighbours m and m+1 tie and the even one wins.
+    """
+    mids = (grid[:-1] + grid[1:]) / 2
+    below = np.searchsorted(mids, mag, side="left")       # #mids < mag
+    at = np.minimum(below, len(mids) - 1)
+    tie = mids[at] == mag
+    return np.where(tie & (below % 2 == 1), below + 1, below)
 
 
 _E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
@@ -102,17 +103,17 @@ def e2m1_encode(v) -> np.ndarray:
     """Round float values to e2m1 codes: nearest, ties to even, |v| > 6
     saturates to 6.  The sign is kept, so a negative value that rounds to zero
     gives code 8 (-0)."""
-    v = np.asarray(v, dtype=np.float64)
-    mag_code = _rn_even_on_grid(np.abs(v), _E2M1_GRID)
-    return (mag_code | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+    v = np.asarray(v)
+    mag_code = _rn_even_on_grid(np.abs(v), _E2M1_GRID).astype(np.uint8)
+    return mag_code | (np.signbit(v).astype(np.uint8) << 3)
 
 
 def e4m3_encode(v) -> np.ndarray:
     """Round float values to E4M3FN bytes: nearest, ties to even, |v| > 448
     saturates to 448 (satfinite).  Sign kept."""
-    v = np.asarray(v, dtype=np.float64)
-    mag_code = _rn_even_on_grid(np.abs(v), _E4M3_GRID)
-    return (mag_code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+    v = np.asarray(v)
+    mag_code = _rn_even_on_grid(np.abs(v), _E4M3_GRID).astype(np.uint8)
+    return mag_code | (np.signbit(v).astype(np.uint8) << 7)
 
 
 # ---------------------------------------------------------------------------

@@ -111,7 +111,7 @@ int fp4_pack_expert(const float* gate, const float* up, const float* down,
  *   lower expert index, NaN last.
  * weights [T x k] FP32 output: exp(l_j - l_0) / sum_i exp(l_i - l_0) over
  *   the selected k (sums to 1).
- * Limits: 1 <= k <= min(E, 32), E <= 4096. */
+ * Limits: 1 <= k <= min(E, 32), E <= 1024. */
 int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, const float* bias,
                     int T, int H, int E, int k,
                     int32_t* idx, float* weights, float* logits, void* stream);

@@ -173,6 +173,81 @@ class DecodeStack:
         return g, ev
 
 
+class PromptLayer:
+    """Qwen-shaped prompt through one MoE layer: T=2451 tokens, 512 NVFP4
+    experts, top-10 with a Zipf(1.1) router bias; a step is router + the
+    grouped tensor-core expert pass."""
+
+    T = 2451
+    WORKLOAD = 2
+
+    def __init__(self, torch, moe, synth, device):
+        self.torch, self.moe = torch, moe
+        self.s = moe.shape(H, I, moe.FMT_NVFP4)
+        rb = moe.moe_expert_record_bytes(self.s)
+        self.pool = torch.empty(E, rb, dtype=torch.uint8, device=device)
+        for e in range(E):
+            g, up, d = synth.expert_weights(H, I, synth.expert_seed(self.WORKLOAD, 0, e), device=device)
+            moe.fp4_pack_expert(g, up, d, self.s, record=self.pool[e])
+        self.ptrs = moe.pointer_table([self.pool[e] for e in range(E)])
+        self.x = synth.activations(self.T, H, synth.seed_of(self.WORKLOAD, 0, synth.T_X), device=device)
+        self.wr = synth.router_weights(E, H, synth.seed_of(self.WORKLOAD, 0, synth.T_ROUTER), device=device)
+        self.bias = synth.zipf_bias(E, synth.seed_of(self.WORKLOAD, 0, synth.T_BIAS)).to(device)
+        self.idx = torch.empty(self.T, K_TOP, dtype=torch.int32, device=device)
+        self.w = torch.empty(self.T, K_TOP, dtype=torch.float32, device=device)
+        self.logits = torch.empty(self.T, E, dtype=torch.float32, device=device)
+        self.y = torch.empty(self.T, H, dtype=torch.float32, device=device)
+        self.ws = torch.empty(moe.moe_experts_grouped_workspace(self.T, K_TOP, E, self.s),
+                              dtype=torch.uint8, device=device)
+        self.st = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def step(self):
+        moe = self.moe
+        moe.moe_router_topk(self.x, self.wr, self.bias, K_TOP, self.idx, self.w, self.logits)
+        moe.moe_experts_grouped(self.x, self.idx, self.w, self.ptrs, self.s, self.y, self.ws, self.st)
+
+    def measure(self, steps: int, warm: int):
+        torch = self.torch
+        for _ in range(warm):
+            self.step()
+        torch.cuda.synchronize()
+        tot_step, tot_exp = 0.0, 0.0
+        for i in range(steps):
+            self.flush.fill_(i & 0xFF)          # L2 flush: 512 MB write between steps
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record()
+            self.moe.moe_router_topk(self.x, self.wr, self.bias, K_TOP, self.idx, self.w, self.logits)
+            b.record()
+            self.moe.moe_experts_grouped(self.x, self.idx, self.w, self.ptrs, self.s, self.y, self.ws,
+                                         self.st)
+            c.record()
+            torch.cuda.synchronize()
+            tot_step += a.elapsed_time(c)
+            tot_exp += b.elapsed_time(c)
+        ms, ms_exp = tot_step / steps, tot_exp / steps
+        counts = torch.bincount(self.idx.flatten().long(), minlength=E)
+        hit = int((counts > 0).sum().item())
+        flops = 2.0 * self.T * K_TOP * 3 * H * I
+        return {"tokens_per_s": round(self.T / (ms / 1e3), 1), "ms_per_layer": round(ms, 4),
+                "expert_pass_ms": round(ms_exp, 4),
+                "expert_tflops": round(flops / (ms_exp / 1e3) / 1e12, 2),
+                "expert_weight_gbs": round(hit * self.pool.shape[1] / (ms_exp / 1e3) / 1e9, 1),
+                "experts_hit": hit, "max_tokens_per_expert": int(counts.max().item()),
+                "tokens": self.T, "dev_status": int(self.st.item()),
+                "l2": "flushed (512 MB write) between steps"}
+
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest value over all ranks (the slowest rank's time)."""
+    import torch
+    if dist is None or not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _hash_sources():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_scaled_fp4_softmax_gb300", "csrc")
@@ -241,9 +316,7 @@ def run_ours(args):
     clocks = sampler.stop()
     ms = t_start.elapsed_time(t_end) / steps
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dist, dev)
         dist.barrier()
     st = int(wl.st.item())
 
@@ -302,6 +375,17 @@ def run_ours(args):
                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4,
                "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 240 per token"}
 
+    prompt = None
+    if not args.no_prompt:
+        del wl.slots
+        torch.cuda.empty_cache()
+        try:
+            pl = PromptLayer(torch, moe, synth, dev)
+            prompt = pl.measure(max(3, min(steps, 20)), 3)
+            del pl
+        except Exception as exc:  # report, do not hide
+            prompt = {"error": repr(exc)[:300]}
+
     peak, peak_kind = _peaks()
     value = wl.expert_bytes_per_step() * world / (ms / 1e3) / 1e9
     per_launch_bytes = K_TOP * wl.rec_bytes + H * 2 + H * 4 + K_TOP * I * 4 * 2
@@ -340,6 +424,7 @@ def run_ours(args):
         "gpu_launches": wl.kernels_per_step * steps,
         "clocks": clocks,
         "e2e": e2e,
+        "prompt": prompt,
         "dev_status": st,
         "setup_s": round(wl.setup_s, 1),
     }
@@ -354,9 +439,21 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
+def _pack_one(u):
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+    g, up, d = synth.expert_weights(H, I, synth.expert_seed(WORKLOAD_ID, 0, int(u)))
+    return O.pack_expert(g.numpy(), up.numpy(), d.numpy(), O.FMT_NVFP4)
+
+
 def _oracle_sample(budget_s: float, max_layers: int = LAYERS):
     """Run the oracle through the decode stack for one token until the time
-    budget is used; returns (expert bytes processed, seconds, layers)."""
+    budget is used; returns (expert bytes processed, seconds, layers).  The
+    records are inputs: the oracle packs them itself, in spawned worker
+    processes, outside the timed part."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
     import torch
 
     from block_scaled_fp4_softmax_gb300 import synth
@@ -368,25 +465,25 @@ def _oracle_sample(budget_s: float, max_layers: int = LAYERS):
     rec_bytes = O.record_bytes(H, I, O.FMT_NVFP4)
     x = bits(synth.activations(1, H, synth.seed_of(WORKLOAD_ID, 100, synth.T_X)))
     done_bytes, busy, layers = 0, 0.0, 0
-    for L in range(max_layers):
-        wr = bits(synth.router_weights(E, H, synth.seed_of(WORKLOAD_ID, L, synth.T_ROUTER)))
-        rng = np.random.default_rng(synth.seed_of(WORKLOAD_ID, L, synth.T_PERM))
-        choice = rng.permutation(UNIQUE_EXPERTS)[:E]
-        t0 = time.perf_counter()
-        idx, w = O.topk_softmax(O.router_logits(x, wr), K_TOP)
-        busy += time.perf_counter() - t0
-        recs = {}
-        for e in idx.ravel():          # records are inputs: pack them untimed
-            g, u, d = synth.expert_weights(H, I, synth.expert_seed(WORKLOAD_ID, 0, int(choice[e])))
-            recs[int(e)] = O.pack_expert(g.numpy(), u.numpy(), d.numpy(), O.FMT_NVFP4)
-        t0 = time.perf_counter()
-        y = O.moe_layer_decode(x, idx, w, recs, H, I, O.FMT_NVFP4)
-        x = O.rmsnorm_bf16(y, 1e-6)
-        busy += time.perf_counter() - t0
-        done_bytes += K_TOP * rec_bytes
-        layers += 1
-        if busy >= budget_s:
-            break
+    with cf.ProcessPoolExecutor(max_workers=min(K_TOP, os.cpu_count() or 2),
+                                mp_context=mp.get_context("spawn")) as ex:
+        for L in range(max_layers):
+            wr = bits(synth.router_weights(E, H, synth.seed_of(WORKLOAD_ID, L, synth.T_ROUTER)))
+            rng = np.random.default_rng(synth.seed_of(WORKLOAD_ID, L, synth.T_PERM))
+            choice = rng.permutation(UNIQUE_EXPERTS)[:E]
+            t0 = time.perf_counter()
+            idx, w = O.topk_softmax(O.router_logits(x, wr), K_TOP)
+            busy += time.perf_counter() - t0
+            sel = [int(e) for e in idx.ravel()]
+            recs = dict(zip(sel, ex.map(_pack_one, [int(choice[e]) for e in sel])))
+            t0 = time.perf_counter()
+            y = O.moe_layer_decode(x, idx, w, recs, H, I, O.FMT_NVFP4)
+            x = O.rmsnorm_bf16(y, 1e-6)
+            busy += time.perf_counter() - t0
+            done_bytes += K_TOP * rec_bytes
+            layers += 1
+            if busy >= budget_s:
+                break
     return done_bytes, busy, layers
 
 
@@ -439,6 +536,39 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile_case(args):
+    """A small case of one kernel family for ncu: the decode layer on a 64-expert
+    pool (177 MB of records, larger than L2), or the prompt layer."""
+    import torch
+
+    from block_scaled_fp4_softmax_gb300 import build, moe, synth
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    if args.profile_case == "decode_layer":
+        s = moe.shape(H, I, moe.FMT_NVFP4)
+        nE = 64
+        pool = torch.empty(nE, moe.moe_expert_record_bytes(s), dtype=torch.uint8, device=dev)
+        for e in range(nE):
+            g, up, d = synth.expert_weights(H, I, synth.expert_seed(0, 0, e), device=dev)
+            moe.fp4_pack_expert(g, up, d, s, record=pool[e])
+        ptrs = moe.pointer_table([pool[e] for e in range(nE)])
+        wr = synth.router_weights(nE, H, synth.seed_of(0, 0, synth.T_ROUTER), device=dev)
+        ws = torch.zeros(moe.moe_experts_decode_workspace(1, K_TOP, s), dtype=torch.uint8, device=dev)
+        y = torch.empty(1, H, dtype=torch.float32, device=dev)
+        for i in range(args.warmup + args.steps):
+            x = synth.activations(1, H, synth.seed_of(0, 50 + i, synth.T_X), device=dev)
+            idx, w, _ = moe.moe_router_topk(x, wr, None, K_TOP)
+            moe.moe_experts_decode(x, idx, w, ptrs, s, y, ws)
+        torch.cuda.synchronize()
+    else:
+        pl = PromptLayer(torch, moe, synth, dev)
+        for _ in range(args.warmup + args.steps):
+            pl.step()
+        torch.cuda.synchronize()
+    print("profile case done", file=sys.stderr)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,12 +577,17 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prompt", action="store_true")
+    ap.add_argument("--profile-case", choices=("none", "decode_layer", "prompt_layer"), default="none",
+                    help="small fixed case for ncu captures (no JSON line)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile_case != "none":
+        run_profile_case(args)
     else:
         run_ours(args)
 

@@ -139,24 +139,28 @@ class DecodeStack:
                               device=device)
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         self.setup_s = time.time() - t0
-        self.kernels_per_step = LAYERS * 5 - 1
+        self.kernels_per_step = LAYERS * 2
         self.ev = None
 
     def expert_bytes_per_step(self):
         return LAYERS * K_TOP * self.rec_bytes
 
     def run_layers(self, timing_events=None):
+        """One token through the 48 layers: layer 0 routes x0; every later
+        layer RMS-chains the previous output inside its router launch."""
         moe = self.moe
         for L in range(LAYERS):
-            moe.moe_router_topk(self.x, self.wr[L], None, K_TOP, self.idx, self.w, self.logits)
+            if L == 0:
+                moe.moe_router_topk(self.x, self.wr[L], None, K_TOP, self.idx, self.w, self.logits)
+            else:
+                moe.moe_rmsnorm_router_topk(self.y, self.wr[L], None, K_TOP, 1e-6, self.x, self.idx,
+                                            self.w, self.logits)
             if timing_events is not None:
                 timing_events[L][0].record()
             moe.moe_experts_decode(self.x, self.idx, self.w, self.ptrs[L], self.s, self.y, self.ws,
                                    self.st)
             if timing_events is not None:
                 timing_events[L][1].record()
-            if L + 1 < LAYERS:
-                moe.moe_rmsnorm_bf16(self.y, 1e-6, self.x)
 
     def capture(self, with_events: bool):
         torch = self.torch
@@ -373,7 +377,7 @@ def run_ours(args):
         wall = (time.perf_counter() - t0) / e_steps
         e2e = {"value": round(wl.expert_bytes_per_step() / wall / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4,
-               "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 240 per token"}
+               "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 96 per token"}
 
     prompt = None
     if not args.no_prompt:
@@ -411,11 +415,11 @@ def run_ours(args):
                    "expert_bytes_per_step": wl.expert_bytes_per_step(),
                    "l2": "inputs larger than L2: 1.33 GB of distinct expert records per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph of 239 kernel launches per step"},
+                   "launch": "CUDA graph, 2 kernels per layer (cluster router with RMS chaining; streaming expert pass), programmatic dependent launch"},
         "tokens_per_s": round(world * 1e3 / ms, 2),
         "hbm_frac": {"of_measured": round(value / world / peak, 4), "measured_gbs": peak,
                      "of_nominal_8000": round(value / world / 8000.0, 4)},
-        "roofline": {"bound": "hbm", "kernel": "moe_experts_decode (gate/up + down kernels)",
+        "roofline": {"bound": "hbm", "kernel": "moe_experts_decode: stream_kernel (TMA ring, gate/up + down in one launch)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "peak_kind": peak_kind + " (burst copy)",
                      "frac": round(achieved / peak, 4),

@@ -15,7 +15,10 @@
 // Activations (x, then h) sit in shared memory as float2 pairs laid out
 // [pair-of-elements][unit], so that 32 lanes reading 32 consecutive units
 // touch 32 consecutive 8-byte words (no bank conflicts).
+#include <algorithm>
+
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace {
 
@@ -230,192 +233,345 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(
 // Raises a kernel's dynamic shared-memory limit once (the attribute call is
 // not repeated, so later launches can be captured in a CUDA graph).
 // ---------------------------------------------------------------------------
-// Fused expert pass for a handful of pairs (T*k <= 64): one persistent
-// cooperative kernel runs gate/up + SwiGLU, a grid barrier, then down + the
-// weighted combine.  Before waiting at the barrier every warp issues the loads
-// of its first down row, so the down weights stream while the slowest gate/up
-// rows finish.  Scratch: h [P][I] (transposed float2 layout per pair) and two
-// barrier words.
+// Streaming expert pass (T*k <= 64): one CTA per SM.  One producer thread
+// walks this CTA's share of the selected records -- first the gate/up rows,
+// then the down rows -- and moves it with 1-D TMA bulk copies into a ring of
+// shared-memory slots, so every byte the CTA needs is requested at kernel
+// entry and the HBM pipe stays full.  Fifteen consumer warps compute from
+// shared memory: gate/up + SwiGLU rows -> h (global scratch), one grid
+// barrier, then down rows against h and the weighted combine, accumulated per
+// output row in a fixed order (bit-reproducible).  Slots that hold down rows
+// are filled while the consumers still work on gate/up.
 // ---------------------------------------------------------------------------
-struct FusedArgs {
+namespace st {
+
+constexpr int kThreads = 512;      // warps 0-14 consume, warp 15 produces
+constexpr int kCWarps = 15;
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kSlots = 6;
+constexpr int kSlotBytes = 24576;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct Args {
   const uint16_t* x;
   const int32_t* idx;
   const float* w;
   int T, k;
   const void* const* ptrs;
   int E, H, I;
-  float* hws;
-  unsigned* bar;
+  float* hws;      // [P][I] FP32, row-major
+  unsigned* bar;   // grid barrier words
   float* y;
-  int32_t* st;
+  int32_t* status;
 };
 
-constexpr int kFusedMaxPairs = 64;
+struct Geo {
+  int P, upr, updr, G, ch1, ch2;
+  long long r0, r1, q0, q1;  // this CTA's gate/up row pairs and output rows
+};
+
+__device__ __forceinline__ Geo geometry(const Args& a, int fmt) {
+  Geo g;
+  g.P = a.T * a.k;
+  g.upr = a.H >> 5;
+  g.updr = a.I >> 5;
+  g.G = fmt == MOE_FMT_NVFP4 ? 16 : 32;
+  const int b1 = 2 * (a.H / 2 + a.H / g.G);
+  g.ch1 = max(1, (kSlotBytes - 64) / b1);
+  g.ch2 = max(1, min(64, (kSlotBytes - 32) / (a.I / 2 + a.I / g.G)));
+  const long long R1 = (long long)g.P * a.I, R2 = (long long)a.T * a.H;
+  g.r0 = (long long)blockIdx.x * R1 / gridDim.x;
+  g.r1 = (long long)(blockIdx.x + 1) * R1 / gridDim.x;
+  g.q0 = (long long)blockIdx.x * R2 / gridDim.x;
+  g.q1 = (long long)(blockIdx.x + 1) * R2 / gridDim.x;
+  return g;
+}
+
+struct Win {  // 16-byte aligned window [lo, lo + bytes) around a byte range
+  size_t lo;
+  uint32_t bytes, delta;
+};
+__device__ __forceinline__ Win window(size_t start, size_t len) {
+  Win w;
+  w.lo = start & ~(size_t)15;
+  const size_t hi = (start + len + 15) & ~(size_t)15;
+  w.bytes = (uint32_t)(hi - w.lo);
+  w.delta = (uint32_t)(start - w.lo);
+  return w;
+}
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 2) decode_fused_kernel(FusedArgs a) {
-  extern __shared__ float2 act[];  // phase 1: x [T][16][H/32]; phase 2: h [P][16][I/32]
-  __shared__ const uint8_t* recs[kFusedMaxPairs];
-  __shared__ float wts[kFusedMaxPairs];
-  __shared__ int bar_ok;
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem;                                          // kSlots x kSlotBytes
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSlots * kSlotBytes);
+  uint64_t* empty = full + kSlots;
+  const uint8_t** recs = reinterpret_cast<const uint8_t**>(empty + kSlots);  // [64]
+  float* wts = reinterpret_cast<float*>(recs + 64);                          // [64]
+  int* flags = reinterpret_cast<int*>(wts + 64);                             // [0] abort, [1] barrier ok
+  float* yacc = reinterpret_cast<float*>(flags + 4);                         // [rows/CTA + 1]
   moe::pdl_launch_dependents();
-  moe::pdl_wait();
 
-  const int P = a.T * a.k;
-  const int H = a.H, I = a.I;
-  const int upr = H >> 5, updr = I >> 5;
+  const Geo g = geometry(a, FMT);
+  const int rows_cta = (int)(g.q1 - g.q0);
+  int* ybad = reinterpret_cast<int*>(yacc + rows_cta + 1);
+  float2* act = reinterpret_cast<float2*>(
+      (reinterpret_cast<uintptr_t>(ybad + rows_cta + 1) + 15) & ~(uintptr_t)15);
+  const moe::RecordOffsets o = moe::record_offsets(a.H, a.I, FMT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (kThreads / 32) + warp;
-  const int NW = gridDim.x * (kThreads / 32);
-  const moe::RecordOffsets o = moe::record_offsets(H, I, FMT);
-  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
-  constexpr int sstep = 32 / G;
 
-  // x of every token, transposed float2 layout per token
-  for (int h0 = threadIdx.x * 8; h0 < a.T * H; h0 += kThreads * 8) {
-    const int t = h0 / H, hh = h0 - t * H;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      moe::tc::mbar_init(&full[s], 1);
+      moe::tc::mbar_init(&empty[s], kCWarps);
+    }
+    flags[0] = 0;
+    moe::tc::mbar_fence_init();
+  }
+  for (int r = threadIdx.x; r <= rows_cta; r += kThreads) {
+    yacc[r] = 0.f;
+    ybad[r] = 0;
+  }
+  moe::pdl_wait();
+  if (threadIdx.x < g.P) {
+    recs[threadIdx.x] = checked_record(a.idx[threadIdx.x], a.E, a.ptrs,
+                                       blockIdx.x == 0 ? a.status : nullptr);
+    wts[threadIdx.x] = a.w[threadIdx.x];
+  }
+  // x of every token, transposed float2 layout [t][16][H/32]
+  for (int h0 = threadIdx.x * 8; h0 < a.T * a.H; h0 += kThreads * 8) {
+    const int t = h0 / a.H, hh = h0 - t * a.H;
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + h0));
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
     const int c = hh >> 5, pe0 = (hh & 31) >> 1;
-    float2* xt = act + (size_t)t * 16 * upr;
+    float2* xt = act + (size_t)t * 16 * g.upr;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      xt[(pe0 + i) * upr + c] =
+      xt[(pe0 + i) * g.upr + c] =
           make_float2(moe::bf16_bits_to_f32(wv[i] & 0xFFFFu), moe::bf16_bits_to_f32(wv[i] >> 16));
   }
-  if (threadIdx.x < P) {
-    recs[threadIdx.x] = checked_record(a.idx[threadIdx.x], a.E, a.ptrs,
-                                       blockIdx.x == 0 ? a.st : nullptr);
-    wts[threadIdx.x] = a.w[threadIdx.x];
-  }
   __syncthreads();
 
-  // ---- phase 1: one warp per (pair, intermediate row) ----
-  const int tasks1 = P * I;
-  for (int tau = gw; tau < tasks1; tau += NW) {
-    const int p = tau / I, i = tau - p * I;
-    const uint8_t* rec = recs[p];
-    float* hp = a.hws + (size_t)p * I;
-    const int hoff = 2 * (((i & 31) >> 1) * updr + (i >> 5)) + (i & 1);
-    if (!rec) {
-      if (lane == 0) hp[hoff] = __uint_as_float(0x7FC00000u);
-      continue;
-    }
-    const float2* xt = act + (size_t)(p / a.k) * 16 * upr;
-    const uint8_t* gcode = rec + o.gate + (size_t)i * (H / 2);
-    const uint8_t* ucode = rec + o.up + (size_t)i * (H / 2);
-    const uint8_t* gsc = rec + o.gate_s + (size_t)i * (H / G);
-    const uint8_t* usc = rec + o.up_s + (size_t)i * (H / G);
-    float gacc = 0.f, uacc = 0.f;
-    const int nunits = 2 * upr;
-    for (int base = 0; base < nunits; base += 32 * kUnitBatch) {
-      uint4 q[kUnitBatch];
-      uint32_t sb[kUnitBatch];
-#pragma unroll
-      for (int m = 0; m < kUnitBatch; ++m) {
-        const int u = base + lane + 32 * m;
-        if (u < nunits) {
-          const bool is_up = u >= upr;
-          const int c = is_up ? u - upr : u;
-          q[m] = moe::ldg_stream((is_up ? ucode : gcode) + 16 * c);
-          sb[m] = load_scale_bits<FMT>((is_up ? usc : gsc) + sstep * c);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < kUnitBatch; ++m) {
-        const int u = base + lane + 32 * m;
-        if (u < nunits) {
-          const bool is_up = u >= upr;
-          const int c = is_up ? u - upr : u;
-          const float d = unit_dot_col<FMT>(q[m], sb[m], xt + c, upr);
-          if (is_up) uacc += d;
-          else gacc += d;
-        }
-      }
-    }
-    gacc = moe::warp_sum(gacc);
-    uacc = moe::warp_sum(uacc);
-    if (lane == 0) hp[hoff] = gacc / (1.0f + expf(-gacc)) * uacc;
-  }
+  volatile int* abort_flag = flags;
+  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  constexpr int sstep = 32 / G;
 
-  // ---- prefetch the first unit batch of this warp's first down row ----
-  const int tasks2 = a.T * H;
-  const int nunits2 = a.k * updr;
-  uint4 q0[kUnitBatch];
-  uint32_t s0[kUnitBatch];
-  if (gw < tasks2) {
-    const int t = gw / H, n = gw - t * H;
-#pragma unroll
-    for (int m = 0; m < kUnitBatch; ++m) {
-      const int u = lane + 32 * m;
-      if (u < nunits2) {
-        const int j = u / updr, c = u - j * updr;
-        const uint8_t* rec = recs[t * a.k + j];
+  if (warp == kCWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int c = 0;
+      bool ok = true;
+      auto next_slot = [&](int& slot) -> bool {
+        slot = c % kSlots;
+        if (*abort_flag ||
+            !moe::tc::mbar_wait(&empty[slot], ((c / kSlots) & 1) ^ 1,
+                                moe::tc::globaltimer() + kWaitNs)) {
+          *abort_flag = 1;
+          moe::status_or(a.status, MOE_DEV_TIMEOUT);
+          return false;
+        }
+        return true;
+      };
+      for (long long r = g.r0; r < g.r1 && ok;) {
+        const int p = (int)(r / a.I), i0 = (int)(r - (long long)p * a.I);
+        const int n = (int)min((long long)g.ch1, min(g.r1 - r, (long long)(a.I - i0)));
+        int slot;
+        if (!(ok = next_slot(slot))) break;
+        const uint8_t* rec = recs[p];
+        const uint32_t base = moe::tc::smem_u32(ring + slot * kSlotBytes);
+        const uint32_t cb = (uint32_t)n * (a.H / 2);
+        const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
+        const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
+        const uint32_t total = rec ? 2 * cb + gw.bytes + uw.bytes : 0;
+        moe::tc::mbar_arrive_expect_tx(&full[slot], total);
         if (rec) {
-          q0[m] = moe::ldg_stream(rec + o.down + (size_t)n * (I / 2) + 16 * c);
-          s0[m] = load_scale_bits<FMT>(rec + o.down_s + (size_t)n * (I / G) + sstep * c);
+          moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i0 * (a.H / 2), cb, &full[slot]);
+          moe::tc::bulk_g2s(base + cb, rec + o.up + (size_t)i0 * (a.H / 2), cb, &full[slot]);
+          moe::tc::bulk_g2s(base + 2 * cb, rec + gw.lo, gw.bytes, &full[slot]);
+          moe::tc::bulk_g2s(base + 2 * cb + gw.bytes, rec + uw.lo, uw.bytes, &full[slot]);
         }
+        ++c;
+        r += n;
       }
+      for (long long q = g.q0; q < g.q1 && ok;) {
+        const int t = (int)(q / a.H), n0 = (int)(q - (long long)t * a.H);
+        const int nr = (int)min((long long)g.ch2, min(g.q1 - q, (long long)(a.H - n0)));
+        for (int j = 0; j < a.k && ok; ++j) {
+          int slot;
+          if (!(ok = next_slot(slot))) break;
+          const uint8_t* rec = recs[t * a.k + j];
+          const uint32_t base = moe::tc::smem_u32(ring + slot * kSlotBytes);
+          const uint32_t cb = (uint32_t)nr * (a.I / 2);
+          const Win dw = window(o.down_s + (size_t)n0 * (a.I / G), (size_t)nr * (a.I / G));
+          moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? cb + dw.bytes : 0);
+          if (rec) {
+            moe::tc::bulk_g2s(base, rec + o.down + (size_t)n0 * (a.I / 2), cb, &full[slot]);
+            moe::tc::bulk_g2s(base + cb, rec + dw.lo, dw.bytes, &full[slot]);
+          }
+          ++c;
+        }
+        q += nr;
+      }
+      // every issued copy must land before this CTA may exit
+      for (int cc = max(0, c - kSlots); cc < c; ++cc)
+        moe::tc::mbar_wait(&full[cc % kSlots], (cc / kSlots) & 1, moe::tc::globaltimer() + kWaitNs);
     }
-  }
-
-  if (!moe::grid_barrier(a.bar, gridDim.x, moe::global_ns() + 2000000000ull, &bar_ok)) {
-    if (threadIdx.x == 0) moe::status_or(a.st, MOE_DEV_TIMEOUT);
-    return;
-  }
-
-  // ---- stage h of every pair (L2 reads; written by other CTAs) ----
-  {
-    const float4* src = reinterpret_cast<const float4*>(a.hws);
-    float4* dst = reinterpret_cast<float4*>(act);
-    const int n16 = P * I / 4;
-    for (int i = threadIdx.x; i < n16; i += kThreads) dst[i] = __ldcg(src + i);
+  } else {
+    // ------------------------------------------------------------ consumers
+    int c = 0;
+    bool ok = true;
+    auto take = [&](int& slot) -> bool {
+      slot = c % kSlots;
+      if (*abort_flag ||
+          !moe::tc::mbar_wait(&full[slot], (c / kSlots) & 1, moe::tc::globaltimer() + kWaitNs)) {
+        *abort_flag = 1;
+        moe::status_or(a.status, MOE_DEV_TIMEOUT);
+        return false;
+      }
+      return true;
+    };
+    auto release = [&](int slot) {
+      __syncwarp();
+      if (lane == 0) moe::tc::mbar_arrive(&empty[slot]);
+      ++c;
+    };
+    // gate/up + SwiGLU
+    for (long long r = g.r0; r < g.r1 && ok;) {
+      const int p = (int)(r / a.I), i0 = (int)(r - (long long)p * a.I);
+      const int n = (int)min((long long)g.ch1, min(g.r1 - r, (long long)(a.I - i0)));
+      int slot;
+      if (!(ok = take(slot))) break;
+      const uint8_t* base = ring + slot * kSlotBytes;
+      const uint8_t* rec = recs[p];
+      const uint32_t cb = (uint32_t)n * (a.H / 2);
+      const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
+      const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
+      const float2* xt = act + (size_t)(p / a.k) * 16 * g.upr;
+      for (int rr = warp; rr < n; rr += kCWarps) {
+        float hv = __uint_as_float(0x7FC00000u);
+        if (rec) {
+          const uint8_t* gcode = base + (size_t)rr * (a.H / 2);
+          const uint8_t* ucode = base + cb + (size_t)rr * (a.H / 2);
+          const uint8_t* gsc = base + 2 * cb + gw.delta + (size_t)rr * (a.H / G);
+          const uint8_t* usc = base + 2 * cb + gw.bytes + uw.delta + (size_t)rr * (a.H / G);
+          float gacc = 0.f, uacc = 0.f;
+          for (int u = lane; u < 2 * g.upr; u += 32) {
+            const bool is_up = u >= g.upr;
+            const int cix = is_up ? u - g.upr : u;
+            const uint4 q = *reinterpret_cast<const uint4*>((is_up ? ucode : gcode) + 16 * cix);
+            const uint8_t* sp = (is_up ? usc : gsc) + sstep * cix;
+            const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8)
+                                                     : (uint32_t)sp[0];
+            const float d = unit_dot_col<FMT>(q, sb, xt + cix, g.upr);
+            if (is_up) uacc += d;
+            else gacc += d;
+          }
+          gacc = moe::warp_sum(gacc);
+          uacc = moe::warp_sum(uacc);
+          hv = gacc / (1.0f + expf(-gacc)) * uacc;
+        }
+        if (lane == 0) a.hws[(size_t)p * a.I + i0 + rr] = hv;
+      }
+      release(slot);
+      r += n;
+    }
+    // grid barrier among the consumer threads of every CTA
+    moe::tc::named_sync(1, kCThreads);
+    if (threadIdx.x == 0) {
+      int good = ok && !*abort_flag;
+      if (good) {
+        const unsigned e0 = moe::ld_acquire_gpu(a.bar + 1);
+        __threadfence();
+        const unsigned old = atomicAdd(a.bar, 1u);
+        if (old == gridDim.x - 1) {
+          atomicExch(a.bar, 0u);
+          __threadfence();
+          atomicAdd(a.bar + 1, 1u);
+        } else {
+          const uint64_t dl = moe::global_ns() + kWaitNs;
+          while (moe::ld_acquire_gpu(a.bar + 1) == e0) {
+            if (moe::global_ns() > dl) {
+              good = 0;
+              break;
+            }
+          }
+        }
+        __threadfence();
+      }
+      if (!good) {
+        *abort_flag = 1;
+        moe::status_or(a.status, MOE_DEV_TIMEOUT);
+      }
+      flags[1] = good;
+    }
+    moe::tc::named_sync(1, kCThreads);
+    ok = flags[1] != 0;
+    if (ok && rows_cta > 0) {
+      // stage h of the tokens this CTA's output rows belong to
+      const int t_lo = (int)(g.q0 / a.H), t_hi = (int)((g.q1 - 1) / a.H);
+      const int n_el = (t_hi - t_lo + 1) * a.k * a.I;
+      const float* src = a.hws + (size_t)t_lo * a.k * a.I;
+      for (int e = threadIdx.x; e < n_el; e += kCThreads) {
+        const int pj = e / a.I, i = e - pj * a.I;  // pair relative to t_lo*k
+        const float v = __ldcg(src + e);
+        float* dst = reinterpret_cast<float*>(act + (size_t)pj * 16 * g.updr);
+        dst[2 * (((i & 31) >> 1) * g.updr + (i >> 5)) + (i & 1)] = v;
+      }
+      moe::tc::named_sync(1, kCThreads);
+      // down + weighted combine
+      for (long long q = g.q0; q < g.q1 && ok;) {
+        const int t = (int)(q / a.H), n0 = (int)(q - (long long)t * a.H);
+        const int nr = (int)min((long long)g.ch2, min(g.q1 - q, (long long)(a.H - n0)));
+        for (int j = 0; j < a.k && ok; ++j) {
+          int slot;
+          if (!(ok = take(slot))) break;
+          const uint8_t* base = ring + slot * kSlotBytes;
+          const int pj = t * a.k + j;
+          const uint8_t* rec = recs[pj];
+          const uint32_t cb = (uint32_t)nr * (a.I / 2);
+          const Win dw = window(o.down_s + (size_t)n0 * (a.I / G), (size_t)nr * (a.I / G));
+          const float2* hcol = act + (size_t)(pj - t_lo * a.k) * 16 * g.updr;
+          for (int rr = warp; rr < nr; rr += kCWarps) {
+            const int yi = (int)(q - g.q0) + rr;
+            if (!rec) {
+              if (lane == 0) ybad[yi] = 1;
+              continue;
+            }
+            const uint8_t* dcode = base + (size_t)rr * (a.I / 2);
+            const uint8_t* dsc = base + cb + dw.delta + (size_t)rr * (a.I / G);
+            float acc = 0.f;
+            for (int u = lane; u < g.updr; u += 32) {
+              const uint4 qv = *reinterpret_cast<const uint4*>(dcode + 16 * u);
+              const uint8_t* sp = dsc + sstep * u;
+              const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8)
+                                                       : (uint32_t)sp[0];
+              acc += unit_dot_col<FMT>(qv, sb, hcol + u, g.updr);
+            }
+            acc = moe::warp_sum(acc);
+            if (lane == 0) yacc[yi] += wts[pj] * acc;
+          }
+          release(slot);
+        }
+        q += nr;
+      }
+      moe::tc::named_sync(1, kCThreads);
+      for (int r = threadIdx.x; r < rows_cta; r += kCThreads)
+        a.y[g.q0 + r] = (ybad[r] || !ok) ? __uint_as_float(0x7FC00000u) : yacc[r];
+    }
   }
   __syncthreads();
-
-  // ---- phase 2: one warp per (token, output row) ----
-  for (int tau = gw; tau < tasks2; tau += NW) {
-    const int t = tau / H, n = tau - t * H;
-    float acc = 0.f;
-    bool bad = false;
-    for (int base = 0; base < nunits2; base += 32 * kUnitBatch) {
-      uint4 q[kUnitBatch];
-      uint32_t sb[kUnitBatch];
-      const bool first = (tau == gw) && (base == 0);
-#pragma unroll
-      for (int m = 0; m < kUnitBatch; ++m) {
-        const int u = base + lane + 32 * m;
-        if (u < nunits2) {
-          const int j = u / updr, c = u - j * updr;
-          const uint8_t* rec = recs[t * a.k + j];
-          if (first) {
-            q[m] = q0[m];
-            sb[m] = s0[m];
-          } else if (rec) {
-            q[m] = moe::ldg_stream(rec + o.down + (size_t)n * (I / 2) + 16 * c);
-            sb[m] = load_scale_bits<FMT>(rec + o.down_s + (size_t)n * (I / G) + sstep * c);
-          }
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < kUnitBatch; ++m) {
-        const int u = base + lane + 32 * m;
-        if (u < nunits2) {
-          const int j = u / updr, c = u - j * updr;
-          const int pj = t * a.k + j;
-          if (recs[pj]) {
-            acc += wts[pj] * unit_dot_col<FMT>(q[m], sb[m], act + (size_t)pj * 16 * updr + c, updr);
-          } else {
-            bad = true;
-          }
-        }
-      }
-    }
-    acc = moe::warp_sum(acc);
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) a.y[(size_t)t * H + n] = bad ? __uint_as_float(0x7FC00000u) : acc;
-  }
 }
+
+size_t smem_bytes(int T, int k, int H, int I, int sms) {
+  const long long R2 = (long long)T * H;
+  const long long rows = (R2 + sms - 1) / sms + 1;
+  const long long ntok = std::min<long long>(T, rows / H + 2);
+  const size_t act = std::max<size_t>((size_t)T * H * 4, (size_t)ntok * k * I * 4);
+  return (size_t)kSlots * kSlotBytes + 2 * kSlots * 8 + 64 * 8 + 64 * 4 + 16 +
+         (size_t)(rows + 1) * 8 + 16 + act;
+}
+
+}  // namespace st
 
 template <typename K>
 bool ensure_smem(K kernel, size_t bytes, size_t* granted) {
@@ -444,32 +600,43 @@ int launch_decode(const uint16_t* x, const int32_t* idx, const float* w, int T, 
   return moe::launch_status();
 }
 
-bool fused_fits(int T, int k, int H, int I) {
-  const long long P = (long long)T * k;
-  return P <= kFusedMaxPairs && (long long)T * H * 4 <= 96 * 1024 &&
-         P * I * 4 <= 96 * 1024;
+int stream_smem_limit() {
+  static int limit = 0;
+  if (limit == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      limit = 0;
+  }
+  return limit;
 }
 
-size_t fused_smem(int T, int k, int H, int I) {
-  const size_t a = (size_t)T * H * 4, b = (size_t)T * k * I * 4;
-  return a > b ? a : b;
+int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 0;
+  }
+  return sms;
+}
+
+// The streaming kernel takes T*k <= 64 pairs whose shared-memory plan fits.
+bool stream_fits(int T, int k, int H, int I) {
+  const int sms = sm_count();
+  if (sms <= 0 || (long long)T * k > 64) return false;
+  return st::smem_bytes(T, k, H, I, sms) + 1024 <= (size_t)stream_smem_limit();
 }
 
 template <int FMT>
-int launch_fused(const FusedArgs& fa, cudaStream_t stream) {
-  const size_t smem = fused_smem(fa.T, fa.k, fa.H, fa.I);
+int launch_stream(const st::Args& sa, cudaStream_t stream) {
+  const int sms = sm_count();
+  const size_t smem = st::smem_bytes(sa.T, sa.k, sa.H, sa.I, sms);
   static size_t granted = 0;
-  if (!ensure_smem(decode_fused_kernel<FMT>, smem, &granted)) return MOE_ERR_CUDA;
-  int dev = 0, sms = 0, occ = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_fused_kernel<FMT>, kThreads, smem) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
-  occ = occ < 1 ? 1 : (occ > 3 ? 3 : occ);
-  // Grid = resident capacity, so every CTA is on an SM together (the grid
-  // barrier needs that); its waits are bounded in any case.
-  return moe::launch_pdl(decode_fused_kernel<FMT>, dim3(sms * occ), dim3(kThreads), smem, stream, fa);
+  if (!ensure_smem(st::stream_kernel<FMT>, smem, &granted)) return MOE_ERR_CUDA;
+  // one CTA per SM: all CTAs are resident together, as the grid barrier needs
+  return moe::launch_pdl(st::stream_kernel<FMT>, dim3(sms), dim3(st::kThreads), smem, stream, sa);
 }
 
 }  // namespace
@@ -494,24 +661,24 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
   if (!moe::aligned16(x_bf16) || !moe::aligned16(workspace)) return MOE_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
   float* hws = reinterpret_cast<float*>(workspace);
-  if (fused_fits(T, k, s.hidden, s.inter)) {
-    FusedArgs fa;
-    fa.x = x_bf16;
-    fa.idx = idx;
-    fa.w = weights;
-    fa.T = T;
-    fa.k = k;
-    fa.ptrs = expert_ptrs;
-    fa.E = E;
-    fa.H = s.hidden;
-    fa.I = s.inter;
-    fa.hws = hws;
-    fa.bar = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(workspace) +
+  if (stream_fits(T, k, s.hidden, s.inter)) {
+    st::Args sa;
+    sa.x = x_bf16;
+    sa.idx = idx;
+    sa.w = weights;
+    sa.T = T;
+    sa.k = k;
+    sa.ptrs = expert_ptrs;
+    sa.E = E;
+    sa.H = s.hidden;
+    sa.I = s.inter;
+    sa.hws = hws;
+    sa.bar = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(workspace) +
                                          (size_t)T * k * s.inter * sizeof(float));
-    fa.y = y;
-    fa.st = dev_status;
-    return s.format == MOE_FMT_NVFP4 ? launch_fused<MOE_FMT_NVFP4>(fa, st)
-                                     : launch_fused<MOE_FMT_MXFP4>(fa, st);
+    sa.y = y;
+    sa.status = dev_status;
+    return s.format == MOE_FMT_NVFP4 ? launch_stream<MOE_FMT_NVFP4>(sa, st)
+                                     : launch_stream<MOE_FMT_MXFP4>(sa, st);
   }
   if (s.format == MOE_FMT_NVFP4)
     return launch_decode<MOE_FMT_NVFP4>(x_bf16, idx, weights, T, k, expert_ptrs, E, s.hidden,

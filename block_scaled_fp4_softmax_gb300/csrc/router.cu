@@ -7,6 +7,7 @@
 // waits on the router's answer, so routing stays on the device here and no
 // index ever travels to the host.
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace {
 
@@ -209,6 +210,251 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
   for (int i = threadIdx.x; i < H; i += 256) x[(size_t)t * H + i] = f64_to_bf16_rn((double)yr[i] * inv);
 }
 
+// ---------------------------------------------------------------------------
+// Small-T router in one launch: a cluster of kCl CTAs.  Each CTA pulls its
+// contiguous slice of W_r rows into shared memory with one bulk copy issued
+// before it waits on the previous kernel (the weights never depend on it),
+// builds x (from x_bf16, or as RMS chaining of the previous layer's y), and
+// computes its experts' logits in the fixed order.  After a cluster barrier,
+// CTA 0 reads every CTA's logits through distributed shared memory and runs
+// the top-k + softmax per token.
+// ---------------------------------------------------------------------------
+constexpr int kCl = 16;
+constexpr int kClThreads = 256;
+constexpr int kClMaxT = 4;
+
+struct ClusterArgs {
+  const uint16_t* x;    // [T, H] BF16, or NULL when y_prev is given
+  const float* y_prev;  // [T, H] FP32 to RMS-normalise, or NULL
+  double eps;
+  uint16_t* x_out;      // written by CTA 0 when y_prev is given (may be NULL otherwise)
+  const uint16_t* wr;
+  const float* bias;
+  int T, H, E, k, epc;  // experts per CTA
+  int32_t* idx;
+  float* weights;
+  float* logits;
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ float dsmem_ld_f32(const float* local_addr, uint32_t rank) {
+  uint32_t a = moe::tc::smem_u32(local_addr), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kClThreads) router_cluster_kernel(ClusterArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(sm);
+  double* part = reinterpret_cast<double*>(sm + 16);                 // [256]
+  float* lg = reinterpret_cast<float*>(sm + 16 + 256 * 8);           // [kClMaxT][epc]
+  uint16_t* xs = reinterpret_cast<uint16_t*>(lg + kClMaxT * a.epc);  // [T][H] BF16
+  uint16_t* ws = reinterpret_cast<uint16_t*>(
+      (reinterpret_cast<uintptr_t>(xs + (size_t)a.T * a.H) + 127) & ~(uintptr_t)127);  // [epc][H]
+  const uint32_t rank = cluster_ctarank();
+  const int e0 = (int)rank * a.epc;
+  const int ne = max(0, min(a.epc, a.E - e0));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool wok = true;
+
+  if (threadIdx.x == 0) {
+    moe::tc::mbar_init(wbar, 1);
+    moe::tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)ne * a.H * 2;
+    moe::tc::mbar_arrive_expect_tx(wbar, bytes);
+    if (bytes) moe::tc::bulk_g2s(moe::tc::smem_u32(ws), a.wr + (size_t)e0 * a.H, bytes, wbar);
+  }
+  moe::pdl_launch_dependents();
+  moe::pdl_wait();
+
+  // x for every token
+  for (int t = 0; t < a.T; ++t) {
+    if (a.y_prev) {
+      const float* yr = a.y_prev + (size_t)t * a.H;
+      double acc = 0.0;
+      for (int i = threadIdx.x; i < a.H; i += kClThreads) {
+        const double v = (double)yr[i];
+        acc = fma(v, v, acc);
+      }
+      part[threadIdx.x] = acc;
+      __syncthreads();
+      for (int w = kClThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+      }
+      const double inv = 1.0 / sqrt(part[0] / (double)a.H + a.eps);
+      for (int i = threadIdx.x; i < a.H; i += kClThreads) {
+        const uint16_t b = f64_to_bf16_rn((double)yr[i] * inv);
+        xs[(size_t)t * a.H + i] = b;
+        if (rank == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = b;
+      }
+      __syncthreads();
+    } else {
+      for (int i = threadIdx.x * 8; i < a.H; i += kClThreads * 8)
+        *reinterpret_cast<uint4*>(xs + (size_t)t * a.H + i) =
+            __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + i));
+    }
+  }
+  __syncthreads();
+  if (!moe::tc::mbar_wait(wbar, 0, moe::global_ns() + 2000000000ull)) wok = false;
+
+  // logits: warp -> expert, lane j -> chunks j, j+32, ... (fixed order)
+  const int nchunk = a.H >> 3;
+  for (int q = warp; q < ne; q += kClThreads / 32) {
+    float acc[kClMaxT];
+#pragma unroll
+    for (int t = 0; t < kClMaxT; ++t) acc[t] = 0.0f;
+    const uint16_t* wrow = ws + (size_t)q * a.H;
+    for (int c = lane; c < nchunk; c += 32) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(wrow + 8 * c);
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int t = 0; t < kClMaxT; ++t) {
+        if (t < a.T) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * a.H + 8 * c);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float xf = moe::bf16_bits_to_f32((i & 1) ? (xw[i >> 1] >> 16) : (xw[i >> 1] & 0xFFFFu));
+            const float wf = moe::bf16_bits_to_f32((i & 1) ? (ww[i >> 1] >> 16) : (ww[i >> 1] & 0xFFFFu));
+            acc[t] = __fmaf_rn(xf, wf, acc[t]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kClMaxT; ++t) {
+      float v = acc[t];
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
+      if (t < a.T && lane == 0) {
+        const int e = e0 + q;
+        if (a.bias) v = __fadd_rn(v, a.bias[e]);
+        if (!wok) v = __uint_as_float(0x7FC00000u);
+        lg[t * a.epc + q] = v;
+        a.logits[(size_t)t * a.E + e] = v;
+      }
+    }
+  }
+  cluster_sync_all();
+
+  // top-k in CTA 0, one warp per token, candidates read over DSMEM
+  if (rank == 0 && warp < a.T) {
+    const int t = warp;
+    unsigned long long cand[32];
+    const int epl = (a.E + 31) / 32;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      cand[i] = 0ull;
+      const int e = lane + 32 * i;
+      if (i < epl && e < a.E) {
+        const uint32_t owner = (uint32_t)(e / a.epc);
+        const float v = dsmem_ld_f32(lg + t * a.epc + (e - (int)owner * a.epc), owner);
+        cand[i] = ((unsigned long long)ordered_key(v) << 32) | (unsigned long long)(~(uint32_t)e);
+      }
+    }
+    int my_e = 0;
+    float my_l = 0.0f;
+    for (int r = 0; r < a.k; ++r) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) best = cand[i] > best ? cand[i] : best;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
+        best = o > best ? o : best;
+      }
+      const int e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
+      if ((e & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i == (e >> 5)) cand[i] = 0ull;
+      }
+      if (lane == r) {
+        my_e = e;
+        my_l = key_to_float((uint32_t)(best >> 32));
+      }
+    }
+    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+    const float ex = lane < a.k ? expf(my_l - l0) : 0.0f;
+    const float sum = moe::warp_sum(ex);
+    if (lane < a.k) {
+      a.idx[(size_t)t * a.k + lane] = my_e;
+      a.weights[(size_t)t * a.k + lane] = __fdiv_rn(ex, sum);
+    }
+  }
+  cluster_sync_all();  // keep every CTA's shared memory alive until CTA 0 is done
+}
+
+size_t cluster_smem(int T, int H, int epc) {
+  return 16 + 256 * 8 + (size_t)kClMaxT * epc * 4 + (size_t)T * H * 2 + 128 + (size_t)epc * H * 2;
+}
+
+int cluster_smem_limit() {
+  static int limit = -1;
+  if (limit < 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      limit = 0;
+  }
+  return limit;
+}
+
+bool cluster_fits(int T, int H, int E) {
+  const int epc = (E + kCl - 1) / kCl;
+  return T >= 1 && T <= kClMaxT && E <= 1024 && H % 8 == 0 &&
+         cluster_smem(T, H, epc) <= (size_t)cluster_smem_limit();
+}
+
+int launch_cluster_router(const ClusterArgs& a0, cudaStream_t st) {
+  ClusterArgs a = a0;
+  a.epc = (a.E + kCl - 1) / kCl;
+  const size_t smem = cluster_smem(a.T, a.H, a.epc);
+  static size_t granted = 0;
+  static bool nonportable = false;
+  if (!nonportable) {
+    if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    nonportable = true;
+  }
+  if (smem > granted) {
+    if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    granted = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCl);
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, router_cluster_kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, const float* bias,
@@ -220,6 +466,20 @@ extern "C" int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, 
   if (!moe::aligned16(x_bf16) || !moe::aligned16(wr_bf16)) return MOE_ERR_ALIGNMENT;
   if (T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
+  if (cluster_fits(T, H, E)) {
+    ClusterArgs a = {};
+    a.x = x_bf16;
+    a.wr = wr_bf16;
+    a.bias = bias;
+    a.T = T;
+    a.H = H;
+    a.E = E;
+    a.k = k;
+    a.idx = idx;
+    a.weights = weights;
+    a.logits = logits;
+    return launch_cluster_router(a, st);
+  }
   const int threads = 256;
   int rc;
   if (T < 4) {
@@ -249,4 +509,36 @@ extern "C" int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16
   if (T == 0) return MOE_OK;
   return moe::launch_pdl(rmsnorm_bf16_kernel, dim3(T), dim3(256), 0, (cudaStream_t)stream, y, H,
                          eps, x_bf16);
+}
+
+extern "C" int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps,
+                                       uint16_t* x_out, const uint16_t* wr_bf16, const float* bias,
+                                       int E, int k, int32_t* idx, float* weights, float* logits,
+                                       void* stream) {
+  if (!y_prev || !x_out || !wr_bf16 || !idx || !weights || !logits) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || k > 32 || !(eps >= 0.0))
+    return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (!moe::aligned16(wr_bf16) || !moe::aligned16(x_out)) return MOE_ERR_ALIGNMENT;
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cluster_fits(T, H, E)) {
+    ClusterArgs a = {};
+    a.y_prev = y_prev;
+    a.eps = eps;
+    a.x_out = x_out;
+    a.wr = wr_bf16;
+    a.bias = bias;
+    a.T = T;
+    a.H = H;
+    a.E = E;
+    a.k = k;
+    a.idx = idx;
+    a.weights = weights;
+    a.logits = logits;
+    return launch_cluster_router(a, st);
+  }
+  int rc = moe_rmsnorm_bf16(y_prev, T, H, eps, x_out, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_router_topk(x_out, wr_bf16, bias, T, H, E, k, idx, weights, logits, stream);
 }

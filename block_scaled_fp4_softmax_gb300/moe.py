@@ -31,6 +31,7 @@ EXPORTS = (
     "fp4_pack_expert",
     "moe_router_topk",
     "moe_rmsnorm_bf16",
+    "moe_rmsnorm_router_topk",
     "moe_experts_decode_workspace",
     "moe_experts_decode",
     "moe_bucket_workspace",
@@ -65,6 +66,8 @@ _SIGS = {
     "fp4_pack_expert": (_i, [_vp, _vp, _vp, ExpertShape, _vp, _vp]),
     "moe_router_topk": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "moe_rmsnorm_bf16": (_i, [_vp, _i, _i, ctypes.c_double, _vp, _vp]),
+    "moe_rmsnorm_router_topk": (_i, [_vp, _i, _i, ctypes.c_double, _vp, _vp, _vp, _i, _i, _vp, _vp,
+                                     _vp, _vp]),
     "moe_experts_decode_workspace": (_sz, [_i, _i, ExpertShape]),
     "moe_experts_decode": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _sz,
                                 _vp, _vp]),
@@ -185,6 +188,30 @@ def moe_rmsnorm_bf16(y, eps: float = 1e-6, x=None, stream=None):
     _check(load().moe_rmsnorm_bf16(_ptr(y), T, H, float(eps), _ptr(x), _stream(stream)),
            "moe_rmsnorm_bf16")
     return x
+
+
+def moe_rmsnorm_router_topk(y_prev, wr, bias, k: int, eps: float = 1e-6, x_out=None, idx=None,
+                            weights=None, logits=None, stream=None):
+    """RMS chaining of y_prev fused with the router; returns (x, idx, weights, logits)."""
+    _cuda(y_prev, "y_prev", torch.float32)
+    _cuda(wr, "wr", torch.bfloat16)
+    if bias is not None:
+        _cuda(bias, "bias", torch.float32)
+    T, H = y_prev.shape
+    E = wr.shape[0]
+    dev = y_prev.device
+    if x_out is None:
+        x_out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if idx is None:
+        idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(T, k, dtype=torch.float32, device=dev)
+    if logits is None:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    _check(load().moe_rmsnorm_router_topk(_ptr(y_prev), T, H, float(eps), _ptr(x_out), _ptr(wr),
+                                          _ptr(bias), E, k, _ptr(idx), _ptr(weights), _ptr(logits),
+                                          _stream(stream)), "moe_rmsnorm_router_topk")
+    return x_out, idx, weights, logits
 
 
 def moe_experts_decode_workspace(T: int, k: int, s: ExpertShape) -> int:

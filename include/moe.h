@@ -123,6 +123,14 @@ int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, const float
 int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16_t* x_bf16,
                      void* stream);
 
+/* Layer chaining fused with the router, for stacked decode: x = RMS chaining
+ * of y_prev exactly as moe_rmsnorm_bf16 computes it (written to x_out), then
+ * moe_router_topk on that x.  Same outputs, same limits; for T <= 4 with a
+ * router slice that fits in shared memory it is a single cluster launch. */
+int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps, uint16_t* x_out,
+                            const uint16_t* wr_bf16, const float* bias, int E, int k,
+                            int32_t* idx, float* weights, float* logits, void* stream);
+
 /* Workspace bytes moe_experts_decode needs for T tokens, k experts each.
  * The workspace holds the FP32 SwiGLU intermediate and, at its end, the words
  * of a grid barrier: it must be zero-filled before its first use.  Every call

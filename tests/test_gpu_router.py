@@ -86,3 +86,20 @@ def test_router_repeatable():
         out = moe.moe_router_topk(x, wr, None, 10)
         for a, b in zip(ref, out):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("T,E,H,k", [(1, 512, 2560, 10), (1, 384, 4096, 6), (3, 64, 2560, 10),
+                                     (6, 512, 2560, 10)])
+def test_rmsnorm_router_fused_exact(T, E, H, k):
+    g = torch.Generator().manual_seed(T * E)
+    y = torch.randn(T, H, generator=g) * 0.05
+    wr = synth.router_weights(E, H, seed=T + E)
+    x, idx, w, logits = moe.moe_rmsnorm_router_topk(y.cuda(), wr.cuda(), None, k, eps=1e-6)
+    torch.cuda.synchronize()
+    want_x = O.rmsnorm_bf16(y.numpy(), 1e-6)
+    assert np.array_equal(bits(x), want_x)
+    want_l = O.router_logits(want_x, bits(wr))
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), want_l.view(np.uint32))
+    want_i, want_w = O.topk_softmax(want_l, k)
+    assert np.array_equal(idx.cpu().numpy(), want_i)
+    assert np.allclose(w.cpu().numpy(), want_w, rtol=1e-6, atol=0)

@@ -17,11 +17,12 @@
 // One persistent CTA per SM walks a static list of tiles (expert, token tile,
 // weight-row tile).  Warp roles:
 //   warp 0          TMEM allocation; lane 0 issues tcgen05.mma and commits
-//   warps 1-3       gather B rows (tokens' x or h) with cp.async into
-//                   128-byte-swizzled shared memory
-//   warps 4-11      load FP4 codes + block scales, convert e2m1 x scale to BF16
+//   warps 1-2       gather B rows (tokens' x or h) with cp.async into
+//                   128-byte-swizzled shared memory; each thread owns two rows
+//                   and resolves their source addresses once per tile
+//   warps 3-10      load FP4 codes + block scales, convert e2m1 x scale to BF16
 //                   (exact) and store the A tile, 128-byte swizzled
-//   warps 12-15     epilogue: tcgen05.ld from TMEM, SwiGLU or weighted combine
+//   warps 11-14     epilogue: tcgen05.ld from TMEM, SwiGLU or weighted combine
 // Every mbarrier wait is bounded by the global timer; a wait that runs out sets
 // MOE_DEV_TIMEOUT and the CTA drains and exits.
 #include "common.cuh"
@@ -34,10 +35,11 @@ using namespace moe::tc;
 constexpr int BM = 128;      // weight rows per tile (MMA M)
 constexpr int BK = 64;       // K elements per stage (128 bytes of BF16)
 constexpr int BN = 128;      // max tokens per tile (MMA N, padded to 16)
-constexpr int kThreads = 512;
-constexpr int kLoaderThreads = 96;     // warps 1-3
-constexpr int kProducerThreads = 256;  // warps 4-11
-constexpr int kEpiThreads = 128;       // warps 12-15
+constexpr int kThreads = 480;
+constexpr int kLoaderThreads = 64;     // warps 1-2: two B rows each
+constexpr int kProducerThreads = 256;  // warps 3-10
+constexpr int kEpiThreads = 128;       // warps 11-14
+constexpr int kProdWarp0 = 3, kEpiWarp0 = 11;
 constexpr int kPrefetch = 4;           // k-steps of FP4 codes a producer holds in registers
 constexpr int kLoaderDepth = 2;        // cp.async groups a loader keeps in flight
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
@@ -63,7 +65,8 @@ struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;             // 16 KB
   static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = NA * BN;               // 256 or 128
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/ +
+                                 2 * BN * 8 /*per-column token and weight, two tiles*/;
 };
 
 struct TileInfo {
@@ -137,8 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tab_ready = drain + 1;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tab_ready + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* col_tok = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);  // [2][BN]
+  float* col_w = reinterpret_cast<float*>(col_tok + 2 * BN);                        // [2][BN]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = PHASE == 0 ? a.H : a.I;  // contraction length
@@ -156,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiThreads);
     mbar_init(drain, 1);
+    mbar_init(&tab_ready[0], kEpiThreads);
+    mbar_init(&tab_ready[1], kEpiThreads);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -215,40 +223,50 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
       mbar_wait(drain, 0, globaltimer() + kWaitNs);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < kProdWarp0) {
     // ------------------------------------------------------------- B loaders
-    const int lt_id = threadIdx.x - 32;  // 0..95
-    int pending = 0;                      // steps issued but not yet signalled
+    const int lid = threadIdx.x - 32;  // 0..63; rows lid and lid + 64
+    int pending = 0;                    // steps issued but not yet signalled
     int cur_tile = -1;
-    TileInfo ti{};
+    const uint16_t* src_row[2] = {a.x, a.x};
+    uint32_t src_bytes[2] = {0, 0};
     for (int gs = 0; gs < my_steps; ++gs) {
       const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
       const int stage = gs % C::STAGES;
       if (lt != cur_tile) {
         cur_tile = lt;
-        ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
+        const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
+        const int n_rows = max(16, (ti.count + 15) & ~15);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = lid + 64 * h;
+          src_bytes[h] = n < ti.count ? 16u : 0u;
+          src_row[h] = a.x;
+          if (n < ti.count) {
+            if (PHASE == 0) {
+              const int p = __ldg(a.pairs + ti.row0 + n);
+              src_row[h] = a.x + (size_t)(p / a.k) * a.H;
+            } else {
+              src_row[h] = a.hbuf + (size_t)(ti.row0 + n) * a.I;
+            }
+          }
+          if (n >= n_rows) src_bytes[h] = 0xFFFFFFFFu;  // row not part of this tile's MMA
+        }
       }
       if (*abort_flag || !mbar_wait(&empty[stage], ((gs / C::STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
         fail();
         break;
       }
       const uint32_t b_addr = smem_u32(smem + stage * C::STAGE_BYTES + C::NA * C::A_BYTES);
-      const int n_rows = max(16, (ti.count + 15) & ~15);
-      for (int c = lt_id; c < n_rows * 8; c += kLoaderThreads) {
-        const int n = c >> 3, ch = c & 7;
-        const uint32_t dst = b_addr + n * 128 + ((ch ^ (n & 7)) << 4);
-        const uint16_t* src = a.x;
-        uint32_t bytes = 0;
-        if (n < ti.count) {
-          if (PHASE == 0) {
-            const int p = __ldg(a.pairs + ti.row0 + n);
-            src = a.x + (size_t)(p / a.k) * a.H + ks * BK + ch * 8;
-          } else {
-            src = a.hbuf + (size_t)(ti.row0 + n) * a.I + ks * BK + ch * 8;
-          }
-          bytes = 16;
-        }
-        cp_async16(dst, src, bytes);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (src_bytes[h] == 0xFFFFFFFFu) continue;
+        const int n = lid + 64 * h;
+        const uint16_t* src = src_row[h] + (src_bytes[h] ? ks * BK : 0);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          cp_async16(b_addr + n * 128 + ((ch ^ (n & 7)) << 4), src + (src_bytes[h] ? ch * 8 : 0),
+                     src_bytes[h]);
       }
       cp_async_commit();
       ++pending;
@@ -264,21 +282,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     if (!*abort_flag) {
       for (int gs = my_steps - pending; gs < my_steps; ++gs) mbar_arrive(&full[gs % C::STAGES]);
     }
-  } else if (warp < 12) {
+  } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------ A dequant producers
-    const int pid = threadIdx.x - 128;  // 0..255
+    const int pid = threadIdx.x - kProdWarp0 * 32;  // 0..255
     const int r = pid >> 1, half = pid & 1;
     uint4 q[kPrefetch][C::NA];
     uint32_t sb[kPrefetch][C::NA];
     const uint8_t* rec_of[kPrefetch];
     // issue the loads of step gs into slot gs % kPrefetch
+    int cached_lt = -1;
+    const uint8_t* cached_rec = nullptr;
+    size_t cached_row = 0;
     auto issue_slot = [&](int gs, const int slot) {
       const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
-      const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
-      const uint8_t* rec = tile_record(a, ti.e);
+      if (lt != cached_lt) {
+        cached_lt = lt;
+        const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
+        cached_rec = tile_record(a, ti.e);
+        cached_row = (size_t)ti.mt * BM + r;
+      }
+      const uint8_t* rec = cached_rec;
       rec_of[slot] = rec;
       if (rec == nullptr) return;
-      const size_t row = (size_t)ti.mt * BM + r;
+      const size_t row = cached_row;
 #pragma unroll
       for (int m = 0; m < C::NA; ++m) {
         size_t coff, soff;
@@ -338,16 +364,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    const int q4 = warp - 12;                 // TMEM lane quarter
+    // A warp may only touch TMEM lanes 32*(warp % 4) .. +31.
+    const int q4 = warp & 3;
     const int row = q4 * 32 + lane;           // accumulator row = weight row in tile
+    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     for (int lt = 0; lt < my_tiles; ++lt) {
       const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
+      // per-column token and router weight, once per tile, double buffered: a
+      // thread can be at most one tile ahead of the slowest (acc_empty counts
+      // every epilogue thread), so tile lt never overwrites a table in use.
+      int* tok = col_tok + (lt & 1) * BN;
+      float* wcol = col_w + (lt & 1) * BN;
+      if (PHASE == 1) {
+        if (et < ti.count) {
+          const int p = __ldg(a.pairs + ti.row0 + et);
+          tok[et] = p / a.k;
+          wcol[et] = __ldg(a.weights + p);
+        }
+        mbar_arrive(&tab_ready[lt & 1]);
+        if (!mbar_wait(&tab_ready[lt & 1], (lt >> 1) & 1, globaltimer() + kWaitNs)) {
+          fail();
+          break;
+        }
+      }
       if (*abort_flag || !mbar_wait(acc_full, lt & 1, globaltimer() + kWaitNs)) {
         fail();
         break;
       }
       fence_after_sync();
+      const int col = ti.mt * BM + row;
       for (int c0 = 0; c0 < ti.count; c0 += 16) {
         uint32_t v0[16];
         tmem_ld16(lane_addr + c0, v0);
@@ -355,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
           uint32_t v1[16];
           tmem_ld16(lane_addr + BN + c0, v1);
           tmem_ld_wait();
-          const int col = ti.mt * BM + row;  // intermediate index
+          uint16_t* hrow = a.hbuf + (size_t)(ti.row0 + c0) * a.I + col;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < ti.count) {
@@ -363,20 +409,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
               const float u = __uint_as_float(v1[j]);
               const float h = g / (1.0f + expf(-g)) * u;
               const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-              a.hbuf[(size_t)(ti.row0 + c0 + j) * a.I + col] = *reinterpret_cast<const uint16_t*>(&hb);
+              hrow[(size_t)j * a.I] = *reinterpret_cast<const uint16_t*>(&hb);
             }
           }
         } else {
           tmem_ld_wait();
-          const int col = ti.mt * BM + row;  // output feature
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c0 + j < ti.count) {
-              const int p = __ldg(a.pairs + ti.row0 + c0 + j);
-              const float w = __ldg(a.weights + p);
-              const int t = p / a.k;
-              atomicAdd(a.y + (size_t)t * a.H + col, w * __uint_as_float(v0[j]));
-            }
+            if (c0 + j < ti.count)
+              atomicAdd(a.y + (size_t)tok[c0 + j] * a.H + col, wcol[c0 + j] * __uint_as_float(v0[j]));
           }
         }
       }

@@ -686,3 +686,70 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
   return launch_decode<MOE_FMT_MXFP4>(x_bf16, idx, weights, T, k, expert_ptrs, E, s.hidden,
                                       s.inter, y, hws, dev_status, st);
 }
+
+// ---------------------------------------------------------------------------
+// Decode without any caller-side or library-side allocation.
+//
+// Some callers of this library cannot allocate device memory on the decode
+// path: a plugin inside a host framework that is handed only its input and
+// output buffers, or a latency-critical serving loop that must never enter an
+// allocator.  For them the scratch of moe_experts_decode (the SwiGLU
+// intermediate and the grid-barrier words) lives in the file-scope array
+// below, which every GPU that loads this library holds until the process
+// exits.  Host code must not use the array's name as a device address: the
+// address is fetched once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)2 << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// The device address of g_decode_scratch on the current device (set up on
+// the first call for that device).
+int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" size_t moe_experts_decode_noalloc_limit(void) { return kStaticScratchBytes; }
+
+extern "C" int moe_experts_decode_noalloc(const uint16_t* x_bf16, const int32_t* idx,
+                                          const float* weights, int T, int k,
+                                          const void* const* expert_ptrs, int E,
+                                          moe_expert_shape s, float* y, int32_t* dev_status,
+                                          void* stream) {
+  if (!x_bf16 || !idx || !weights || !expert_ptrs || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || k <= 0 || k > 32 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (!moe::shape_ok(s)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  const size_t need = moe_experts_decode_workspace(T, k, s);
+  if (need == 0 || need > kStaticScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  const int rc = static_scratch(&scratch);
+  if (rc != MOE_OK) return rc;
+  // The array keeps whatever the previous call left; the barrier words sit
+  // right after this call's h and must start at zero.
+  const size_t bar_off = (size_t)T * k * s.inter * sizeof(float);
+  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + bar_off, 0, need - bar_off,
+                      (cudaStream_t)stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return moe_experts_decode(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y, scratch,
+                            kStaticScratchBytes, dev_status, stream);
+}

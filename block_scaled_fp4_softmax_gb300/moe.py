@@ -34,6 +34,8 @@ EXPORTS = (
     "moe_rmsnorm_router_topk",
     "moe_experts_decode_workspace",
     "moe_experts_decode",
+    "moe_experts_decode_noalloc_limit",
+    "moe_experts_decode_noalloc",
     "moe_bucket_workspace",
     "moe_bucket_by_expert",
     "moe_experts_grouped_workspace",
@@ -71,6 +73,8 @@ _SIGS = {
     "moe_experts_decode_workspace": (_sz, [_i, _i, ExpertShape]),
     "moe_experts_decode": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _sz,
                                 _vp, _vp]),
+    "moe_experts_decode_noalloc_limit": (_sz, []),
+    "moe_experts_decode_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _vp]),
     "moe_bucket_workspace": (_sz, [_i, _i, _i]),
     "moe_bucket_by_expert": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_experts_grouped_workspace": (_sz, [_i, _i, _i, ExpertShape]),
@@ -242,6 +246,26 @@ def moe_experts_decode(x, idx, weights, ptrs, s: ExpertShape, y=None, workspace=
                                      ptrs.numel(), s, _ptr(y), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(),
                                      _ptr(dev_status), _stream(stream)), "moe_experts_decode")
+    return y
+
+
+def moe_experts_decode_noalloc_limit() -> int:
+    return int(load().moe_experts_decode_noalloc_limit())
+
+
+def moe_experts_decode_noalloc(x, idx, weights, ptrs, s: ExpertShape, y, dev_status=None,
+                               stream=None):
+    """Decode with the library's static scratch: the caller passes the output
+    buffer ``y`` too, and nothing is allocated on either side."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(idx, "idx", torch.int32)
+    _cuda(weights, "weights", torch.float32)
+    _cuda(ptrs, "expert_ptrs", torch.int64)
+    _cuda(y, "y", torch.float32)
+    T, k = idx.shape
+    _check(load().moe_experts_decode_noalloc(_ptr(x), _ptr(idx), _ptr(weights), T, k, _ptr(ptrs),
+                                             ptrs.numel(), s, _ptr(y), _ptr(dev_status),
+                                             _stream(stream)), "moe_experts_decode_noalloc")
     return y
 
 

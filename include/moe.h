@@ -161,6 +161,28 @@ int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* 
                        moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
                        int32_t* dev_status, void* stream);
 
+/* Decode without allocation.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory on the decode
+ * path, such as a plugin that a host framework hands only its input and
+ * output buffers, or a serving loop that must never enter an allocator.  It
+ * computes exactly what moe_experts_decode computes, with the same arguments
+ * minus the workspace: the scratch is a static device array inside the
+ * library of moe_experts_decode_noalloc_limit() bytes (2 MiB), held by every
+ * GPU that loads the library until the process exits.
+ *  - A call whose moe_experts_decode_workspace(T, k, s) exceeds that limit
+ *    returns MOE_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array per device: calls whose kernels overlap
+ *    on the GPU (other streams, other threads) race and give wrong results.
+ *    The part that must start at zero is cleared by each call on `stream`.
+ *  - No cudaMalloc, cudaFree or other allocating routine is called. */
+size_t moe_experts_decode_noalloc_limit(void);
+int moe_experts_decode_noalloc(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
+                               int T, int k, const void* const* expert_ptrs, int E,
+                               moe_expert_shape s, float* y, int32_t* dev_status, void* stream);
+
 /* Bucketing of routed pairs by expert (first page, "The engine", item 5:
  * the whole prompt runs through a layer at once; second page, "v3": each
  * expert's tokens are found by comparing the index tensor with the expert).

@@ -242,6 +242,36 @@ class PromptLayer:
                 "l2": "flushed (512 MB write) between steps"}
 
 
+def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
+    """FP8 row-scaled GEMV on the two proposed shapes; GB/s of W + x + y per
+    call, L2 flushed between calls."""
+    out = {}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    for M, K in ((8192, 2560), (2560, 4096)):
+        # enough distinct matrices that consecutive calls never share L2 lines
+        n = max(2, (256 << 20) // (M * K) + 1)
+        ws = [synth.expert_matrix((M, K), seed=M + K + i, device=device).to(torch.float8_e4m3fn)
+              .view(torch.uint8) for i in range(n)]
+        s = synth.uniform((M,), seed=M, lo=0.5, hi=2.0, device=device)
+        x = synth.activations(1, K, seed=K, device=device)[0]
+        y = torch.empty(M, dtype=torch.float32, device=device)
+        for i in range(3):
+            moe.fp8_rowscale_gemv(ws[i % n], s, x, y)
+        tot = 0.0
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            moe.fp8_rowscale_gemv(ws[i % n], s, x, y)
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        us = tot / reps * 1e3
+        nbytes = M * K + M * 4 + K * 2 + M * 4
+        out[f"{M}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    return out
+
+
 def max_over_ranks(value: float, dist=None, device="cpu") -> float:
     """The largest value over all ranks (the slowest rank's time)."""
     import torch
@@ -390,6 +420,13 @@ def run_ours(args):
         except Exception as exc:  # report, do not hide
             prompt = {"error": repr(exc)[:300]}
 
+    fp8 = None
+    if not args.no_prompt:
+        try:
+            fp8 = measure_fp8_gemv(torch, moe, synth, dev)
+        except Exception as exc:
+            fp8 = {"error": repr(exc)[:300]}
+
     peak, peak_kind = _peaks()
     value = wl.expert_bytes_per_step() * world / (ms / 1e3) / 1e9
     per_launch_bytes = K_TOP * wl.rec_bytes + H * 2 + H * 4 + K_TOP * I * 4 * 2
@@ -429,6 +466,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
         "prompt": prompt,
+        "fp8_gemv": fp8,
         "dev_status": st,
         "setup_s": round(wl.setup_s, 1),
     }

@@ -89,6 +89,16 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return d;
 }
 
+// 16-byte load of weights read once: no L1 allocation, and the L2 fetches the
+// surrounding 256 bytes so the following k-steps of the same row hit in L2.
+__device__ __forceinline__ uint4 ldg_stream_l2pf(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // Streaming 16-byte load that does not allocate in L1 (weights are read once).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;

@@ -250,6 +250,7 @@ constexpr int kCWarps = 15;
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kSlots = 6;
 constexpr int kSlotBytes = 24576;
+constexpr int kMaxChunkUnits = 1536;  // per-chunk partial sums kept in shared memory
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Args {
@@ -266,19 +267,31 @@ struct Args {
 };
 
 struct Geo {
-  int P, upr, updr, G, ch1, ch2;
+  int P, upr, updr, ch1, ch2;
   long long r0, r1, q0, q1;  // this CTA's gate/up row pairs and output rows
 };
+
+// Rows per chunk: bounded by the slot size, by the partial-sum buffer and (for
+// gate/up) by one reduction warp per row pair.
+__host__ __device__ inline void chunk_rows(int H, int I, int G, int& ch1, int& ch2) {
+  const int b1 = 2 * (H / 2 + H / G);
+  ch1 = (kSlotBytes - 64) / b1;
+  ch1 = ch1 < kCWarps ? ch1 : kCWarps;
+  const int u1 = 2 * (H / 32);
+  ch1 = ch1 < kMaxChunkUnits / u1 ? ch1 : kMaxChunkUnits / u1;
+  ch1 = ch1 < 1 ? 1 : ch1;
+  ch2 = (kSlotBytes - 32) / (I / 2 + I / G);
+  ch2 = ch2 < 64 ? ch2 : 64;
+  ch2 = ch2 < kMaxChunkUnits / (I / 32) ? ch2 : kMaxChunkUnits / (I / 32);
+  ch2 = ch2 < 1 ? 1 : ch2;
+}
 
 __device__ __forceinline__ Geo geometry(const Args& a, int fmt) {
   Geo g;
   g.P = a.T * a.k;
   g.upr = a.H >> 5;
   g.updr = a.I >> 5;
-  g.G = fmt == MOE_FMT_NVFP4 ? 16 : 32;
-  const int b1 = 2 * (a.H / 2 + a.H / g.G);
-  g.ch1 = max(1, (kSlotBytes - 64) / b1);
-  g.ch2 = max(1, min(64, (kSlotBytes - 32) / (a.I / 2 + a.I / g.G)));
+  chunk_rows(a.H, a.I, fmt == MOE_FMT_NVFP4 ? 16 : 32, g.ch1, g.ch2);
   const long long R1 = (long long)g.P * a.I, R2 = (long long)a.T * a.H;
   g.r0 = (long long)blockIdx.x * R1 / gridDim.x;
   g.r1 = (long long)(blockIdx.x + 1) * R1 / gridDim.x;
@@ -300,7 +313,44 @@ __device__ __forceinline__ Win window(size_t start, size_t len) {
   return w;
 }
 
-template <int FMT>
+// One 16-byte unit of codes (32 elements) against activations held as float4
+// quads: quad qq (elements 4qq..4qq+3 of the unit) at act[qq * stride].  Four
+// independent accumulators (one per code word) keep the FMA chains short.
+template <int FMT, int STRIDE>
+__device__ __forceinline__ float unit_dot_q(uint4 q, uint32_t sbits, const float4* act, int stride_rt) {
+  const int stride = STRIDE > 0 ? STRIDE : stride_rt;
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float2 acc[4];
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    acc[wi] = make_float2(0.f, 0.f);
+    const float4 x0 = act[(2 * wi) * stride];
+    const float4 x1 = act[(2 * wi + 1) * stride];
+    const float2 xp[4] = {make_float2(x0.x, x0.y), make_float2(x0.z, x0.w), make_float2(x1.x, x1.y),
+                          make_float2(x1.z, x1.w)};
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      const uint32_t h2 = moe::e2m1x2_to_f16x2((w[wi] >> (8 * bi)) & 0xFFu);
+      const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      acc[wi] = moe::ffma2(wf, xp[bi], acc[wi]);
+    }
+  }
+  const float a = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+  const float b = (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+  if (FMT == MOE_FMT_NVFP4) {
+    const float2 s = moe::e4m3x2_to_f32x2(sbits);
+    return a * s.x + b * s.y;
+  } else {
+    return (a + b) * moe::ue8m0_to_f32(sbits);
+  }
+}
+
+// float element e of a unit-quad layout: quad (e%32)/4 at [quad][unit]
+__device__ __forceinline__ int quad_index(int e, int stride) {
+  return (((e & 31) >> 2) * stride + (e >> 5)) * 4 + (e & 3);
+}
+
+template <int FMT, int UPR, int UPDR>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;                                          // kSlots x kSlotBytes
@@ -309,13 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   const uint8_t** recs = reinterpret_cast<const uint8_t**>(empty + kSlots);  // [64]
   float* wts = reinterpret_cast<float*>(recs + 64);                          // [64]
   int* flags = reinterpret_cast<int*>(wts + 64);                             // [0] abort, [1] barrier ok
-  float* yacc = reinterpret_cast<float*>(flags + 4);                         // [rows/CTA + 1]
+  float* part = reinterpret_cast<float*>(flags + 4);                         // [2][kMaxChunkUnits]
+  float* yacc = part + 2 * kMaxChunkUnits;                                   // [rows/CTA + 1]
   moe::pdl_launch_dependents();
 
   const Geo g = geometry(a, FMT);
+  const int upr = UPR > 0 ? UPR : g.upr;
+  const int updr = UPDR > 0 ? UPDR : g.updr;
   const int rows_cta = (int)(g.q1 - g.q0);
   int* ybad = reinterpret_cast<int*>(yacc + rows_cta + 1);
-  float2* act = reinterpret_cast<float2*>(
+  float4* act = reinterpret_cast<float4*>(
       (reinterpret_cast<uintptr_t>(ybad + rows_cta + 1) + 15) & ~(uintptr_t)15);
   const moe::RecordOffsets o = moe::record_offsets(a.H, a.I, FMT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -323,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       moe::tc::mbar_init(&full[s], 1);
-      moe::tc::mbar_init(&empty[s], kCWarps);
+      moe::tc::mbar_init(&empty[s], 1);
     }
     flags[0] = 0;
     moe::tc::mbar_fence_init();
@@ -338,17 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
                                        blockIdx.x == 0 ? a.status : nullptr);
     wts[threadIdx.x] = a.w[threadIdx.x];
   }
-  // x of every token, transposed float2 layout [t][16][H/32]
-  for (int h0 = threadIdx.x * 8; h0 < a.T * a.H; h0 += kThreads * 8) {
+  // x of every token as float quads [t][8][H/32]
+  for (int h0 = threadIdx.x * 4; h0 < a.T * a.H; h0 += kThreads * 4) {
     const int t = h0 / a.H, hh = h0 - t * a.H;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + h0));
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    const int c = hh >> 5, pe0 = (hh & 31) >> 1;
-    float2* xt = act + (size_t)t * 16 * g.upr;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      xt[(pe0 + i) * g.upr + c] =
-          make_float2(moe::bf16_bits_to_f32(wv[i] & 0xFFFFu), moe::bf16_bits_to_f32(wv[i] >> 16));
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.x + h0));
+    act[(size_t)t * 8 * upr + ((hh & 31) >> 2) * upr + (hh >> 5)] =
+        make_float4(moe::bf16_bits_to_f32(v.x & 0xFFFFu), moe::bf16_bits_to_f32(v.x >> 16),
+                    moe::bf16_bits_to_f32(v.y & 0xFFFFu), moe::bf16_bits_to_f32(v.y >> 16));
   }
   __syncthreads();
 
@@ -382,8 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
         const uint32_t cb = (uint32_t)n * (a.H / 2);
         const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
         const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
-        const uint32_t total = rec ? 2 * cb + gw.bytes + uw.bytes : 0;
-        moe::tc::mbar_arrive_expect_tx(&full[slot], total);
+        moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? 2 * cb + gw.bytes + uw.bytes : 0);
         if (rec) {
           moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i0 * (a.H / 2), cb, &full[slot]);
           moe::tc::bulk_g2s(base + cb, rec + o.up + (size_t)i0 * (a.H / 2), cb, &full[slot]);
@@ -418,67 +466,69 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
     }
   } else {
     // ------------------------------------------------------------ consumers
+    // Control flow is the same for every consumer thread (fixed trip counts),
+    // so the named barriers always match; after a timeout the work is skipped.
+    const int ct = threadIdx.x;  // 0..479
     int c = 0;
-    bool ok = true;
-    auto take = [&](int& slot) -> bool {
-      slot = c % kSlots;
-      if (*abort_flag ||
-          !moe::tc::mbar_wait(&full[slot], (c / kSlots) & 1, moe::tc::globaltimer() + kWaitNs)) {
+    auto take = [&](int slot) -> bool {
+      if (*abort_flag) return false;
+      if (!moe::tc::mbar_wait(&full[slot], (c / kSlots) & 1, moe::tc::globaltimer() + kWaitNs)) {
         *abort_flag = 1;
         moe::status_or(a.status, MOE_DEV_TIMEOUT);
         return false;
       }
       return true;
     };
-    auto release = [&](int slot) {
-      __syncwarp();
-      if (lane == 0) moe::tc::mbar_arrive(&empty[slot]);
-      ++c;
-    };
-    // gate/up + SwiGLU
-    for (long long r = g.r0; r < g.r1 && ok;) {
+    // gate/up + SwiGLU: every consumer thread takes units of the chunk; one
+    // warp per row pair then adds the partial sums in a fixed order.
+    for (long long r = g.r0; r < g.r1;) {
       const int p = (int)(r / a.I), i0 = (int)(r - (long long)p * a.I);
       const int n = (int)min((long long)g.ch1, min(g.r1 - r, (long long)(a.I - i0)));
-      int slot;
-      if (!(ok = take(slot))) break;
+      const int slot = c % kSlots;
+      float* pbuf = part + (c & 1) * kMaxChunkUnits;
+      const bool live = take(slot);
       const uint8_t* base = ring + slot * kSlotBytes;
       const uint8_t* rec = recs[p];
       const uint32_t cb = (uint32_t)n * (a.H / 2);
       const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
       const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
-      const float2* xt = act + (size_t)(p / a.k) * 16 * g.upr;
-      for (int rr = warp; rr < n; rr += kCWarps) {
-        float hv = __uint_as_float(0x7FC00000u);
-        if (rec) {
-          const uint8_t* gcode = base + (size_t)rr * (a.H / 2);
-          const uint8_t* ucode = base + cb + (size_t)rr * (a.H / 2);
-          const uint8_t* gsc = base + 2 * cb + gw.delta + (size_t)rr * (a.H / G);
-          const uint8_t* usc = base + 2 * cb + gw.bytes + uw.delta + (size_t)rr * (a.H / G);
-          float gacc = 0.f, uacc = 0.f;
-          for (int u = lane; u < 2 * g.upr; u += 32) {
-            const bool is_up = u >= g.upr;
-            const int cix = is_up ? u - g.upr : u;
-            const uint4 q = *reinterpret_cast<const uint4*>((is_up ? ucode : gcode) + 16 * cix);
-            const uint8_t* sp = (is_up ? usc : gsc) + sstep * cix;
-            const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8)
-                                                     : (uint32_t)sp[0];
-            const float d = unit_dot_col<FMT>(q, sb, xt + cix, g.upr);
-            if (is_up) uacc += d;
-            else gacc += d;
-          }
-          gacc = moe::warp_sum(gacc);
-          uacc = moe::warp_sum(uacc);
-          hv = gacc / (1.0f + expf(-gacc)) * uacc;
+      const float4* xt = act + (size_t)(p / a.k) * 8 * upr;
+      const int nunits = n * 2 * upr;
+      if (live && rec) {
+        for (int qf = ct; qf < nunits; qf += kCThreads) {
+          const int rr = qf / (2 * upr), rem = qf - rr * 2 * upr;
+          const bool is_up = rem >= upr;
+          const int cix = is_up ? rem - upr : rem;
+          const uint4 q = *reinterpret_cast<const uint4*>(base + (is_up ? cb : 0) + (size_t)rr * (a.H / 2) + 16 * cix);
+          const uint8_t* sp = base + 2 * cb + (is_up ? gw.bytes + uw.delta : gw.delta) + (size_t)rr * (a.H / G) + sstep * cix;
+          const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) : (uint32_t)sp[0];
+          pbuf[qf] = unit_dot_q<FMT, UPR>(q, sb, xt + cix, upr);
         }
-        if (lane == 0) a.hws[(size_t)p * a.I + i0 + rr] = hv;
       }
-      release(slot);
+      moe::tc::named_sync(1, kCThreads);
+      if (ct == 0) moe::tc::mbar_arrive(&empty[slot]);
+      if (warp < n) {
+        float hv = __uint_as_float(0x7FC00000u);
+        if (live && rec) {
+          const float* pr = pbuf + warp * 2 * upr;
+          float gs = 0.f, us = 0.f;
+          for (int u = lane; u < upr; u += 32) {
+            gs += pr[u];
+            us += pr[upr + u];
+          }
+          gs = moe::warp_sum(gs);
+          us = moe::warp_sum(us);
+          hv = gs / (1.0f + expf(-gs)) * us;
+        }
+        if (lane == 0) a.hws[(size_t)p * a.I + i0 + warp] = hv;
+      }
+      ++c;
       r += n;
     }
     // grid barrier among the consumer threads of every CTA
     moe::tc::named_sync(1, kCThreads);
-    if (threadIdx.x == 0) {
-      int good = ok && !*abort_flag;
+    if (ct == 0) {
+      int good = !*abort_flag;
       if (good) {
         const unsigned e0 = moe::ld_acquire_gpu(a.bar + 1);
         __threadfence();
@@ -505,58 +555,65 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
       flags[1] = good;
     }
     moe::tc::named_sync(1, kCThreads);
-    ok = flags[1] != 0;
-    if (ok && rows_cta > 0) {
-      // stage h of the tokens this CTA's output rows belong to
+    if (rows_cta > 0) {
+      // stage h of the tokens this CTA's output rows belong to, float quads
+      // [pair][8][I/32]
       const int t_lo = (int)(g.q0 / a.H), t_hi = (int)((g.q1 - 1) / a.H);
-      const int n_el = (t_hi - t_lo + 1) * a.k * a.I;
-      const float* src = a.hws + (size_t)t_lo * a.k * a.I;
-      for (int e = threadIdx.x; e < n_el; e += kCThreads) {
-        const int pj = e / a.I, i = e - pj * a.I;  // pair relative to t_lo*k
-        const float v = __ldcg(src + e);
-        float* dst = reinterpret_cast<float*>(act + (size_t)pj * 16 * g.updr);
-        dst[2 * (((i & 31) >> 1) * g.updr + (i >> 5)) + (i & 1)] = v;
+      const int n_q = (t_hi - t_lo + 1) * a.k * a.I / 4;
+      const float4* src = reinterpret_cast<const float4*>(a.hws + (size_t)t_lo * a.k * a.I);
+      if (flags[1]) {
+        for (int e4 = ct; e4 < n_q; e4 += kCThreads) {
+          const int e = 4 * e4;
+          const int pj = e / a.I, i = e - pj * a.I;
+          act[(size_t)pj * 8 * updr + ((i & 31) >> 2) * updr + (i >> 5)] = __ldcg(src + e4);
+        }
       }
       moe::tc::named_sync(1, kCThreads);
-      // down + weighted combine
-      for (long long q = g.q0; q < g.q1 && ok;) {
+      // down + weighted combine: units over all consumer threads, then one
+      // thread per output row adds its partials in a fixed order
+      for (long long q = g.q0; q < g.q1;) {
         const int t = (int)(q / a.H), n0 = (int)(q - (long long)t * a.H);
         const int nr = (int)min((long long)g.ch2, min(g.q1 - q, (long long)(a.H - n0)));
-        for (int j = 0; j < a.k && ok; ++j) {
-          int slot;
-          if (!(ok = take(slot))) break;
+        for (int j = 0; j < a.k; ++j) {
+          const int slot = c % kSlots;
+          float* pbuf = part + (c & 1) * kMaxChunkUnits;
+          const bool live = take(slot);
           const uint8_t* base = ring + slot * kSlotBytes;
           const int pj = t * a.k + j;
           const uint8_t* rec = recs[pj];
           const uint32_t cb = (uint32_t)nr * (a.I / 2);
           const Win dw = window(o.down_s + (size_t)n0 * (a.I / G), (size_t)nr * (a.I / G));
-          const float2* hcol = act + (size_t)(pj - t_lo * a.k) * 16 * g.updr;
-          for (int rr = warp; rr < nr; rr += kCWarps) {
-            const int yi = (int)(q - g.q0) + rr;
-            if (!rec) {
-              if (lane == 0) ybad[yi] = 1;
-              continue;
+          const float4* hcol = act + (size_t)(pj - t_lo * a.k) * 8 * updr;
+          const int nunits = nr * updr;
+          if (live && rec) {
+            for (int qf = ct; qf < nunits; qf += kCThreads) {
+              const int rr = qf / updr, u = qf - rr * updr;
+              const uint4 qv = *reinterpret_cast<const uint4*>(base + (size_t)rr * (a.I / 2) + 16 * u);
+              const uint8_t* sp = base + cb + dw.delta + (size_t)rr * (a.I / G) + sstep * u;
+              const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) : (uint32_t)sp[0];
+              pbuf[qf] = unit_dot_q<FMT, UPDR>(qv, sb, hcol + u, updr);
             }
-            const uint8_t* dcode = base + (size_t)rr * (a.I / 2);
-            const uint8_t* dsc = base + cb + dw.delta + (size_t)rr * (a.I / G);
-            float acc = 0.f;
-            for (int u = lane; u < g.updr; u += 32) {
-              const uint4 qv = *reinterpret_cast<const uint4*>(dcode + 16 * u);
-              const uint8_t* sp = dsc + sstep * u;
-              const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8)
-                                                       : (uint32_t)sp[0];
-              acc += unit_dot_col<FMT>(qv, sb, hcol + u, g.updr);
-            }
-            acc = moe::warp_sum(acc);
-            if (lane == 0) yacc[yi] += wts[pj] * acc;
           }
-          release(slot);
+          moe::tc::named_sync(1, kCThreads);
+          if (ct == 0) moe::tc::mbar_arrive(&empty[slot]);
+          if (ct < nr) {
+            const int yi = (int)(q - g.q0) + ct;
+            if (live && rec) {
+              const float* pr = pbuf + ct * updr;
+              float s = 0.f;
+              for (int u = 0; u < updr; ++u) s += pr[u];
+              yacc[yi] += wts[pj] * s;
+            } else {
+              ybad[yi] = 1;
+            }
+          }
+          ++c;
         }
         q += nr;
       }
       moe::tc::named_sync(1, kCThreads);
-      for (int r = threadIdx.x; r < rows_cta; r += kCThreads)
-        a.y[g.q0 + r] = (ybad[r] || !ok) ? __uint_as_float(0x7FC00000u) : yacc[r];
+      for (int r = ct; r < rows_cta; r += kCThreads)
+        a.y[g.q0 + r] = (ybad[r] || *abort_flag) ? __uint_as_float(0x7FC00000u) : yacc[r];
     }
   }
   __syncthreads();
@@ -568,7 +625,7 @@ size_t smem_bytes(int T, int k, int H, int I, int sms) {
   const long long ntok = std::min<long long>(T, rows / H + 2);
   const size_t act = std::max<size_t>((size_t)T * H * 4, (size_t)ntok * k * I * 4);
   return (size_t)kSlots * kSlotBytes + 2 * kSlots * 8 + 64 * 8 + 64 * 4 + 16 +
-         (size_t)(rows + 1) * 8 + 16 + act;
+         2 * kMaxChunkUnits * 4 + (size_t)(rows + 1) * 8 + 16 + act;
 }
 
 }  // namespace st
@@ -629,14 +686,24 @@ bool stream_fits(int T, int k, int H, int I) {
   return st::smem_bytes(T, k, H, I, sms) + 1024 <= (size_t)stream_smem_limit();
 }
 
+template <int FMT, int UPR, int UPDR>
+int launch_stream_shape(const st::Args& sa, size_t smem, int sms, cudaStream_t stream) {
+  static size_t granted = 0;
+  if (!ensure_smem(st::stream_kernel<FMT, UPR, UPDR>, smem, &granted)) return MOE_ERR_CUDA;
+  return moe::launch_pdl(st::stream_kernel<FMT, UPR, UPDR>, dim3(sms), dim3(st::kThreads), smem,
+                         stream, sa);
+}
+
 template <int FMT>
 int launch_stream(const st::Args& sa, cudaStream_t stream) {
   const int sms = sm_count();
   const size_t smem = st::smem_bytes(sa.T, sa.k, sa.H, sa.I, sms);
-  static size_t granted = 0;
-  if (!ensure_smem(st::stream_kernel<FMT>, smem, &granted)) return MOE_ERR_CUDA;
-  // one CTA per SM: all CTAs are resident together, as the grid barrier needs
-  return moe::launch_pdl(st::stream_kernel<FMT>, dim3(sms), dim3(st::kThreads), smem, stream, sa);
+  // one CTA per SM: all CTAs are resident together, as the grid barrier needs.
+  // The row strides are compile-time constants for the two model shapes.
+  const int upr = sa.H / 32, updr = sa.I / 32;
+  if (upr == 80 && updr == 20) return launch_stream_shape<FMT, 80, 20>(sa, smem, sms, stream);
+  if (upr == 128 && updr == 90) return launch_stream_shape<FMT, 128, 90>(sa, smem, sms, stream);
+  return launch_stream_shape<FMT, 0, 0>(sa, smem, sms, stream);
 }
 
 }  // namespace

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
         }
         const uint8_t* cp = rec + coff + row * (K / 2) + ks * (BK / 2) + half * 16;
         const uint8_t* sp = rec + soff + row * (K / G) + (ks * BK + half * 32) / G;
-        q[slot][m] = moe::ldg_stream(cp);
+        q[slot][m] = moe::ldg_stream_l2pf(cp);
         sb[slot][m] = FMT == MOE_FMT_NVFP4 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(sp))
                                            : (uint32_t)__ldg(sp);
       }
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
           break;
         }
       }
-      if (*abort_flag || !mbar_wait(acc_full, lt & 1, globaltimer() + kWaitNs)) {
+      if (*abort_flag || !mbar_wait_backoff(acc_full, lt & 1, globaltimer() + kWaitNs)) {
         fail();
         break;
       }

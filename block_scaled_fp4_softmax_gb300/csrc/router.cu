@@ -111,6 +111,46 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Selects the k best of the lanes' candidates (composite keys, unique): round
+// r takes the largest key below round r-1's winner, so nothing is ever
+// removed and the candidate array stays in registers.  Lane r ends with
+// expert r and its logit.
+template <int EPL>
+__device__ __forceinline__ void warp_select_topk(const unsigned long long (&cand)[EPL], int k,
+                                                 int lane, int& my_e, float& my_l) {
+  unsigned long long prev = ~0ull;
+  my_e = 0;
+  my_l = 0.0f;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (cand[i] < prev && cand[i] > best) best = cand[i];
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
+      best = o > best ? o : best;
+    }
+    prev = best;
+    if (lane == r) {
+      my_e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
+      my_l = key_to_float((uint32_t)(best >> 32));
+    }
+  }
+}
+
+// Writes idx/weights of one token from the selection above.
+__device__ __forceinline__ void write_topk(int lane, int k, int my_e, float my_l, int32_t* idx,
+                                           float* weights) {
+  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane < k ? expf(my_l - l0) : 0.0f;
+  const float sum = moe::warp_sum(ex);
+  if (lane < k) {
+    idx[lane] = my_e;
+    weights[lane] = __fdiv_rn(ex, sum);
+  }
+}
+
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E,
                                                    int k, int32_t* __restrict__ idx,
@@ -130,84 +170,52 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       cand[i] = ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)e);
     }
   }
-  int my_e = 0;
-  float my_l = 0.0f;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) best = cand[i] > best ? cand[i] : best;
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
-      best = o > best ? o : best;
-    }
-    const int e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
-    if ((e & 31) == lane) {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (i == (e >> 5)) cand[i] = 0ull;
-    }
-    if (lane == r) {
-      my_e = e;
-      my_l = key_to_float((uint32_t)(best >> 32));
-    }
-  }
-  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-  const float ex = lane < k ? expf(my_l - l0) : 0.0f;
-  const float sum = moe::warp_sum(ex);
-  if (lane < k) {
-    idx[(size_t)t * k + lane] = my_e;
-    weights[(size_t)t * k + lane] = __fdiv_rn(ex, sum);
-  }
+  int my_e;
+  float my_l;
+  warp_select_topk<EPL>(cand, k, lane, my_e, my_l);
+  write_topk(lane, k, my_e, my_l, idx + (size_t)t * k, weights + (size_t)t * k);
 }
 
 // ---------------------------------------------------------------------------
-// RMS chaining: one CTA per token, FP64 mean of squares in a fixed tree, one
-// rounding to BF16 (ties to even) from FP64.
+// RMS chaining in FP32, one fixed order (so the BF16 result is reproducible):
+// thread t of 256 sums y[t + 256 m]^2 for m ascending (square rounded, then
+// added), a pairwise tree combines the 256 partial sums, mean = sum / H,
+// r = 1 / sqrt(mean + eps) with IEEE sqrt and divide, x = BF16_rn(y * r).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint16_t f64_to_bf16_rn(double v) {
-  if (v == 0.0 || !isfinite(v)) {
-    const float f = (float)v;  // zero, inf and NaN convert exactly enough
-    uint32_t b = __float_as_uint(f);
-    if (f != f) b = 0x7FC00000u;
-    return (uint16_t)(b >> 16);
+__device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ yr, int H, float eps,
+                                                     float* part) {
+  float acc = 0.0f;
+  for (int i = threadIdx.x; i < H; i += 256) {
+    const float v = yr[i];
+    acc = __fadd_rn(acc, __fmul_rn(v, v));
   }
-  const double a = fabs(v);
-  const int e = ilogb(a);
-  const int qe = max(e - 7, -133);
-  const double q = rint(scalbn(a, -qe));
-  double r = scalbn(q, qe);
-  uint32_t bits;
-  if (r >= 0x1.ffp127) {
-    bits = 0x7F800000u;
-  } else {
-    bits = __float_as_uint((float)r);  // exact: r has at most 8 significant bits
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] = __fadd_rn(part[threadIdx.x], part[threadIdx.x + w]);
+    __syncthreads();
   }
-  if (v < 0) bits |= 0x80000000u;
-  return (uint16_t)(bits >> 16);
+  const float mean = __fdiv_rn(part[0], (float)H);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+  __syncthreads();  // part[] may be reused by the caller
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
 }
 
 __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restrict__ y, int H,
-                                                           double eps,
+                                                           float eps,
                                                            uint16_t* __restrict__ x) {
-  __shared__ double part[256];
+  __shared__ float part[256];
   moe::pdl_launch_dependents();
   moe::pdl_wait();
   const int t = blockIdx.x;
   const float* yr = y + (size_t)t * H;
-  double s = 0.0;
-  for (int i = threadIdx.x; i < H; i += 256) {
-    const double v = (double)yr[i];
-    s = fma(v, v, s);
-  }
-  part[threadIdx.x] = s;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-    __syncthreads();
-  }
-  const double inv = 1.0 / sqrt(part[0] / (double)H + eps);
-  for (int i = threadIdx.x; i < H; i += 256) x[(size_t)t * H + i] = f64_to_bf16_rn((double)yr[i] * inv);
+  const float r = rms_inv_fixed_order(yr, H, eps, part);
+  for (int i = threadIdx.x; i < H; i += 256) x[(size_t)t * H + i] = f32_to_bf16_bits(__fmul_rn(yr[i], r));
 }
 
 // ---------------------------------------------------------------------------
@@ -226,7 +234,7 @@ constexpr int kClMaxT = 4;
 struct ClusterArgs {
   const uint16_t* x;    // [T, H] BF16, or NULL when y_prev is given
   const float* y_prev;  // [T, H] FP32 to RMS-normalise, or NULL
-  double eps;
+  float eps;
   uint16_t* x_out;      // written by CTA 0 when y_prev is given (may be NULL otherwise)
   const uint16_t* wr;
   const float* bias;
@@ -253,10 +261,29 @@ __device__ __forceinline__ float dsmem_ld_f32(const float* local_addr, uint32_t 
   return v;
 }
 
+template <int EPL>
+__device__ __forceinline__ void cluster_topk(const ClusterArgs& a, const float* lg, int t, int lane) {
+  unsigned long long cand[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    cand[i] = 0ull;
+    const int e = lane + 32 * i;
+    if (e < a.E) {
+      const uint32_t owner = (uint32_t)(e / a.epc);
+      const float v = dsmem_ld_f32(lg + t * a.epc + (e - (int)owner * a.epc), owner);
+      cand[i] = ((unsigned long long)ordered_key(v) << 32) | (unsigned long long)(~(uint32_t)e);
+    }
+  }
+  int my_e;
+  float my_l;
+  warp_select_topk<EPL>(cand, a.k, lane, my_e, my_l);
+  write_topk(lane, a.k, my_e, my_l, a.idx + (size_t)t * a.k, a.weights + (size_t)t * a.k);
+}
+
 __global__ void __launch_bounds__(kClThreads) router_cluster_kernel(ClusterArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* wbar = reinterpret_cast<uint64_t*>(sm);
-  double* part = reinterpret_cast<double*>(sm + 16);                 // [256]
+  float* part = reinterpret_cast<float*>(sm + 16);                   // [256]
   float* lg = reinterpret_cast<float*>(sm + 16 + 256 * 8);           // [kClMaxT][epc]
   uint16_t* xs = reinterpret_cast<uint16_t*>(lg + kClMaxT * a.epc);  // [T][H] BF16
   uint16_t* ws = reinterpret_cast<uint16_t*>(
@@ -284,24 +311,12 @@ __global__ void __launch_bounds__(kClThreads) router_cluster_kernel(ClusterArgs 
   for (int t = 0; t < a.T; ++t) {
     if (a.y_prev) {
       const float* yr = a.y_prev + (size_t)t * a.H;
-      double acc = 0.0;
+      const float r = rms_inv_fixed_order(yr, a.H, a.eps, part);
       for (int i = threadIdx.x; i < a.H; i += kClThreads) {
-        const double v = (double)yr[i];
-        acc = fma(v, v, acc);
-      }
-      part[threadIdx.x] = acc;
-      __syncthreads();
-      for (int w = kClThreads / 2; w > 0; w >>= 1) {
-        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-        __syncthreads();
-      }
-      const double inv = 1.0 / sqrt(part[0] / (double)a.H + a.eps);
-      for (int i = threadIdx.x; i < a.H; i += kClThreads) {
-        const uint16_t b = f64_to_bf16_rn((double)yr[i] * inv);
+        const uint16_t b = f32_to_bf16_bits(__fmul_rn(yr[i], r));
         xs[(size_t)t * a.H + i] = b;
         if (rank == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = b;
       }
-      __syncthreads();
     } else {
       for (int i = threadIdx.x * 8; i < a.H; i += kClThreads * 8)
         *reinterpret_cast<uint4*>(xs + (size_t)t * a.H + i) =
@@ -353,48 +368,13 @@ __global__ void __launch_bounds__(kClThreads) router_cluster_kernel(ClusterArgs 
 
   // top-k in CTA 0, one warp per token, candidates read over DSMEM
   if (rank == 0 && warp < a.T) {
-    const int t = warp;
-    unsigned long long cand[32];
     const int epl = (a.E + 31) / 32;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      cand[i] = 0ull;
-      const int e = lane + 32 * i;
-      if (i < epl && e < a.E) {
-        const uint32_t owner = (uint32_t)(e / a.epc);
-        const float v = dsmem_ld_f32(lg + t * a.epc + (e - (int)owner * a.epc), owner);
-        cand[i] = ((unsigned long long)ordered_key(v) << 32) | (unsigned long long)(~(uint32_t)e);
-      }
-    }
-    int my_e = 0;
-    float my_l = 0.0f;
-    for (int r = 0; r < a.k; ++r) {
-      unsigned long long best = 0ull;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) best = cand[i] > best ? cand[i] : best;
-#pragma unroll
-      for (int d = 16; d > 0; d >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
-        best = o > best ? o : best;
-      }
-      const int e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
-      if ((e & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i == (e >> 5)) cand[i] = 0ull;
-      }
-      if (lane == r) {
-        my_e = e;
-        my_l = key_to_float((uint32_t)(best >> 32));
-      }
-    }
-    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-    const float ex = lane < a.k ? expf(my_l - l0) : 0.0f;
-    const float sum = moe::warp_sum(ex);
-    if (lane < a.k) {
-      a.idx[(size_t)t * a.k + lane] = my_e;
-      a.weights[(size_t)t * a.k + lane] = __fdiv_rn(ex, sum);
-    }
+    if (epl <= 1) cluster_topk<1>(a, lg, warp, lane);
+    else if (epl <= 2) cluster_topk<2>(a, lg, warp, lane);
+    else if (epl <= 4) cluster_topk<4>(a, lg, warp, lane);
+    else if (epl <= 8) cluster_topk<8>(a, lg, warp, lane);
+    else if (epl <= 16) cluster_topk<16>(a, lg, warp, lane);
+    else cluster_topk<32>(a, lg, warp, lane);
   }
   cluster_sync_all();  // keep every CTA's shared memory alive until CTA 0 is done
 }
@@ -508,7 +488,7 @@ extern "C" int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16
   if (!y || !x_bf16 || T < 0 || H <= 0 || !(eps >= 0.0)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   return moe::launch_pdl(rmsnorm_bf16_kernel, dim3(T), dim3(256), 0, (cudaStream_t)stream, y, H,
-                         eps, x_bf16);
+                         (float)eps, x_bf16);
 }
 
 extern "C" int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps,
@@ -525,7 +505,7 @@ extern "C" int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double
   if (cluster_fits(T, H, E)) {
     ClusterArgs a = {};
     a.y_prev = y_prev;
-    a.eps = eps;
+    a.eps = (float)eps;
     a.x_out = x_out;
     a.wr = wr_bf16;
     a.bias = bias;

@@ -55,6 +55,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// The same wait for threads off the critical path: after a few tries it
+// sleeps between polls so the spinning does not steal issue slots.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity,
+                                                  uint64_t deadline_ns) {
+  for (int i = 0; i < 8; ++i)
+    if (mbar_test(bar, parity)) return true;
+  while (true) {
+    __nanosleep(64);
+    if (mbar_test(bar, parity)) return true;
+    if (globaltimer() > deadline_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // cp.async (16-byte, L2 only), with zero fill when src_bytes == 0
 // ---------------------------------------------------------------------------

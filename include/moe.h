@@ -116,9 +116,13 @@ int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, const float
                     int T, int H, int E, int k,
                     int32_t* idx, float* weights, float* logits, void* stream);
 
-/* Layer chaining for stacked decode: x[t] = BF16(y[t] / sqrt(mean(y[t]^2) +
- * eps)), no learnable weight; the mean and the division are done in FP64 and
- * the result is rounded once to BF16 (ties to even).
+/* Layer chaining for stacked decode: x[t] = BF16(y[t] * r), r = 1 /
+ * sqrt(mean(y[t]^2) + eps), no learnable weight.  FP32 in one fixed order so
+ * the result is reproducible bit for bit: thread i of 256 sums y[i + 256 m]^2
+ * for m ascending (square rounded, then added), a pairwise tree adds partial
+ * i + w into partial i for w = 128, 64, ..., 1, mean = sum / H, r uses IEEE
+ * sqrt and divide, and y * r is rounded once to BF16 (ties to even).  eps is
+ * rounded to FP32.
  * y [T x H] FP32 input, x_bf16 [T x H] output. */
 int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16_t* x_bf16,
                      void* stream);

@@ -445,12 +445,32 @@ def moe_layer_grouped_by_expert(x_bits, idx, weights, records, H: int, I: int, f
 
 
 def rmsnorm_bf16(y, eps: float = 1e-6) -> np.ndarray:
-    """Layer-chaining glue for stacked decode: x_next = BF16(y / sqrt(mean(y^2)
-    + eps)) with no learnable weight, computed in float64 and rounded once to
-    BF16.  Returns BF16 bit patterns (uint16) [T, H]."""
-    y = np.asarray(y, dtype=np.float64)
-    ms = np.mean(y * y, axis=1, keepdims=True)
-    return bf16_round_bits(y / np.sqrt(ms + eps))
+    """Layer-chaining glue for stacked decode: x_next = BF16(y * r) with
+    r = 1 / sqrt(mean(y^2) + eps) and no learnable weight.
+
+    The pages only say the next layer's input is the previous output,
+    RMS-normalised; the reading taken is FP32 arithmetic in one fixed order, so
+    the BF16 result is reproducible bit for bit: 256 strided partial sums
+    (partial t adds y[t + 256 m]^2 for m ascending, each square rounded, then
+    added), a pairwise tree partial[t] += partial[t + w] for w = 128, 64, ..., 1,
+    mean = sum / H, r = 1 / sqrt(mean + eps) with IEEE sqrt and divide, and
+    x = y * r rounded once to BF16 (ties to even).  Returns BF16 bit patterns
+    (uint16) [T, H]."""
+    y = np.asarray(y, dtype=np.float32)
+    T, H = y.shape
+    part = np.zeros((T, 256), dtype=np.float32)
+    for m in range((H + 255) // 256):
+        seg = y[:, 256 * m: 256 * (m + 1)]
+        n = seg.shape[1]
+        part[:, :n] = part[:, :n] + seg * seg
+    w = 128
+    while w >= 1:
+        part[:, :w] = part[:, :w] + part[:, w: 2 * w]
+        w //= 2
+    mean = part[:, 0] / np.float32(H)
+    r = np.float32(1.0) / np.sqrt(mean + np.float32(eps))
+    x = y * r[:, None]
+    return bf16_round_bits(x.astype(np.float64))
 
 
 # ---------------------------------------------------------------------------

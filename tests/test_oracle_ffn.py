@@ -189,15 +189,32 @@ def test_bucketing_brute_force():
     assert list(pairs) == want
 
 
-def test_rmsnorm_matches_torch_then_bf16():
+def test_rmsnorm_close_to_torch_float64_then_bf16():
     rng = np.random.default_rng(10)
-    y = (rng.standard_normal((4, 256)) * 0.3).astype(np.float32)
+    y = (rng.standard_normal((4, 2560)) * 0.3).astype(np.float32)
     got = O.rmsnorm_bf16(y, 1e-6)
-    ref = torch.nn.functional.rms_norm(torch.from_numpy(y).double(), (256,), eps=1e-6)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(y).double(), (2560,), eps=1e-6)
     want = O.bf16_round_bits(ref.numpy())
-    assert np.array_equal(got, want)
+    # FP32 rounding of r moves a value across a BF16 tie only very rarely, and
+    # then by one unit in the last place
+    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert diff.max() <= 1 and np.count_nonzero(diff) <= 2
     xs = O.bf16_bits_to_f32(got).astype(np.float64)
     assert np.allclose(np.sqrt(np.mean(xs * xs, axis=1)), 1.0, atol=1e-2)
+
+
+def test_rmsnorm_special_cases():
+    # constant rows: every element maps to sign(c) / sqrt(1 + eps/c^2)
+    y = np.array([[2.0] * 512, [-0.5] * 512], dtype=np.float32)
+    x = O.bf16_bits_to_f32(O.rmsnorm_bf16(y, 1e-6))
+    assert np.all(x[0] == 1.0) and np.all(x[1] == -1.0)
+    # a zero row stays zero (r = 1/sqrt(eps) times 0)
+    z = O.rmsnorm_bf16(np.zeros((1, 256), dtype=np.float32), 1e-6)
+    assert np.all(z == 0)
+    # scale invariance up to rounding: y and 4y (exact power of two) agree bit for bit
+    rng = np.random.default_rng(12)
+    y = rng.standard_normal((2, 768)).astype(np.float32)
+    assert np.array_equal(O.rmsnorm_bf16(y, 0.0), O.rmsnorm_bf16(4 * y, 0.0))
 
 
 def test_fp8_gemv_brute_force():

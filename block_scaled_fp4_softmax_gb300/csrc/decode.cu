@@ -245,12 +245,11 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(
 // ---------------------------------------------------------------------------
 namespace st {
 
-constexpr int kThreads = 512;      // warps 0-14 consume, warp 15 produces
+constexpr int kThreads = 512;      // warps 0-14 consume, warp 15 lanes 0-3 produce
 constexpr int kCWarps = 15;
 constexpr int kCThreads = kCWarps * 32;
-constexpr int kSlots = 6;
-constexpr int kSlotBytes = 24576;
-constexpr int kMaxChunkUnits = 1536;  // per-chunk partial sums kept in shared memory
+constexpr int kProdLanes = 4;
+constexpr int kMaxSlots = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Args {
@@ -264,47 +263,16 @@ struct Args {
   unsigned* bar;   // grid barrier words
   float* y;
   int32_t* status;
+  int slots;       // ring slots (<= kMaxSlots)
+  int slot_bytes;  // bytes per slot (multiple of 128)
+  int jn;          // experts per down-projection chunk
 };
-
-struct Geo {
-  int P, upr, updr, ch1, ch2;
-  long long r0, r1, q0, q1;  // this CTA's gate/up row pairs and output rows
-};
-
-// Rows per chunk: bounded by the slot size, by the partial-sum buffer and (for
-// gate/up) by one reduction warp per row pair.
-__host__ __device__ inline void chunk_rows(int H, int I, int G, int& ch1, int& ch2) {
-  const int b1 = 2 * (H / 2 + H / G);
-  ch1 = (kSlotBytes - 64) / b1;
-  ch1 = ch1 < kCWarps ? ch1 : kCWarps;
-  const int u1 = 2 * (H / 32);
-  ch1 = ch1 < kMaxChunkUnits / u1 ? ch1 : kMaxChunkUnits / u1;
-  ch1 = ch1 < 1 ? 1 : ch1;
-  ch2 = (kSlotBytes - 32) / (I / 2 + I / G);
-  ch2 = ch2 < 64 ? ch2 : 64;
-  ch2 = ch2 < kMaxChunkUnits / (I / 32) ? ch2 : kMaxChunkUnits / (I / 32);
-  ch2 = ch2 < 1 ? 1 : ch2;
-}
-
-__device__ __forceinline__ Geo geometry(const Args& a, int fmt) {
-  Geo g;
-  g.P = a.T * a.k;
-  g.upr = a.H >> 5;
-  g.updr = a.I >> 5;
-  chunk_rows(a.H, a.I, fmt == MOE_FMT_NVFP4 ? 16 : 32, g.ch1, g.ch2);
-  const long long R1 = (long long)g.P * a.I, R2 = (long long)a.T * a.H;
-  g.r0 = (long long)blockIdx.x * R1 / gridDim.x;
-  g.r1 = (long long)(blockIdx.x + 1) * R1 / gridDim.x;
-  g.q0 = (long long)blockIdx.x * R2 / gridDim.x;
-  g.q1 = (long long)(blockIdx.x + 1) * R2 / gridDim.x;
-  return g;
-}
 
 struct Win {  // 16-byte aligned window [lo, lo + bytes) around a byte range
   size_t lo;
   uint32_t bytes, delta;
 };
-__device__ __forceinline__ Win window(size_t start, size_t len) {
+__host__ __device__ inline Win window(size_t start, size_t len) {
   Win w;
   w.lo = start & ~(size_t)15;
   const size_t hi = (start + len + 15) & ~(size_t)15;
@@ -313,30 +281,42 @@ __device__ __forceinline__ Win window(size_t start, size_t len) {
   return w;
 }
 
-// One 16-byte unit of codes (32 elements) against activations held as float4
-// quads: quad qq (elements 4qq..4qq+3 of the unit) at act[qq * stride].  Four
-// independent accumulators (one per code word) keep the FMA chains short.
-template <int FMT, int STRIDE>
-__device__ __forceinline__ float unit_dot_q(uint4 q, uint32_t sbits, const float4* act, int stride_rt) {
-  const int stride = STRIDE > 0 ? STRIDE : stride_rt;
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float2 acc[4];
-#pragma unroll
-  for (int wi = 0; wi < 4; ++wi) {
-    acc[wi] = make_float2(0.f, 0.f);
-    const float4 x0 = act[(2 * wi) * stride];
-    const float4 x1 = act[(2 * wi + 1) * stride];
-    const float2 xp[4] = {make_float2(x0.x, x0.y), make_float2(x0.z, x0.w), make_float2(x1.x, x1.y),
-                          make_float2(x1.z, x1.w)};
-#pragma unroll
-    for (int bi = 0; bi < 4; ++bi) {
-      const uint32_t h2 = moe::e2m1x2_to_f16x2((w[wi] >> (8 * bi)) & 0xFFu);
-      const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      acc[wi] = moe::ffma2(wf, xp[bi], acc[wi]);
-    }
-  }
-  const float a = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-  const float b = (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+// Host and device agree on the chunk plan: a gate/up chunk is one row pair
+// (gate row | up row | gate scale window | up scale window); a down chunk is
+// one output row of one token for experts [j0, j0 + jn) (per expert: row of
+// codes | scale window).  The slot holds the larger of a gate/up chunk and
+// one expert row of down.
+__host__ __device__ inline int plan_slot_bytes(int H, int I, int G) {
+  const int p1 = 2 * (H / 2) + 2 * (H / G + 32);
+  const int p2 = I / 2 + I / G + 32;
+  const int s = p1 > p2 ? p1 : p2;
+  return (s + 127) & ~127;
+}
+__host__ __device__ inline int plan_jn(int k, int I, int G, int slot_bytes) {
+  const int j = slot_bytes / (I / 2 + I / G + 32);
+  return j < 1 ? 1 : (j > k ? k : j);
+}
+
+// FP16 x FP16 -> FP32 fused multiply-add (the product is exact in FP32).
+__device__ __forceinline__ float fma_h(uint32_t a_lo16, uint32_t b_lo16, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;"
+      : "=f"(d)
+      : "h"((uint16_t)(a_lo16 & 0xFFFFu)), "h"((uint16_t)(b_lo16 & 0xFFFFu)), "f"(c));
+  return d;
+}
+
+// 8 e2m1 codes (one word) -> 4 f16x2, element 2i in the low half of out[i].
+__device__ __forceinline__ void cvt_e2m1x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+template <int FMT>
+__device__ __forceinline__ float apply_scale(float a, float b, uint32_t sbits) {
   if (FMT == MOE_FMT_NVFP4) {
     const float2 s = moe::e4m3x2_to_f32x2(sbits);
     return a * s.x + b * s.y;
@@ -345,189 +325,271 @@ __device__ __forceinline__ float unit_dot_q(uint4 q, uint32_t sbits, const float
   }
 }
 
-// float element e of a unit-quad layout: quad (e%32)/4 at [quad][unit]
-__device__ __forceinline__ int quad_index(int e, int stride) {
-  return (((e & 31) >> 2) * stride + (e >> 5)) * 4 + (e & 3);
+// One unit (16 bytes = 32 codes) against FP16 activations: quad qq of the
+// unit (elements 8qq..8qq+7 as 4 f16x2) at xq[qq * stride].
+template <int FMT, int STRIDE>
+__device__ __forceinline__ float unit_dot_h(uint4 q, uint32_t sbits, const uint4* xq, int stride_rt) {
+  const int stride = STRIDE > 0 ? STRIDE : stride_rt;
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // two per scale block
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const uint4 xv4 = xq[wi * stride];
+    const uint32_t xv[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
+    uint32_t h[4];
+    cvt_e2m1x8(w[wi], h);
+    const int a0 = (wi >> 1) * 2;
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      acc[a0] = fma_h(h[bi], xv[bi], acc[a0]);
+      acc[a0 + 1] = fma_h(h[bi] >> 16, xv[bi] >> 16, acc[a0 + 1]);
+    }
+  }
+  return apply_scale<FMT>(acc[0] + acc[1], acc[2] + acc[3], sbits);
+}
+
+// The same against an FP32 operand carried as FP16 hi + lo parts.
+template <int FMT, int STRIDE>
+__device__ __forceinline__ float unit_dot_h2(uint4 q, uint32_t sbits, const uint4* hi, const uint4* lo,
+                                             int stride_rt) {
+  const int stride = STRIDE > 0 ? STRIDE : stride_rt;
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const uint4 h4 = hi[wi * stride], l4 = lo[wi * stride];
+    const uint32_t hv[4] = {h4.x, h4.y, h4.z, h4.w}, lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    uint32_t c[4];
+    cvt_e2m1x8(w[wi], c);
+    const int a0 = (wi >> 1) * 2;
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      acc[a0] = fma_h(c[bi], hv[bi], acc[a0]);
+      acc[a0 + 1] = fma_h(c[bi] >> 16, hv[bi] >> 16, acc[a0 + 1]);
+      acc[a0] = fma_h(c[bi], lv[bi], acc[a0]);
+      acc[a0 + 1] = fma_h(c[bi] >> 16, lv[bi] >> 16, acc[a0 + 1]);
+    }
+  }
+  return apply_scale<FMT>(acc[0] + acc[1], acc[2] + acc[3], sbits);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t scale_bits(const uint8_t* sp) {
+  return FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) : (uint32_t)sp[0];
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 template <int FMT, int UPR, int UPDR>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* ring = smem;                                          // kSlots x kSlotBytes
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSlots * kSlotBytes);
-  uint64_t* empty = full + kSlots;
-  const uint8_t** recs = reinterpret_cast<const uint8_t**>(empty + kSlots);  // [64]
-  float* wts = reinterpret_cast<float*>(recs + 64);                          // [64]
-  int* flags = reinterpret_cast<int*>(wts + 64);                             // [0] abort, [1] barrier ok
-  float* part = reinterpret_cast<float*>(flags + 4);                         // [2][kMaxChunkUnits]
-  float* yacc = part + 2 * kMaxChunkUnits;                                   // [rows/CTA + 1]
+  const int S = a.slots, SB = a.slot_bytes;
+  uint8_t* ring = smem;                                                   // S x SB
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * SB);
+  uint64_t* empty = full + kMaxSlots;
+  const uint8_t** recs = reinterpret_cast<const uint8_t**>(empty + kMaxSlots);  // [64]
+  float* wts = reinterpret_cast<float*>(recs + 64);                              // [64]
+  int* flags = reinterpret_cast<int*>(wts + 64);  // [0] abort, [1] barrier ok
+  // slot_fill[s]: the last chunk a producer started in slot s.  A barrier's
+  // parity is only meaningful once the slot is on the right fill: consumers
+  // first wait for slot_fill == chunk, producers for slot_fill == chunk - S.
+  volatile int* slot_fill = flags + 4;                                   // [kMaxSlots]
+  uint4* act = reinterpret_cast<uint4*>(flags + 4 + kMaxSlots);
   moe::pdl_launch_dependents();
 
-  const Geo g = geometry(a, FMT);
-  const int upr = UPR > 0 ? UPR : g.upr;
-  const int updr = UPDR > 0 ? UPDR : g.updr;
-  const int rows_cta = (int)(g.q1 - g.q0);
-  int* ybad = reinterpret_cast<int*>(yacc + rows_cta + 1);
-  float4* act = reinterpret_cast<float4*>(
-      (reinterpret_cast<uintptr_t>(ybad + rows_cta + 1) + 15) & ~(uintptr_t)15);
+  const int upr = UPR > 0 ? UPR : a.H >> 5;
+  const int updr = UPDR > 0 ? UPDR : a.I >> 5;
   const moe::RecordOffsets o = moe::record_offsets(a.H, a.I, FMT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
+  const int P = a.T * a.k;
+  const long long R1 = (long long)P * a.I, R2 = (long long)a.T * a.H;
+  const long long r0 = (long long)blockIdx.x * R1 / gridDim.x, r1 = (long long)(blockIdx.x + 1) * R1 / gridDim.x;
+  const long long q0 = (long long)blockIdx.x * R2 / gridDim.x, q1 = (long long)(blockIdx.x + 1) * R2 / gridDim.x;
+  const int jn = a.jn;
+  const int cpr = (a.k + jn - 1) / jn;  // down chunks per output row
+  const int n1 = (int)(r1 - r0);        // gate/up chunks of this CTA
+  const int n2 = (int)(q1 - q0) * cpr;  // down chunks of this CTA
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kMaxSlots; ++s) {
       moe::tc::mbar_init(&full[s], 1);
       moe::tc::mbar_init(&empty[s], 1);
+      slot_fill[s] = -1;
     }
     flags[0] = 0;
+    flags[1] = 0;
     moe::tc::mbar_fence_init();
   }
-  for (int r = threadIdx.x; r <= rows_cta; r += kThreads) {
-    yacc[r] = 0.f;
-    ybad[r] = 0;
-  }
   moe::pdl_wait();
-  if (threadIdx.x < g.P) {
+  if (threadIdx.x < P) {
     recs[threadIdx.x] = checked_record(a.idx[threadIdx.x], a.E, a.ptrs,
                                        blockIdx.x == 0 ? a.status : nullptr);
     wts[threadIdx.x] = a.w[threadIdx.x];
   }
-  // x of every token as float quads [t][8][H/32]
-  for (int h0 = threadIdx.x * 4; h0 < a.T * a.H; h0 += kThreads * 4) {
+  // x of every token as FP16 quads [t][4][H/32] (8 values per uint4)
+  for (int h0 = threadIdx.x * 8; h0 < a.T * a.H; h0 += kThreads * 8) {
     const int t = h0 / a.H, hh = h0 - t * a.H;
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(a.x + h0));
-    act[(size_t)t * 8 * upr + ((hh & 31) >> 2) * upr + (hh >> 5)] =
-        make_float4(moe::bf16_bits_to_f32(v.x & 0xFFFFu), moe::bf16_bits_to_f32(v.x >> 16),
-                    moe::bf16_bits_to_f32(v.y & 0xFFFFu), moe::bf16_bits_to_f32(v.y >> 16));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + h0));
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o4[i] = pack_h2(moe::bf16_bits_to_f32(wv[i] & 0xFFFFu), moe::bf16_bits_to_f32(wv[i] >> 16));
+    act[(size_t)t * 4 * upr + ((hh & 31) >> 3) * upr + (hh >> 5)] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
   }
   __syncthreads();
-
   volatile int* abort_flag = flags;
-  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
-  constexpr int sstep = 32 / G;
 
   if (warp == kCWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int c = 0;
+    // ------------------------------------------------------------ producers
+    if (lane < kProdLanes) {
       bool ok = true;
-      auto next_slot = [&](int& slot) -> bool {
-        slot = c % kSlots;
-        if (*abort_flag ||
-            !moe::tc::mbar_wait(&empty[slot], ((c / kSlots) & 1) ^ 1,
-                                moe::tc::globaltimer() + kWaitNs)) {
+      auto claim = [&](int chunk) -> bool {
+        const int slot = chunk % S;
+        const uint64_t dl = moe::tc::globaltimer() + kWaitNs;
+        bool good = !*abort_flag;
+        if (good && chunk >= S) {
+          while (slot_fill[slot] != chunk - S) {
+            if (*abort_flag || moe::tc::globaltimer() > dl) {
+              good = false;
+              break;
+            }
+            __nanosleep(32);
+          }
+        }
+        if (good) good = moe::tc::mbar_wait_backoff(&empty[slot], ((chunk / S) & 1) ^ 1, dl);
+        if (!good) {
           *abort_flag = 1;
           moe::status_or(a.status, MOE_DEV_TIMEOUT);
           return false;
         }
+        slot_fill[slot] = chunk;
         return true;
       };
-      for (long long r = g.r0; r < g.r1 && ok;) {
-        const int p = (int)(r / a.I), i0 = (int)(r - (long long)p * a.I);
-        const int n = (int)min((long long)g.ch1, min(g.r1 - r, (long long)(a.I - i0)));
-        int slot;
-        if (!(ok = next_slot(slot))) break;
-        const uint8_t* rec = recs[p];
-        const uint32_t base = moe::tc::smem_u32(ring + slot * kSlotBytes);
-        const uint32_t cb = (uint32_t)n * (a.H / 2);
-        const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
-        const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
-        moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? 2 * cb + gw.bytes + uw.bytes : 0);
-        if (rec) {
-          moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i0 * (a.H / 2), cb, &full[slot]);
-          moe::tc::bulk_g2s(base + cb, rec + o.up + (size_t)i0 * (a.H / 2), cb, &full[slot]);
-          moe::tc::bulk_g2s(base + 2 * cb, rec + gw.lo, gw.bytes, &full[slot]);
-          moe::tc::bulk_g2s(base + 2 * cb + gw.bytes, rec + uw.lo, uw.bytes, &full[slot]);
-        }
-        ++c;
-        r += n;
-      }
-      for (long long q = g.q0; q < g.q1 && ok;) {
-        const int t = (int)(q / a.H), n0 = (int)(q - (long long)t * a.H);
-        const int nr = (int)min((long long)g.ch2, min(g.q1 - q, (long long)(a.H - n0)));
-        for (int j = 0; j < a.k && ok; ++j) {
-          int slot;
-          if (!(ok = next_slot(slot))) break;
-          const uint8_t* rec = recs[t * a.k + j];
-          const uint32_t base = moe::tc::smem_u32(ring + slot * kSlotBytes);
-          const uint32_t cb = (uint32_t)nr * (a.I / 2);
-          const Win dw = window(o.down_s + (size_t)n0 * (a.I / G), (size_t)nr * (a.I / G));
-          moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? cb + dw.bytes : 0);
+      for (int c = lane; c < n1 + n2 && ok; c += kProdLanes) {
+        if (!(ok = claim(c))) break;
+        const int slot = c % S;
+        const uint32_t base = moe::tc::smem_u32(ring + (size_t)slot * SB);
+        if (c < n1) {  // gate/up row pair
+          const long long r = r0 + c;
+          const int p = (int)(r / a.I), i = (int)(r - (long long)p * a.I);
+          const uint8_t* rec = recs[p];
+          const uint32_t cb = (uint32_t)(a.H / 2);
+          const Win gw = window(o.gate_s + (size_t)i * (a.H / G), a.H / G);
+          const Win uw = window(o.up_s + (size_t)i * (a.H / G), a.H / G);
+          moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? 2 * cb + gw.bytes + uw.bytes : 0);
           if (rec) {
-            moe::tc::bulk_g2s(base, rec + o.down + (size_t)n0 * (a.I / 2), cb, &full[slot]);
-            moe::tc::bulk_g2s(base + cb, rec + dw.lo, dw.bytes, &full[slot]);
+            moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i * cb, cb, &full[slot]);
+            moe::tc::bulk_g2s(base + cb, rec + o.up + (size_t)i * cb, cb, &full[slot]);
+            moe::tc::bulk_g2s(base + 2 * cb, rec + gw.lo, gw.bytes, &full[slot]);
+            moe::tc::bulk_g2s(base + 2 * cb + gw.bytes, rec + uw.lo, uw.bytes, &full[slot]);
           }
-          ++c;
+        } else {  // down: one output row, experts [j0, j1)
+          const int c2 = c - n1;
+          const long long q = q0 + c2 / cpr;
+          const int t = (int)(q / a.H), n = (int)(q - (long long)t * a.H);
+          const int j0 = (c2 % cpr) * jn, j1 = min(a.k, j0 + jn);
+          const uint32_t cb = (uint32_t)(a.I / 2);
+          const Win dw = window(o.down_s + (size_t)n * (a.I / G), a.I / G);
+          uint32_t total = 0;
+          for (int j = j0; j < j1; ++j)
+            if (recs[t * a.k + j]) total += cb + dw.bytes;
+          moe::tc::mbar_arrive_expect_tx(&full[slot], total);
+          uint32_t off = 0;
+          for (int j = j0; j < j1; ++j) {
+            const uint8_t* rec = recs[t * a.k + j];
+            if (rec) {
+              moe::tc::bulk_g2s(base + off, rec + o.down + (size_t)n * cb, cb, &full[slot]);
+              moe::tc::bulk_g2s(base + off + cb, rec + dw.lo, dw.bytes, &full[slot]);
+            }
+            off += cb + dw.bytes;
+          }
         }
-        q += nr;
       }
-      // every issued copy must land before this CTA may exit
-      for (int cc = max(0, c - kSlots); cc < c; ++cc)
-        moe::tc::mbar_wait(&full[cc % kSlots], (cc / kSlots) & 1, moe::tc::globaltimer() + kWaitNs);
+      // every copy this lane issued must land before the CTA may exit
+      for (int c = lane; c < n1 + n2; c += kProdLanes)
+        if (c >= n1 + n2 - S)
+          moe::tc::mbar_wait_backoff(&full[c % S], (c / S) & 1, moe::tc::globaltimer() + kWaitNs);
     }
   } else {
     // ------------------------------------------------------------ consumers
-    // Control flow is the same for every consumer thread (fixed trip counts),
-    // so the named barriers always match; after a timeout the work is skipped.
-    const int ct = threadIdx.x;  // 0..479
-    int c = 0;
-    auto take = [&](int slot) -> bool {
+    auto take = [&](int chunk) -> bool {
       if (*abort_flag) return false;
-      if (!moe::tc::mbar_wait(&full[slot], (c / kSlots) & 1, moe::tc::globaltimer() + kWaitNs)) {
+      const uint64_t dl = moe::tc::globaltimer() + kWaitNs;
+      bool good = true;
+      while (slot_fill[chunk % S] != chunk) {
+        if (*abort_flag || moe::tc::globaltimer() > dl) {
+          good = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+      if (good) good = moe::tc::mbar_wait_backoff(&full[chunk % S], (chunk / S) & 1, dl);
+      if (!good) {
         *abort_flag = 1;
         moe::status_or(a.status, MOE_DEV_TIMEOUT);
         return false;
       }
       return true;
     };
-    // gate/up + SwiGLU: every consumer thread takes units of the chunk; one
-    // warp per row pair then adds the partial sums in a fixed order.
-    for (long long r = g.r0; r < g.r1;) {
-      const int p = (int)(r / a.I), i0 = (int)(r - (long long)p * a.I);
-      const int n = (int)min((long long)g.ch1, min(g.r1 - r, (long long)(a.I - i0)));
-      const int slot = c % kSlots;
-      float* pbuf = part + (c & 1) * kMaxChunkUnits;
-      const bool live = take(slot);
-      const uint8_t* base = ring + slot * kSlotBytes;
+    auto release = [&](int chunk) {
+      __syncwarp();
+      if (lane == 0) moe::tc::mbar_arrive(&empty[chunk % S]);
+    };
+    // gate/up + SwiGLU: chunk c (one row pair) -> warp c % 15
+    for (int c = warp; c < n1; c += kCWarps) {
+      const bool live = take(c);
+      const long long r = r0 + c;
+      const int p = (int)(r / a.I), i = (int)(r - (long long)p * a.I);
       const uint8_t* rec = recs[p];
-      const uint32_t cb = (uint32_t)n * (a.H / 2);
-      const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
-      const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)n * (a.H / G));
-      const float4* xt = act + (size_t)(p / a.k) * 8 * upr;
-      const int nunits = n * 2 * upr;
+      const uint8_t* base = ring + (size_t)(c % S) * SB;
+      const uint32_t cb = (uint32_t)(a.H / 2);
+      const Win gw = window(o.gate_s + (size_t)i * (a.H / G), a.H / G);
+      const Win uw = window(o.up_s + (size_t)i * (a.H / G), a.H / G);
+      const uint4* xt = act + (size_t)(p / a.k) * 4 * upr;
+      float gs = 0.f, us = 0.f;
       if (live && rec) {
-        for (int qf = ct; qf < nunits; qf += kCThreads) {
-          const int rr = qf / (2 * upr), rem = qf - rr * 2 * upr;
-          const bool is_up = rem >= upr;
-          const int cix = is_up ? rem - upr : rem;
-          const uint4 q = *reinterpret_cast<const uint4*>(base + (is_up ? cb : 0) + (size_t)rr * (a.H / 2) + 16 * cix);
-          const uint8_t* sp = base + 2 * cb + (is_up ? gw.bytes + uw.delta : gw.delta) + (size_t)rr * (a.H / G) + sstep * cix;
-          const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) : (uint32_t)sp[0];
-          pbuf[qf] = unit_dot_q<FMT, UPR>(q, sb, xt + cix, upr);
-        }
-      }
-      moe::tc::named_sync(1, kCThreads);
-      if (ct == 0) moe::tc::mbar_arrive(&empty[slot]);
-      if (warp < n) {
-        float hv = __uint_as_float(0x7FC00000u);
-        if (live && rec) {
-          const float* pr = pbuf + warp * 2 * upr;
-          float gs = 0.f, us = 0.f;
-          for (int u = lane; u < upr; u += 32) {
-            gs += pr[u];
-            us += pr[upr + u];
+        if constexpr (UPR > 0) {
+#pragma unroll
+          for (int m = 0; m < (2 * UPR + 31) / 32; ++m) {
+            const int u = lane + 32 * m;
+            if (u < 2 * UPR) {
+              const bool is_up = u >= UPR;
+              const int cix = is_up ? u - UPR : u;
+              const uint4 q = *reinterpret_cast<const uint4*>(base + (is_up ? cb : 0) + 16 * cix);
+              const uint8_t* sp = base + 2 * cb + (is_up ? gw.bytes + uw.delta : gw.delta) + sstep * cix;
+              const float d = unit_dot_h<FMT, UPR>(q, scale_bits<FMT>(sp), xt + cix, UPR);
+              if (is_up) us += d;
+              else gs += d;
+            }
           }
-          gs = moe::warp_sum(gs);
-          us = moe::warp_sum(us);
-          hv = gs / (1.0f + expf(-gs)) * us;
+        } else {
+          for (int u = lane; u < 2 * upr; u += 32) {
+            const bool is_up = u >= upr;
+            const int cix = is_up ? u - upr : u;
+            const uint4 q = *reinterpret_cast<const uint4*>(base + (is_up ? cb : 0) + 16 * cix);
+            const uint8_t* sp = base + 2 * cb + (is_up ? gw.bytes + uw.delta : gw.delta) + sstep * cix;
+            const float d = unit_dot_h<FMT, 0>(q, scale_bits<FMT>(sp), xt + cix, upr);
+            if (is_up) us += d;
+            else gs += d;
+          }
         }
-        if (lane == 0) a.hws[(size_t)p * a.I + i0 + warp] = hv;
       }
-      ++c;
-      r += n;
+      release(c);
+      gs = moe::warp_sum(gs);
+      us = moe::warp_sum(us);
+      if (lane == 0)
+        a.hws[(size_t)p * a.I + i] =
+            (live && rec) ? gs / (1.0f + expf(-gs)) * us : __uint_as_float(0x7FC00000u);
     }
     // grid barrier among the consumer threads of every CTA
     moe::tc::named_sync(1, kCThreads);
-    if (ct == 0) {
+    if (threadIdx.x == 0) {
       int good = !*abort_flag;
       if (good) {
         const unsigned e0 = moe::ld_acquire_gpu(a.bar + 1);
@@ -540,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
         } else {
           const uint64_t dl = moe::global_ns() + kWaitNs;
           while (moe::ld_acquire_gpu(a.bar + 1) == e0) {
+            __nanosleep(32);
             if (moe::global_ns() > dl) {
               good = 0;
               break;
@@ -555,77 +618,83 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
       flags[1] = good;
     }
     moe::tc::named_sync(1, kCThreads);
-    if (rows_cta > 0) {
-      // stage h of the tokens this CTA's output rows belong to, float quads
-      // [pair][8][I/32]
-      const int t_lo = (int)(g.q0 / a.H), t_hi = (int)((g.q1 - 1) / a.H);
-      const int n_q = (t_hi - t_lo + 1) * a.k * a.I / 4;
+    if (q1 > q0) {
+      // h of the tokens of this CTA's output rows as FP16 hi and lo quads:
+      // hi [pair][4][I/32], then lo at +npairs*4*(I/32)
+      const int t_lo = (int)(q0 / a.H), t_hi = (int)((q1 - 1) / a.H);
+      const int npairs = (t_hi - t_lo + 1) * a.k;
+      const int n8 = npairs * a.I / 8;
+      uint4* hhi = act;
+      uint4* hlo = act + (size_t)npairs * 4 * updr;
       const float4* src = reinterpret_cast<const float4*>(a.hws + (size_t)t_lo * a.k * a.I);
       if (flags[1]) {
-        for (int e4 = ct; e4 < n_q; e4 += kCThreads) {
-          const int e = 4 * e4;
+        for (int e8 = threadIdx.x; e8 < n8; e8 += kCThreads) {
+          const int e = 8 * e8;
           const int pj = e / a.I, i = e - pj * a.I;
-          act[(size_t)pj * 8 * updr + ((i & 31) >> 2) * updr + (i >> 5)] = __ldcg(src + e4);
+          const float4 v0 = __ldcg(src + 2 * e8), v1 = __ldcg(src + 2 * e8 + 1);
+          const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          uint32_t hv[4], lv[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const __half h0 = __float2half_rn(v[2 * m]), h1 = __float2half_rn(v[2 * m + 1]);
+            hv[m] = pack_h2(__half2float(h0), __half2float(h1));
+            lv[m] = pack_h2(v[2 * m] - __half2float(h0), v[2 * m + 1] - __half2float(h1));
+          }
+          const size_t at = (size_t)pj * 4 * updr + ((i & 31) >> 3) * updr + (i >> 5);
+          hhi[at] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          hlo[at] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
         }
       }
       moe::tc::named_sync(1, kCThreads);
-      // down + weighted combine: units over all consumer threads, then one
-      // thread per output row adds its partials in a fixed order
-      for (long long q = g.q0; q < g.q1;) {
-        const int t = (int)(q / a.H), n0 = (int)(q - (long long)t * a.H);
-        const int nr = (int)min((long long)g.ch2, min(g.q1 - q, (long long)(a.H - n0)));
-        for (int j = 0; j < a.k; ++j) {
-          const int slot = c % kSlots;
-          float* pbuf = part + (c & 1) * kMaxChunkUnits;
-          const bool live = take(slot);
-          const uint8_t* base = ring + slot * kSlotBytes;
-          const int pj = t * a.k + j;
-          const uint8_t* rec = recs[pj];
-          const uint32_t cb = (uint32_t)nr * (a.I / 2);
-          const Win dw = window(o.down_s + (size_t)n0 * (a.I / G), (size_t)nr * (a.I / G));
-          const float4* hcol = act + (size_t)(pj - t_lo * a.k) * 8 * updr;
-          const int nunits = nr * updr;
-          if (live && rec) {
-            for (int qf = ct; qf < nunits; qf += kCThreads) {
-              const int rr = qf / updr, u = qf - rr * updr;
-              const uint4 qv = *reinterpret_cast<const uint4*>(base + (size_t)rr * (a.I / 2) + 16 * u);
-              const uint8_t* sp = base + cb + dw.delta + (size_t)rr * (a.I / G) + sstep * u;
-              const uint32_t sb = FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) : (uint32_t)sp[0];
-              pbuf[qf] = unit_dot_q<FMT, UPDR>(qv, sb, hcol + u, updr);
+      // down + weighted combine: output row rr of this CTA -> warp rr % 15,
+      // which walks its row's chunks (experts in ascending order)
+      for (int rr = warp; rr < (int)(q1 - q0); rr += kCWarps) {
+        const long long q = q0 + rr;
+        const int t = (int)(q / a.H), n = (int)(q - (long long)t * a.H);
+        float acc = 0.f;
+        bool bad = false;
+        for (int cc = 0; cc < cpr; ++cc) {
+          const int c = n1 + rr * cpr + cc;
+          const bool live = take(c);
+          const uint8_t* base = ring + (size_t)(c % S) * SB;
+          const int j0 = cc * jn, j1 = min(a.k, j0 + jn);
+          const uint32_t cb = (uint32_t)(a.I / 2);
+          const Win dw = window(o.down_s + (size_t)n * (a.I / G), a.I / G);
+          const uint32_t per = cb + dw.bytes;  // bytes per expert in the slot
+          for (int j = j0; j < j1; ++j)
+            if (!(live && recs[t * a.k + j])) bad = true;
+          if (!bad) {
+            // units of experts j0..j1 flattened over the lanes
+            const int nu = (j1 - j0) * updr;
+            for (int f = lane; f < nu; f += 32) {
+              const int jj = f / updr, u = f - jj * updr;
+              const int pj = t * a.k + j0 + jj;
+              const uint8_t* eb = base + (size_t)jj * per;
+              const uint4 qv = *reinterpret_cast<const uint4*>(eb + 16 * u);
+              const uint8_t* sp = eb + cb + dw.delta + sstep * u;
+              const size_t col = (size_t)(pj - t_lo * a.k) * 4 * updr + u;
+              acc += wts[pj] * unit_dot_h2<FMT, UPDR>(qv, scale_bits<FMT>(sp), hhi + col, hlo + col, updr);
             }
           }
-          moe::tc::named_sync(1, kCThreads);
-          if (ct == 0) moe::tc::mbar_arrive(&empty[slot]);
-          if (ct < nr) {
-            const int yi = (int)(q - g.q0) + ct;
-            if (live && rec) {
-              const float* pr = pbuf + ct * updr;
-              float s = 0.f;
-              for (int u = 0; u < updr; ++u) s += pr[u];
-              yacc[yi] += wts[pj] * s;
-            } else {
-              ybad[yi] = 1;
-            }
-          }
-          ++c;
+          release(c);
         }
-        q += nr;
+        acc = moe::warp_sum(acc);
+        if (lane == 0)
+          a.y[(size_t)t * a.H + n] = (bad || *abort_flag) ? __uint_as_float(0x7FC00000u) : acc;
       }
-      moe::tc::named_sync(1, kCThreads);
-      for (int r = ct; r < rows_cta; r += kCThreads)
-        a.y[g.q0 + r] = (ybad[r] || *abort_flag) ? __uint_as_float(0x7FC00000u) : yacc[r];
     }
   }
   __syncthreads();
 }
 
-size_t smem_bytes(int T, int k, int H, int I, int sms) {
+// Shared memory for `slots` ring slots plus the activation region: x as FP16
+// quads (T*H halves) in phase 1, h as FP16 hi + lo quads in phase 2.
+inline size_t smem_bytes(int T, int k, int H, int I, int sms, int slots, int slot_bytes) {
   const long long R2 = (long long)T * H;
   const long long rows = (R2 + sms - 1) / sms + 1;
   const long long ntok = std::min<long long>(T, rows / H + 2);
-  const size_t act = std::max<size_t>((size_t)T * H * 4, (size_t)ntok * k * I * 4);
-  return (size_t)kSlots * kSlotBytes + 2 * kSlots * 8 + 64 * 8 + 64 * 4 + 16 +
-         2 * kMaxChunkUnits * 4 + (size_t)(rows + 1) * 8 + 16 + act;
+  const size_t act = std::max<size_t>((size_t)T * H * 2, (size_t)ntok * k * I * 4);
+  return (size_t)slots * slot_bytes + 2 * kMaxSlots * 8 + 64 * 8 + 64 * 4 + 16 + kMaxSlots * 4 + act;
 }
 
 }  // namespace st
@@ -679,11 +748,18 @@ int sm_count() {
   return sms;
 }
 
-// The streaming kernel takes T*k <= 64 pairs whose shared-memory plan fits.
-bool stream_fits(int T, int k, int H, int I) {
+// The streaming kernel takes T*k <= 64 pairs when at least 16 ring slots fit
+// next to the activations.
+int stream_slots(int T, int k, int H, int I, int fmt, int* slot_bytes) {
   const int sms = sm_count();
-  if (sms <= 0 || (long long)T * k > 64) return false;
-  return st::smem_bytes(T, k, H, I, sms) + 1024 <= (size_t)stream_smem_limit();
+  if (sms <= 0 || (long long)T * k > 64) return 0;
+  const int G = fmt == MOE_FMT_NVFP4 ? 16 : 32;
+  *slot_bytes = st::plan_slot_bytes(H, I, G);
+  const size_t limit = (size_t)stream_smem_limit();
+  const size_t fixed = st::smem_bytes(T, k, H, I, sms, 0, *slot_bytes) + 1024;
+  if (fixed >= limit) return 0;
+  const int slots = (int)std::min<size_t>(st::kMaxSlots, (limit - fixed) / *slot_bytes);
+  return slots >= 16 ? slots : 0;
 }
 
 template <int FMT, int UPR, int UPDR>
@@ -697,7 +773,7 @@ int launch_stream_shape(const st::Args& sa, size_t smem, int sms, cudaStream_t s
 template <int FMT>
 int launch_stream(const st::Args& sa, cudaStream_t stream) {
   const int sms = sm_count();
-  const size_t smem = st::smem_bytes(sa.T, sa.k, sa.H, sa.I, sms);
+  const size_t smem = st::smem_bytes(sa.T, sa.k, sa.H, sa.I, sms, sa.slots, sa.slot_bytes);
   // one CTA per SM: all CTAs are resident together, as the grid barrier needs.
   // The row strides are compile-time constants for the two model shapes.
   const int upr = sa.H / 32, updr = sa.I / 32;
@@ -728,8 +804,13 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
   if (!moe::aligned16(x_bf16) || !moe::aligned16(workspace)) return MOE_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
   float* hws = reinterpret_cast<float*>(workspace);
-  if (stream_fits(T, k, s.hidden, s.inter)) {
+  int slot_bytes = 0;
+  const int slots = stream_slots(T, k, s.hidden, s.inter, s.format, &slot_bytes);
+  if (slots > 0) {
     st::Args sa;
+    sa.slots = slots;
+    sa.slot_bytes = slot_bytes;
+    sa.jn = st::plan_jn(k, s.inter, s.format == MOE_FMT_NVFP4 ? 16 : 32, slot_bytes);
     sa.x = x_bf16;
     sa.idx = idx;
     sa.w = weights;

@@ -25,6 +25,8 @@
 //   warps 11-14     epilogue: tcgen05.ld from TMEM, SwiGLU or weighted combine
 // Every mbarrier wait is bounded by the global timer; a wait that runs out sets
 // MOE_DEV_TIMEOUT and the CTA drains and exits.
+#include <algorithm>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -45,7 +47,7 @@ constexpr int kLoaderDepth = 2;        // cp.async groups a loader keeps in flig
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 struct GroupedArgs {
-  const uint16_t* x;        // [T, H] BF16
+  const uint16_t* x;        // [T, H] BF16 (FP16 copy when use_f16: see below)
   const int32_t* pairs;     // [P] pair ids sorted by expert
   const int32_t* offsets;   // [E+1]
   const int32_t* ntile_off; // [E+1] exclusive scan of ceil(count/BN)
@@ -55,6 +57,16 @@ struct GroupedArgs {
   uint16_t* hbuf;           // [P, I] BF16, rows in sorted-pair order
   float* y;                 // [T, H] FP32 (zeroed before phase 1)
   int32_t* st;
+};
+
+// Phase 0 of NVFP4 runs as an FP16 x FP16 MMA: e2m1 x E4M3 scale is exact in
+// FP16 and takes one convert plus one packed multiply per pair; x is
+// converted once to FP16 (exact for BF16 values of magnitude in [2^-14,
+// 65504]; smaller ones round to FP16 subnormals, at most 2^-25 away).
+// MXFP4 scales (2^-127..2^127) do not fit FP16, so MXFP4 stays BF16.
+template <int FMT, int PHASE>
+struct OperandF16 {
+  static constexpr bool value = FMT == MOE_FMT_NVFP4 && PHASE == 0;
 };
 
 template <int PHASE>
@@ -130,8 +142,60 @@ __device__ __forceinline__ void dequant_unit(uint4 q, uint32_t sbits, bool poiso
   }
 }
 
+// Asks the L2 to fetch [src, src + bytes) ahead of use (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// One tile's weight rows are one contiguous block per matrix (codes and
+// scales); prefetch them into L2 so the per-k-step loads hit in L2.
+template <int FMT, int PHASE>
+__device__ __forceinline__ void prefetch_tile(const GroupedArgs& a, int tile, int MT, int total_tiles) {
+  if (tile >= total_tiles) return;
+  const TileInfo ti = tile_info(a, tile, MT);
+  const uint8_t* rec = tile_record(a, ti.e);
+  if (rec == nullptr) return;
+  const moe::RecordOffsets ro = moe::record_offsets(a.H, a.I, FMT);
+  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  const int K = PHASE == 0 ? a.H : a.I;
+  const size_t row0 = (size_t)ti.mt * BM;
+  const uint32_t cbytes = (uint32_t)(BM * (K / 2)), sbytes = (uint32_t)(BM * (K / G));
+  if (PHASE == 0) {
+    prefetch_l2(rec + ro.gate + row0 * (K / 2), cbytes);
+    prefetch_l2(rec + ro.up + row0 * (K / 2), cbytes);
+    prefetch_l2(rec + ro.gate_s + row0 * (K / G), sbytes);
+    prefetch_l2(rec + ro.up_s + row0 * (K / G), sbytes);
+  } else {
+    prefetch_l2(rec + ro.down + row0 * (K / 2), cbytes);
+    prefetch_l2(rec + ro.down_s + row0 * (K / G), sbytes);
+  }
+}
+
+// NVFP4 unit -> 32 FP16 (exact): hardware e2m1x2 -> f16x2, times the block's
+// E4M3 scale (as f16x2) in one packed multiply.
+__device__ __forceinline__ void dequant_unit_f16(uint4 q, uint32_t sbits, bool poison, uint4 (&out)[4]) {
+  uint32_t s2;
+  const uint16_t in = (uint16_t)(sbits & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(in));
+  uint32_t sc0 = (s2 & 0xFFFFu) * 0x10001u, sc1 = (s2 >> 16) * 0x10001u;  // broadcast halves
+  if (poison) sc0 = sc1 = 0x7E007E00u;                                    // f16x2 NaN
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const uint32_t sc = wi < 2 ? sc0 : sc1;
+    uint32_t o[4];
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      const uint32_t h2 = moe::e2m1x2_to_f16x2((w[wi] >> (8 * bi)) & 0xFFu);
+      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[bi]) : "r"(h2), "r"(sc));
+    }
+    out[wi] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 template <int FMT, int PHASE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
+  constexpr bool kF16 = OperandF16<FMT, PHASE>::value;
   using C = Cfg<PHASE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -187,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
         const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
         const int n_mma = max(16, (ti.count + 15) & ~15);
-        const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
+        const uint32_t idesc = kF16 ? idesc_f16_f32(BM, n_mma) : idesc_bf16_f32(BM, n_mma);
         if (*abort_flag || !mbar_wait(acc_empty, (lt & 1) ^ 1, globaltimer() + kWaitNs)) {
           fail();
           ok = false;
@@ -300,6 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
         const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
         cached_rec = tile_record(a, ti.e);
         cached_row = (size_t)ti.mt * BM + r;
+        if (pid == 0) {  // this tile (first time) and the next one into L2
+          if (lt == 0) prefetch_tile<FMT, PHASE>(a, blockIdx.x, MT, total_tiles);
+          prefetch_tile<FMT, PHASE>(a, blockIdx.x + (lt + 1) * gridDim.x, MT, total_tiles);
+        }
       }
       const uint8_t* rec = cached_rec;
       rec_of[slot] = rec;
@@ -348,8 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
 #pragma unroll
         for (int m = 0; m < C::NA; ++m) {
           uint4 out[4];
-          dequant_unit<FMT>(poison ? make_uint4(0, 0, 0, 0) : q[slot][m], poison ? 0u : sb[slot][m],
-                            poison, out);
+          if constexpr (kF16)
+            dequant_unit_f16(poison ? make_uint4(0, 0, 0, 0) : q[slot][m], poison ? 0u : sb[slot][m],
+                             poison, out);
+          else
+            dequant_unit<FMT>(poison ? make_uint4(0, 0, 0, 0) : q[slot][m], poison ? 0u : sb[slot][m],
+                              poison, out);
           uint8_t* row_base = sa + m * C::A_BYTES + r * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -472,6 +544,28 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const int32_t* __restri
   if (threadIdx.x == 0) ntile_off[E] = carry;
 }
 
+// x (BF16) -> FP16 for the NVFP4 gate/up MMA.  A magnitude at or above 65520
+// has no FP16 value: MOE_DEV_FP16_RANGE is set (the product rows become inf).
+__global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, long long n, uint16_t* __restrict__ x16,
+                                int32_t* __restrict__ st) {
+  bool bad = false;
+  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * 8; i < n;
+       i += (long long)gridDim.x * blockDim.x * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = moe::bf16_bits_to_f32(wv[j] & 0xFFFFu), hi = moe::bf16_bits_to_f32(wv[j] >> 16);
+      bad |= !(fabsf(lo) < 65520.f) || !(fabsf(hi) < 65520.f);
+      const __half2 h = __floats2half2_rn(lo, hi);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(x16 + i) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (bad) moe::status_or(st, MOE_DEV_FP16_RANGE);
+}
+
 // A pair whose expert index is outside [0, E) was dropped by the bucketing;
 // its token's output row is set to NaN so the error cannot pass silently.
 __global__ void poison_bad_pairs_kernel(const int32_t* __restrict__ idx, int P, int k, int E, int H,
@@ -488,7 +582,7 @@ __global__ void poison_bad_pairs_kernel(const int32_t* __restrict__ idx, int P, 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t counts, offsets, ntile, pairs, hbuf, bucket, total;
+  size_t counts, offsets, ntile, pairs, hbuf, x16, bucket, total;
 };
 
 WsLayout ws_layout(int T, int k, int E, const moe_expert_shape& s) {
@@ -500,6 +594,7 @@ WsLayout ws_layout(int T, int k, int E, const moe_expert_shape& s) {
   w.ntile = o;   o = align256(o + (size_t)(E + 1) * 4);
   w.pairs = o;   o = align256(o + P * 4);
   w.hbuf = o;    o = align256(o + P * (size_t)s.inter * 2);
+  w.x16 = o;     o = align256(o + (s.format == MOE_FMT_NVFP4 ? (size_t)T * s.hidden * 2 : 0));
   w.bucket = o;  o = align256(o + moe_bucket_workspace(T, k, E));
   w.total = o;
   return w;
@@ -574,7 +669,13 @@ extern "C" int moe_experts_grouped(const uint16_t* x_bf16, const int32_t* idx, c
   a.y = y;
   a.st = dev_status;
   if (s.format == MOE_FMT_NVFP4) {
-    rc = launch_phase<MOE_FMT_NVFP4, 0>(a, st);
+    uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + L.x16);
+    const long long n = (long long)T * s.hidden;
+    x_to_f16_kernel<<<(unsigned)std::min<long long>((n / 8 + 255) / 256, 1184), 256, 0, st>>>(
+        x_bf16, n, x16, dev_status);
+    GroupedArgs a0 = a;
+    a0.x = x16;
+    rc = launch_phase<MOE_FMT_NVFP4, 0>(a0, st);
     if (rc == MOE_OK) rc = launch_phase<MOE_FMT_NVFP4, 1>(a, st);
   } else {
     rc = launch_phase<MOE_FMT_MXFP4, 0>(a, st);

@@ -299,10 +299,14 @@ __global__ void __launch_bounds__(kClThreads) router_cluster_kernel(ClusterArgs 
     moe::tc::mbar_fence_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t bytes = (uint32_t)ne * a.H * 2;
-    moe::tc::mbar_arrive_expect_tx(wbar, bytes);
-    if (bytes) moe::tc::bulk_g2s(moe::tc::smem_u32(ws), a.wr + (size_t)e0 * a.H, bytes, wbar);
+  if (warp == 0) {
+    // one bulk copy per W_r row, spread over the lanes of warp 0
+    const uint32_t row_bytes = (uint32_t)a.H * 2;
+    if (lane == 0) moe::tc::mbar_arrive_expect_tx(wbar, (uint32_t)ne * row_bytes);
+    __syncwarp();
+    for (int q = lane; q < ne; q += 32)
+      moe::tc::bulk_g2s(moe::tc::smem_u32(ws + (size_t)q * a.H), a.wr + (size_t)(e0 + q) * a.H,
+                        row_bytes, wbar);
   }
   moe::pdl_launch_dependents();
   moe::pdl_wait();

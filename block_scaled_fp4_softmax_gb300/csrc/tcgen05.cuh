@@ -160,6 +160,13 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// Instruction descriptor, kind::f16: A and B FP16, D FP32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                    // D format: F32
+         | ((uint32_t)(N >> 3) << 17) // N / 8   (A, B format 0: F16)
+         | ((uint32_t)(M >> 4) << 24);// M / 16
+}
+
 // Instruction descriptor, kind::f16: A and B BF16, D FP32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                    // D format: F32

@@ -24,6 +24,7 @@ DEV_NULL_EXPERT = 1
 DEV_MISALIGNED = 2
 DEV_BAD_INDEX = 4
 DEV_TIMEOUT = 8
+DEV_FP16_RANGE = 16
 
 EXPORTS = (
     "moe_expert_record_bytes",

@@ -60,7 +60,8 @@ enum {
   MOE_DEV_NULL_EXPERT = 1, /* a selected expert's record pointer was NULL */
   MOE_DEV_MISALIGNED = 2,  /* a selected expert's record was not 16-byte aligned */
   MOE_DEV_BAD_INDEX = 4,   /* an expert index was outside [0, E) */
-  MOE_DEV_TIMEOUT = 8      /* a bounded wait inside a kernel gave up */
+  MOE_DEV_TIMEOUT = 8,     /* a bounded wait inside a kernel gave up */
+  MOE_DEV_FP16_RANGE = 16  /* prompt path, NVFP4: an activation's magnitude is >= 65520 */
 };
 
 /* Expert shape: hidden size H, intermediate size I, record format.
@@ -204,7 +205,11 @@ int moe_bucket_by_expert(const int32_t* idx, int T, int k, int E, int32_t* count
 size_t moe_experts_grouped_workspace(int T, int k, int E, moe_expert_shape s);
 
 /* Prompt path: the same layer for many tokens as a grouped contraction on
- * the tensor cores (tcgen05, BF16 operands, FP32 accumulation in TMEM).
+ * the tensor cores (tcgen05, FP32 accumulation in TMEM).  Gate/up operands
+ * are FP16 for NVFP4 records (weights exact; x converted from BF16, exact for
+ * magnitudes in [2^-14, 65504], below that rounded to an FP16 subnormal, at
+ * or above 65520 flagged with MOE_DEV_FP16_RANGE) and BF16 for MXFP4; the
+ * down projection is BF16.
  * Same arguments and output as moe_experts_decode, except:
  *  - the SwiGLU intermediate silu(g) * u is rounded to BF16 before the down
  *    projection (it is a BF16 MMA operand);

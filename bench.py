@@ -204,7 +204,10 @@ class PromptLayer:
         self.ws = torch.empty(moe.moe_experts_grouped_workspace(self.T, K_TOP, E, self.s),
                               dtype=torch.uint8, device=device)
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
-        self.flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+        # L2 flush by reading (not writing) a 512 MB buffer: a write sweep would
+        # leave the L2 full of dirty lines whose write-back lands in the next call
+        self.flush = torch.ones(512 << 18, dtype=torch.int32, device=device)
+        self.flush_out = torch.zeros((), dtype=torch.int64, device=device)
 
     def step(self):
         moe = self.moe
@@ -218,7 +221,7 @@ class PromptLayer:
         torch.cuda.synchronize()
         tot_step, tot_exp = 0.0, 0.0
         for i in range(steps):
-            self.flush.fill_(i & 0xFF)          # L2 flush: 512 MB write between steps
+            torch.sum(self.flush, dtype=torch.int64, out=self.flush_out)  # L2 flush (read sweep)
             a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             a.record()
             self.moe.moe_router_topk(self.x, self.wr, self.bias, K_TOP, self.idx, self.w, self.logits)
@@ -239,14 +242,15 @@ class PromptLayer:
                 "expert_weight_gbs": round(hit * self.pool.shape[1] / (ms_exp / 1e3) / 1e9, 1),
                 "experts_hit": hit, "max_tokens_per_expert": int(counts.max().item()),
                 "tokens": self.T, "dev_status": int(self.st.item()),
-                "l2": "flushed (512 MB write) between steps"}
+                "l2": "flushed between steps by reading a 512 MB buffer"}
 
 
 def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
     """FP8 row-scaled GEMV on the two proposed shapes; GB/s of W + x + y per
     call, L2 flushed between calls."""
     out = {}
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = torch.ones(512 << 18, dtype=torch.int32, device=device)   # read sweep evicts the L2
+    flush_out = torch.zeros((), dtype=torch.int64, device=device)
     for M, K in ((8192, 2560), (2560, 4096)):
         # enough distinct matrices that consecutive calls never share L2 lines
         n = max(2, (256 << 20) // (M * K) + 1)
@@ -259,7 +263,7 @@ def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
             moe.fp8_rowscale_gemv(ws[i % n], s, x, y)
         tot = 0.0
         for i in range(reps):
-            flush.fill_(i & 0xFF)
+            torch.sum(flush, dtype=torch.int64, out=flush_out)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             moe.fp8_rowscale_gemv(ws[i % n], s, x, y)
@@ -369,10 +373,11 @@ def run_ours(args):
     except Exception as exc:  # events inside graphs unsupported: time eagerly
         print(f"# graph events unavailable ({exc}); timing the expert pass eagerly", file=sys.stderr)
         samples = []
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        flush = torch.ones(256 << 18, dtype=torch.int32, device=dev)
+        flush_out = torch.zeros((), dtype=torch.int64, device=dev)
         for s in range(steps):
             L = s % LAYERS
-            torch.ops.aten.fill_(flush, s & 0xFF)
+            torch.sum(flush, dtype=torch.int64, out=flush_out)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()

@@ -221,7 +221,7 @@ class PromptLayer:
         torch.cuda.synchronize()
         tot_step, tot_exp = 0.0, 0.0
         for i in range(steps):
-            torch.sum(self.flush, dtype=torch.int64, out=self.flush_out)  # L2 flush (read sweep)
+            torch.sum(self.flush, 0, out=self.flush_out)  # L2 flush (read sweep)
             a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             a.record()
             self.moe.moe_router_topk(self.x, self.wr, self.bias, K_TOP, self.idx, self.w, self.logits)
@@ -263,7 +263,7 @@ def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
             moe.fp8_rowscale_gemv(ws[i % n], s, x, y)
         tot = 0.0
         for i in range(reps):
-            torch.sum(flush, dtype=torch.int64, out=flush_out)
+            torch.sum(flush, 0, out=flush_out)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             moe.fp8_rowscale_gemv(ws[i % n], s, x, y)
@@ -377,7 +377,7 @@ def run_ours(args):
         flush_out = torch.zeros((), dtype=torch.int64, device=dev)
         for s in range(steps):
             L = s % LAYERS
-            torch.sum(flush, dtype=torch.int64, out=flush_out)
+            torch.sum(flush, 0, out=flush_out)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()

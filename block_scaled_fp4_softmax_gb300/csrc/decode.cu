@@ -18,6 +18,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "decode_oneshot.h"
 #include "tcgen05.cuh"
 
 namespace {
@@ -784,10 +785,15 @@ int launch_stream(const st::Args& sa, cudaStream_t stream) {
 
 }  // namespace
 
-// h [T*k][I] FP32, then two barrier words (rounded up to 256 bytes).
+// Workspace: a header of counters (the one-shot kernel's 64-bit grid-barrier
+// counter at 0, the ring kernel's two barrier words at 128, the one-shot
+// kernel's combine counters at 256), then h [T*k][I] FP32, then the weighted
+// expert outputs [T*k][H] FP32 of the one-shot kernel.  The header sits at a
+// fixed place so that calls of any shape can share one workspace.
+constexpr size_t kRingBarrierOffset = 128;
 extern "C" size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s) {
   if (T <= 0 || k <= 0 || !moe::shape_ok(s)) return 0;
-  return (size_t)T * k * s.inter * sizeof(float) + 256;
+  return moe::os::kHeaderBytes + (size_t)T * k * (s.inter + s.hidden) * sizeof(float);
 }
 
 extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
@@ -803,7 +809,27 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
   if (ws_bytes < moe_experts_decode_workspace(T, k, s)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!moe::aligned16(x_bf16) || !moe::aligned16(workspace)) return MOE_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
-  float* hws = reinterpret_cast<float*>(workspace);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
+  if (decode_oneshot_fits(T, k, s.hidden, s.inter, s.format, sm_count(), (size_t)stream_smem_limit())) {
+    DecodeOneshotArgs oa;
+    oa.x = x_bf16;
+    oa.idx = idx;
+    oa.w = weights;
+    oa.T = T;
+    oa.k = k;
+    oa.ptrs = expert_ptrs;
+    oa.E = E;
+    oa.H = s.hidden;
+    oa.I = s.inter;
+    oa.bar = reinterpret_cast<unsigned long long*>(ws);
+    oa.cnt = reinterpret_cast<unsigned*>(ws + moe::os::kBarrierBytes);
+    oa.hws = hws;
+    oa.part = hws + (size_t)T * k * s.inter;
+    oa.y = y;
+    oa.status = dev_status;
+    return launch_decode_oneshot(oa, s.format, sm_count(), stream);
+  }
   int slot_bytes = 0;
   const int slots = stream_slots(T, k, s.hidden, s.inter, s.format, &slot_bytes);
   if (slots > 0) {
@@ -821,8 +847,7 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
     sa.H = s.hidden;
     sa.I = s.inter;
     sa.hws = hws;
-    sa.bar = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(workspace) +
-                                         (size_t)T * k * s.inter * sizeof(float));
+    sa.bar = reinterpret_cast<unsigned*>(ws + kRingBarrierOffset);
     sa.y = y;
     sa.status = dev_status;
     return s.format == MOE_FMT_NVFP4 ? launch_stream<MOE_FMT_NVFP4>(sa, st)
@@ -892,11 +917,9 @@ extern "C" int moe_experts_decode_noalloc(const uint16_t* x_bf16, const int32_t*
   void* scratch = nullptr;
   const int rc = static_scratch(&scratch);
   if (rc != MOE_OK) return rc;
-  // The array keeps whatever the previous call left; the barrier words sit
-  // right after this call's h and must start at zero.
-  const size_t bar_off = (size_t)T * k * s.inter * sizeof(float);
-  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + bar_off, 0, need - bar_off,
-                      (cudaStream_t)stream) != cudaSuccess)
+  // The array keeps whatever the previous call left; its header of barrier
+  // and combine counters must start at zero.
+  if (cudaMemsetAsync(scratch, 0, moe::os::kHeaderBytes, (cudaStream_t)stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return moe_experts_decode(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y, scratch,
                             kStaticScratchBytes, dev_status, stream);

@@ -1,0 +1,113 @@
+// Plan of the one-shot decode expert pass (T*k <= 64, each CTA's share of the
+// selected records fits in shared memory).  Host and device compute it with
+// the same code.
+//
+// Work split over a grid of one CTA per SM:
+//  - gate/up: the P*I row pairs (pair p = t*k + j, row i) in order, an equal
+//    share per CTA; a share is cut into segments (one pair each) and the
+//    segments into pieces of np rows;
+//  - down: the P*H rows (pair p, output row n) in order, an equal share per
+//    CTA, cut into segments (one pair each).
+// Every byte of a CTA's share is requested with a handful of large TMA bulk
+// copies at kernel entry (the copy engine of an SM completes only a few
+// copies per microsecond, so few and large is what keeps HBM busy).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+namespace os {
+
+constexpr int kThreads = 512;  // warps 0-14 compute, warp 15 loads
+constexpr int kCWarps = 15;
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kMaxPairs = 64;
+constexpr int kMaxPieces = 16;    // gate/up pieces of one CTA
+constexpr int kMaxSegs = 4;       // segments of one CTA, per phase
+constexpr int kPieceBytes = 16384;  // target bytes of one matrix in one piece
+constexpr uint32_t kMaxCopy = 32768;
+constexpr int kBlkStride = 64;    // combine counters per token
+constexpr size_t kBarrierBytes = 256;                        // grid-barrier counter
+constexpr size_t kCounterBytes = (size_t)64 * kBlkStride * 4;  // combine counters
+constexpr size_t kHeaderBytes = kBarrierBytes + kCounterBytes;
+
+__host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Geo {
+  int T, k, H, I, G, grid;
+  long long R1, D;    // gate/up row pairs, down rows
+  int rows1, rows2;   // most rows of one CTA, per phase
+  int segs1, segs2;   // most segments of one CTA, per phase
+  int np;             // rows per gate/up piece
+  int pieces2;        // partial sums one down row leaves (32-unit slices it touches)
+  int blk, nblk;      // combine block rows, blocks per token
+  // shared-memory regions (bytes from the start of dynamic shared memory)
+  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, off_part, total;
+};
+
+__host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid) {
+  Geo g;
+  g.T = T; g.k = k; g.H = H; g.I = I; g.G = G; g.grid = grid;
+  const long long P = (long long)T * k;
+  g.R1 = P * I;
+  g.D = P * H;
+  g.rows1 = (int)((g.R1 + grid - 1) / grid);
+  g.rows2 = (int)((g.D + grid - 1) / grid);
+  const long long s1 = (g.rows1 - 1) / I + 2, s2 = (g.rows2 - 1) / H + 2;
+  g.segs1 = (int)(s1 < P ? s1 : P);
+  g.segs2 = (int)(s2 < P ? s2 : P);
+  g.np = kPieceBytes / (H / 2);
+  if (g.np < 1) g.np = 1;
+  g.pieces2 = (I / 32 + 31) / 32 + 1;
+  int blk = (H + 63) / 64;
+  blk = blk < 128 ? 128 : blk;
+  g.blk = (blk + 31) / 32 * 32;
+  g.nblk = (H + g.blk - 1) / g.blk;
+  size_t o = 0;
+  g.off_bar = o;                                  // mbarriers: pieces, scales, down
+  o += (kMaxPieces + 2) * 8;
+  g.off_tab = o = round_up(o, 16);                // tables, weights, scales, flags
+  o += 4096;
+  g.off_codes1 = o = round_up(o, 128);
+  o += (size_t)g.rows1 * H;                       // gate + up codes
+  g.off_scales1 = o = round_up(o, 128);
+  o += 2 * ((size_t)g.rows1 * (H / G) + 32 * (size_t)g.segs1);
+  g.off_codes2 = o = round_up(o, 128);
+  o += (size_t)g.rows2 * (I / 2);
+  g.off_scales2 = o = round_up(o, 128);
+  o += (size_t)g.rows2 * (I / G) + 32 * (size_t)g.segs2;
+  g.off_act = o = round_up(o, 128);
+  const size_t a1 = (size_t)T * H * 2, a2 = (size_t)g.segs2 * I * 4;
+  o += a1 > a2 ? a1 : a2;
+  g.off_part = o = round_up(o, 128);
+  o += (size_t)g.rows2 * g.pieces2 * 4;
+  g.total = round_up(o, 128);
+  return g;
+}
+
+// Upper bound of the gate/up pieces of one CTA.
+__host__ __device__ inline int max_pieces(const Geo& g) { return (g.rows1 + g.np - 1) / g.np + g.segs1; }
+
+}  // namespace os
+}  // namespace moe
+
+// One-shot decode expert pass: true when the shape fits (the caller then
+// launches it with launch_decode_oneshot).
+bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit);
+
+struct DecodeOneshotArgs {
+  const uint16_t* x;
+  const int32_t* idx;
+  const float* w;
+  int T, k;
+  const void* const* ptrs;
+  int E, H, I;
+  unsigned long long* bar;  // grid-barrier counter (workspace start)
+  unsigned* cnt;            // combine counters [64][kBlkStride]
+  float* hws;               // [P][I] SwiGLU intermediate
+  float* part;              // [P][H] weighted expert outputs
+  float* y;
+  int32_t* status;
+};
+int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream);

@@ -461,7 +461,7 @@ def run_ours(args):
         "tokens_per_s": round(world * 1e3 / ms, 2),
         "hbm_frac": {"of_measured": round(value / world / peak, 4), "measured_gbs": peak,
                      "of_nominal_8000": round(value / world / 8000.0, 4)},
-        "roofline": {"bound": "hbm", "kernel": "moe_experts_decode: stream_kernel (TMA ring, gate/up + down in one launch)",
+        "roofline": {"bound": "hbm", "kernel": "moe_experts_decode: oneshot_kernel (one launch: TMA bulk copies, gate/up, grid barrier, down, last-arriver combine)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "peak_kind": peak_kind + " (burst copy)",
                      "frac": round(achieved / peak, 4),

@@ -40,13 +40,18 @@ struct Tab {
   unsigned amax[kMaxPairs];  // max |.| as float bits (x per token, then h per segment)
   float pw[kMaxSegs];        // per down segment: router weight * 2^-e of the FP16 scale of h
   int flags[4];              // [0] abort, [1] grid barrier passed
-  int npieces, nseg1, nseg2, nlast;
+  int npieces, nseg1, nseg2, nlast, ncopies;
   int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];
   uint32_t poff[kMaxPieces];  // piece: gate rows at codes1 + poff, up rows right after
   int sp[kMaxSegs], si0[kMaxSegs], sq0[kMaxSegs], sn[kMaxSegs];
   uint32_t gwo[kMaxSegs], uwo[kMaxSegs];  // first gate / up scale byte of the segment in scales1
   int dp[kMaxSegs], dn0[kMaxSegs], dz0[kMaxSegs], dn[kMaxSegs];
   uint32_t dso[kMaxSegs];                 // first down scale byte of the segment in scales2
+  // bulk copies: shared-memory destination (bytes from the dynamic base),
+  // source offset in the record, bytes, barrier, pair
+  uint64_t csrc[kMaxCopies];
+  uint32_t cdst[kMaxCopies], cbytes[kMaxCopies];
+  uint8_t cbar[kMaxCopies], cpair[kMaxCopies];
   int last[2 * kMaxSegs * 4];             // (token, block) pairs this CTA combines
 };
 static_assert(sizeof(Tab) <= 4096, "table region");
@@ -64,9 +69,27 @@ __host__ __device__ inline Win window(size_t start, size_t len) {
   return w;
 }
 
-// Fills the piece and segment tables of CTA b (no data dependence: runs
-// before the wait for the previous kernel).
-__device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& tb) {
+// Barriers: [0, npieces) one per gate/up piece, kBarScales the gate/up scale
+// windows, kBarDown the down rows and their scale windows.  Each completes
+// once per launch (parity 0).
+constexpr int kBarScales = kMaxPieces, kBarDown = kMaxPieces + 1, kNumBars = kMaxPieces + 2;
+
+// Plans CTA b: pieces, segments and bulk copies, and the arrival count of
+// each barrier (one per copy, plus one for the loader's lane 0).  No data
+// dependence: runs before the wait for the previous kernel.
+__device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& tb, uint32_t* counts) {
+  int nc = 0;
+  auto copy = [&](size_t dst, size_t src, uint32_t bytes, int bar, int pair) {
+    tb.cdst[nc] = (uint32_t)dst;
+    tb.csrc[nc] = src;
+    tb.cbytes[nc] = bytes;
+    tb.cbar[nc] = (uint8_t)bar;
+    tb.cpair[nc] = (uint8_t)pair;
+    ++counts[bar];
+    ++nc;
+  };
+  for (int i = 0; i < kNumBars; ++i) counts[i] = 1;
+  const size_t gsb = (size_t)(g.H / g.G), dsb = (size_t)(g.I / g.G), rb = (size_t)(g.H / 2), drb = (size_t)(g.I / 2);
   const long long r0 = (long long)b * g.R1 / g.grid, r1 = (long long)(b + 1) * g.R1 / g.grid;
   int np = 0, ns = 0;
   uint32_t coff = 0, soff = 0;
@@ -77,12 +100,13 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
     tb.sp[ns] = p;
     tb.si0[ns] = i0;
     tb.sq0[ns] = q0;
-    tb.sn[ns] = n;
-    const Win gw = window(o.gate_s + (size_t)i0 * (g.H / g.G), (size_t)n * (g.H / g.G));
+    const Win gw = window(o.gate_s + (size_t)i0 * gsb, (size_t)n * gsb);
     tb.gwo[ns] = soff + gw.delta;
+    copy(g.off_scales1 + soff, gw.lo, gw.bytes, kBarScales, p);
     soff += gw.bytes;
-    const Win uw = window(o.up_s + (size_t)i0 * (g.H / g.G), (size_t)n * (g.H / g.G));
+    const Win uw = window(o.up_s + (size_t)i0 * gsb, (size_t)n * gsb);
     tb.uwo[ns] = soff + uw.delta;
+    copy(g.off_scales1 + soff, uw.lo, uw.bytes, kBarScales, p);
     soff += uw.bytes;
     for (int a = 0; a < n && np < kMaxPieces; a += g.np) {
       const int m = min(g.np, n - a);
@@ -90,7 +114,10 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
       tb.pn[np] = m;
       tb.pseg[np] = ns;
       tb.poff[np] = coff;
-      coff += (uint32_t)m * g.H;
+      const uint32_t bytes = (uint32_t)(m * rb);
+      copy(g.off_codes1 + coff, o.gate + (size_t)(i0 + a) * rb, bytes, np, p);
+      copy(g.off_codes1 + coff + bytes, o.up + (size_t)(i0 + a) * rb, bytes, np, p);
+      coff += 2 * bytes;
       ++np;
     }
     ++ns;
@@ -99,83 +126,33 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
   tb.npieces = np;
   tb.nseg1 = ns;
   const long long d0 = (long long)b * g.D / g.grid, d1 = (long long)(b + 1) * g.D / g.grid;
+  const int rows_per_copy = (int)(kMaxCopy / drb);
   ns = 0;
   soff = 0;
   for (long long d = d0; d < d1 && ns < kMaxSegs;) {
     const int p = (int)(d / g.H), n0 = (int)(d - (long long)p * g.H);
     const int n = (int)min(d1 - d, (long long)(g.H - n0));
+    const int z0 = (int)(d - d0);
     tb.dp[ns] = p;
     tb.dn0[ns] = n0;
-    tb.dz0[ns] = (int)(d - d0);
+    tb.dz0[ns] = z0;
     tb.dn[ns] = n;
-    const Win dw = window(o.down_s + (size_t)n0 * (g.I / g.G), (size_t)n * (g.I / g.G));
+    for (int a = 0; a < n; a += rows_per_copy) {
+      const int m = min(rows_per_copy, n - a);
+      copy(g.off_codes2 + (size_t)(z0 + a) * drb, o.down + (size_t)(n0 + a) * drb, (uint32_t)(m * drb), kBarDown, p);
+    }
+    const Win dw = window(o.down_s + (size_t)n0 * dsb, (size_t)n * dsb);
     tb.dso[ns] = soff + dw.delta;
+    copy(g.off_scales2 + soff, dw.lo, dw.bytes, kBarDown, p);
     soff += dw.bytes;
     ++ns;
     d += n;
   }
   tb.nseg2 = ns;
+  tb.ncopies = nc;
   tb.nlast = 0;
   tb.flags[0] = 0;
   tb.flags[1] = 0;
-}
-
-// Lane 0 of warp 15: every copy of this CTA's share.  Barriers: [0, npieces)
-// one per gate/up piece, kMaxPieces the gate/up scale windows, kMaxPieces + 1
-// the down rows and their scale windows.  Each barrier completes once per
-// launch (parity 0).
-__device__ void issue_copies(const Geo& g, const RecordOffsets& o, const Tab& tb, uint8_t* smem,
-                             uint64_t* bars) {
-  const uint32_t s1 = tc::smem_u32(smem + g.off_scales1), c1 = tc::smem_u32(smem + g.off_codes1);
-  const uint32_t s2 = tc::smem_u32(smem + g.off_scales2), c2 = tc::smem_u32(smem + g.off_codes2);
-  const size_t gsb = (size_t)(g.H / g.G), dsb = (size_t)(g.I / g.G);
-  // gate/up scale windows first: small, and needed by the first piece
-  uint32_t tx = 0;
-  for (int s = 0; s < tb.nseg1; ++s)
-    if (tb.recs[tb.sp[s]]) {
-      tx += window(o.gate_s + (size_t)tb.si0[s] * gsb, (size_t)tb.sn[s] * gsb).bytes;
-      tx += window(o.up_s + (size_t)tb.si0[s] * gsb, (size_t)tb.sn[s] * gsb).bytes;
-    }
-  tc::mbar_arrive_expect_tx(&bars[kMaxPieces], tx);
-  for (int s = 0; s < tb.nseg1; ++s) {
-    const uint8_t* rec = tb.recs[tb.sp[s]];
-    if (!rec) continue;
-    const Win gw = window(o.gate_s + (size_t)tb.si0[s] * gsb, (size_t)tb.sn[s] * gsb);
-    const Win uw = window(o.up_s + (size_t)tb.si0[s] * gsb, (size_t)tb.sn[s] * gsb);
-    tc::bulk_g2s(s1 + tb.gwo[s] - gw.delta, rec + gw.lo, gw.bytes, &bars[kMaxPieces]);
-    tc::bulk_g2s(s1 + tb.uwo[s] - uw.delta, rec + uw.lo, uw.bytes, &bars[kMaxPieces]);
-  }
-  // gate/up code pieces, in row order
-  const uint32_t rb = (uint32_t)(g.H / 2);
-  for (int pi = 0; pi < tb.npieces; ++pi) {
-    const int s = tb.pseg[pi];
-    const uint8_t* rec = tb.recs[tb.sp[s]];
-    const uint32_t bytes = (uint32_t)tb.pn[pi] * rb;
-    tc::mbar_arrive_expect_tx(&bars[pi], rec ? 2 * bytes : 0);
-    if (!rec) continue;
-    const size_t i = (size_t)tb.si0[s] + (tb.pq0[pi] - tb.sq0[s]);
-    tc::bulk_g2s(c1 + tb.poff[pi], rec + o.gate + i * rb, bytes, &bars[pi]);
-    tc::bulk_g2s(c1 + tb.poff[pi] + bytes, rec + o.up + i * rb, bytes, &bars[pi]);
-  }
-  // down rows and scale windows
-  const uint32_t drb = (uint32_t)(g.I / 2);
-  tx = 0;
-  for (int s = 0; s < tb.nseg2; ++s)
-    if (tb.recs[tb.dp[s]])
-      tx += (uint32_t)tb.dn[s] * drb + window(o.down_s + (size_t)tb.dn0[s] * dsb, (size_t)tb.dn[s] * dsb).bytes;
-  tc::mbar_arrive_expect_tx(&bars[kMaxPieces + 1], tx);
-  const int rows_per_copy = (int)(kMaxCopy / drb);
-  for (int s = 0; s < tb.nseg2; ++s) {
-    const uint8_t* rec = tb.recs[tb.dp[s]];
-    if (!rec) continue;
-    for (int a = 0; a < tb.dn[s]; a += rows_per_copy) {
-      const int m = min(rows_per_copy, tb.dn[s] - a);
-      tc::bulk_g2s(c2 + (uint32_t)(tb.dz0[s] + a) * drb, rec + o.down + (size_t)(tb.dn0[s] + a) * drb,
-                   (uint32_t)m * drb, &bars[kMaxPieces + 1]);
-    }
-    const Win dw = window(o.down_s + (size_t)tb.dn0[s] * dsb, (size_t)tb.dn[s] * dsb);
-    tc::bulk_g2s(s2 + tb.dso[s] - dw.delta, rec + dw.lo, dw.bytes, &bars[kMaxPieces + 1]);
-  }
 }
 
 // Waits (bounded) for one barrier's parity-0 phase; on timeout flags the
@@ -208,14 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const uint8_t* codes2 = smem + g.off_codes2;
   const uint8_t* scales2 = smem + g.off_scales2;
   uint4* act = reinterpret_cast<uint4*>(smem + g.off_act);
-  float* part = reinterpret_cast<float*>(smem + g.off_part);
   volatile int* abort_flag = tb.flags;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kMaxPieces + 2; ++i) tc::mbar_init(&bars[i], 1);
+    uint32_t counts[kNumBars];
+    build_tables(g, blockIdx.x, o, tb, counts);
+    for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], counts[i]);
     tc::mbar_fence_init();
   }
-  if (threadIdx.x == 32) build_tables(g, blockIdx.x, o, tb);
   if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
   // the pointer table does not depend on the previous kernel: warm L2 with it
   for (int i = threadIdx.x; i < (a.E * 8 + 127) / 128; i += kThreads)
@@ -231,13 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     }
     __syncwarp();
     asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");  // records are in place
+    // one copy per lane; a copy of a missing record still arrives (0 bytes)
+    const uint32_t base = tc::smem_u32(smem);
+    for (int c = lane; c < tb.ncopies; c += 32) {
+      const uint8_t* rec = tb.recs[tb.cpair[c]];
+      uint64_t* bar = &bars[tb.cbar[c]];
+      tc::mbar_arrive_expect_tx(bar, rec ? tb.cbytes[c] : 0u);
+      if (rec) tc::bulk_g2s(base + tb.cdst[c], rec + tb.csrc[c], tb.cbytes[c], bar);
+    }
     if (lane == 0) {
-      issue_copies(g, o, tb, smem, bars);
+      for (int i = 0; i < kNumBars; ++i) tc::mbar_arrive(&bars[i]);
       // no copy may still be in flight when the CTA exits
       const uint64_t dl = tc::globaltimer() + kWaitNs;
-      for (int i = 0; i < tb.npieces; ++i) tc::mbar_wait_backoff(&bars[i], 0, dl);
-      tc::mbar_wait_backoff(&bars[kMaxPieces], 0, dl);
-      tc::mbar_wait_backoff(&bars[kMaxPieces + 1], 0, dl);
+      for (int i = 0; i < kNumBars; ++i) tc::mbar_wait_backoff(&bars[i], 0, dl);
     }
     __syncthreads();
     return;
@@ -296,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     const int p = tb.sp[s], t = p / a.k;
     const uint8_t* rec = tb.recs[p];
     bool ok = rec != nullptr;
-    if (ok && !scales_in) ok = scales_in = await(&bars[kMaxPieces], tb, a.status);
+    if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status);
     if (ok) ok = await(&bars[pi], tb, a.status);
     float gs = 0.f, us = 0.f;
     if (ok) {
@@ -373,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const int nz = (int)(d1 - d0);
   uint4* hhi = act;
   uint4* hlo = act + (size_t)g.segs2 * 4 * updr;
-  for (int i = threadIdx.x; i < nz * g.pieces2; i += kCThreads) part[i] = 0.f;
   const bool have_h = tb.flags[1] != 0;
   {
     const int n8 = tb.nseg2 * (a.I / 8);
@@ -443,78 +425,72 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   }
   tc::named_sync(1, kCThreads);
 
-  // down: 32-unit slices of the (row, unit) space of this CTA's down rows,
-  // two slices per warp at a time; a segmented scan over the lanes of one row
-  // leaves the row's partial for that slice
-  const int NU = nz * updr;
-  const int nsl = (NU + 31) / 32;
-  const bool down_in = have_h && nsl > 0 && await(&bars[kMaxPieces + 1], tb, a.status);
-  auto unit_value = [&](int U, int& z) -> float {
-    if (U >= NU) {
-      z = -1;
-      return 0.f;
-    }
-    z = U / updr;
-    const int u = U - z * updr;
-    int s = 0;
-    while (s + 1 < tb.nseg2 && tb.dz0[s + 1] <= z) ++s;
-    if (!down_in || !tb.recs[tb.dp[s]]) return __uint_as_float(0x7FC00000u);
-    const uint4 qv = *reinterpret_cast<const uint4*>(codes2 + (size_t)z * (a.I / 2) + 16 * u);
-    const uint8_t* sp = scales2 + tb.dso[s] + (size_t)(z - tb.dz0[s]) * (a.I / G) + sstep * u;
-    const size_t col = (size_t)s * 4 * updr + u;
-    return dm::unit_dot_h2<FMT, UPDR>(qv, dm::scale_bits<FMT>(sp), hhi + col, hlo + col, updr);
-  };
-  auto store = [&](int sl, int z, float val) {
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const float tv = __shfl_up_sync(0xffffffffu, val, d);
-      const int tz = __shfl_up_sync(0xffffffffu, z, d);
-      if (lane >= d && tz == z) val += tv;
-    }
-    const int zn = __shfl_down_sync(0xffffffffu, z, 1);
-    if (z >= 0 && (lane == 31 || zn != z)) part[(size_t)z * g.pieces2 + sl - (z * updr) / 32] = val;
-  };
-  for (int sl = warp; sl < nsl; sl += 2 * kCWarps) {
-    const int sl2 = sl + kCWarps;
-    int za, zb;
-    const float va = unit_value(sl * 32 + lane, za);
-    const float vb = unit_value(sl2 < nsl ? sl2 * 32 + lane : NU, zb);
-    store(sl, za, va);
-    if (sl2 < nsl) store(sl2, zb, vb);
-  }
-  tc::named_sync(1, kCThreads);
-  // each row: its partials in slice order, times the router weight
-  for (int z = threadIdx.x; z < nz; z += kCThreads) {
-    int s = 0;
-    while (s + 1 < tb.nseg2 && tb.dz0[s + 1] <= z) ++s;
+  // down: each down row to a group of L lanes (L a power of two), lane sub of
+  // the group taking units sub, sub + L, ...; the group's sum is reduced over
+  // its lanes in a fixed order and the row's weighted output goes to global
+  // scratch.  32 / L rows per warp pass, passes round-robin over the warps.
+  constexpr int kUnitsPerLane = 5;
+  int L = 1;
+  while (L < 32 && L * kUnitsPerLane < updr) L <<= 1;
+  const int rows_per_pass = 32 / L;
+  const int npass = (nz + rows_per_pass - 1) / rows_per_pass;
+  const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], tb, a.status);
+  const int sub = lane & (L - 1);
+  int ds = 0;  // a lane's segment only grows, as its rows do
+  for (int ps = warp; ps < npass; ps += kCWarps) {
+    const int z = ps * rows_per_pass + lane / L;
     float v = 0.f;
-    for (int i = 0; i < g.pieces2; ++i) v += part[(size_t)z * g.pieces2 + i];
-    a.part[(size_t)tb.dp[s] * a.H + tb.dn0[s] + (z - tb.dz0[s])] = *abort_flag ? __uint_as_float(0x7FC00000u)
-                                                                                : tb.pw[s] * v;
-  }
-  __threadfence();
-  tc::named_sync(1, kCThreads);
-  // combine: count this CTA's rows into each block of output rows it touches;
-  // the CTA that completes a block adds the block's k expert outputs
-  if (threadIdx.x == 0) {
-    int nl = 0;
-    for (int s = 0; s < tb.nseg2; ++s) {
-      const int t = tb.dp[s] / a.k, n0 = tb.dn0[s], n1 = n0 + tb.dn[s];
-      for (int b = n0 / g.blk; b * g.blk < n1; ++b) {
-        const int lo = max(n0, b * g.blk), hi = min(n1, (b + 1) * g.blk);
-        const unsigned rows = (unsigned)(min(a.H, (b + 1) * g.blk) - b * g.blk);
-        const unsigned target = (unsigned)a.k * rows;
-        unsigned* c = a.cnt + (size_t)t * kBlkStride + b;
-        const unsigned now = atomicAdd(c, (unsigned)(hi - lo)) + (unsigned)(hi - lo);
-        if (now == target) {
-          atomicExch(c, 0u);
-          tb.last[nl++] = t * kBlkStride + b;
-        } else if (now > target) {
-          status_or(a.status, MOE_DEV_WORKSPACE);
+    if (z < nz) {
+      while (ds + 1 < tb.nseg2 && tb.dz0[ds + 1] <= z) ++ds;
+      if (!down_in || !tb.recs[tb.dp[ds]]) {
+        v = __uint_as_float(0x7FC00000u);
+      } else {
+        const uint8_t* crow = codes2 + (size_t)z * (a.I / 2);
+        const uint8_t* srow = scales2 + tb.dso[ds] + (size_t)(z - tb.dz0[ds]) * (a.I / G);
+        const uint4* hs = hhi + (size_t)ds * 4 * updr;
+        const uint4* ls = hlo + (size_t)ds * 4 * updr;
+        if constexpr (UPDR > 0) {
+          constexpr int kL = [] { int l = 1; while (l < 32 && l * kUnitsPerLane < UPDR) l <<= 1; return l; }();
+#pragma unroll
+          for (int m = 0; m < (UPDR + kL - 1) / kL; ++m) {
+            const int u = sub + kL * m;
+            if (u < UPDR)
+              v += dm::unit_dot_h2<FMT, UPDR>(*reinterpret_cast<const uint4*>(crow + 16 * u),
+                                              dm::scale_bits<FMT>(srow + sstep * u), hs + u, ls + u, UPDR);
+          }
+        } else {
+          for (int u = sub; u < updr; u += L)
+            v += dm::unit_dot_h2<FMT, 0>(*reinterpret_cast<const uint4*>(crow + 16 * u),
+                                         dm::scale_bits<FMT>(srow + sstep * u), hs + u, ls + u, updr);
         }
       }
     }
-    tb.nlast = nl;
+    for (int d = L >> 1; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    if (z < nz && sub == 0)
+      a.part[(size_t)tb.dp[ds] * a.H + tb.dn0[ds] + (z - tb.dz0[ds])] =
+          *abort_flag ? __uint_as_float(0x7FC00000u) : tb.pw[ds] * v;
+  }
+  __threadfence();
+  tc::named_sync(1, kCThreads);
+  // combine: count this CTA's rows into each block of output rows it touches
+  // (one thread per down segment); the CTA that completes a block adds the
+  // block's k expert outputs in expert order
+  if (threadIdx.x < tb.nseg2) {
+    const int s = threadIdx.x;
+    const int t = tb.dp[s] / a.k, n0 = tb.dn0[s], n1r = n0 + tb.dn[s];
+    for (int b = n0 / g.blk; b * g.blk < n1r; ++b) {
+      const int lo = max(n0, b * g.blk), hi = min(n1r, (b + 1) * g.blk);
+      const unsigned rows = (unsigned)(min(a.H, (b + 1) * g.blk) - b * g.blk);
+      const unsigned target = (unsigned)a.k * rows;
+      unsigned* c = a.cnt + (size_t)t * kBlkStride + b;
+      const unsigned now = atomicAdd(c, (unsigned)(hi - lo)) + (unsigned)(hi - lo);
+      if (now == target) {
+        atomicExch(c, 0u);
+        tb.last[atomicAdd(&tb.nlast, 1)] = t * kBlkStride + b;
+      } else if (now > target) {
+        status_or(a.status, MOE_DEV_WORKSPACE);
+      }
+    }
     __threadfence();
   }
   tc::named_sync(1, kCThreads);

@@ -25,6 +25,7 @@ constexpr int kCThreads = kCWarps * 32;
 constexpr int kMaxPairs = 64;
 constexpr int kMaxPieces = 16;    // gate/up pieces of one CTA
 constexpr int kMaxSegs = 4;       // segments of one CTA, per phase
+constexpr int kMaxCopies = 48;    // bulk copies of one CTA
 constexpr int kPieceBytes = 16384;  // target bytes of one matrix in one piece
 constexpr uint32_t kMaxCopy = 32768;
 constexpr int kBlkStride = 64;    // combine counters per token
@@ -40,10 +41,10 @@ struct Geo {
   int rows1, rows2;   // most rows of one CTA, per phase
   int segs1, segs2;   // most segments of one CTA, per phase
   int np;             // rows per gate/up piece
-  int pieces2;        // partial sums one down row leaves (32-unit slices it touches)
+  int copies;         // most bulk copies of one CTA
   int blk, nblk;      // combine block rows, blocks per token
   // shared-memory regions (bytes from the start of dynamic shared memory)
-  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, off_part, total;
+  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, total;
 };
 
 __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid) {
@@ -59,7 +60,9 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   g.segs2 = (int)(s2 < P ? s2 : P);
   g.np = kPieceBytes / (H / 2);
   if (g.np < 1) g.np = 1;
-  g.pieces2 = (I / 32 + 31) / 32 + 1;
+  const int rows_per_copy = (int)(kMaxCopy / (I / 2));
+  g.copies = 2 * ((g.rows1 + g.np - 1) / g.np + g.segs1) + 2 * g.segs1 +
+             (g.rows2 + rows_per_copy - 1) / rows_per_copy + 2 * g.segs2;
   int blk = (H + 63) / 64;
   blk = blk < 128 ? 128 : blk;
   g.blk = (blk + 31) / 32 * 32;
@@ -80,8 +83,6 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   g.off_act = o = round_up(o, 128);
   const size_t a1 = (size_t)T * H * 2, a2 = (size_t)g.segs2 * I * 4;
   o += a1 > a2 ? a1 : a2;
-  g.off_part = o = round_up(o, 128);
-  o += (size_t)g.rows2 * g.pieces2 * 4;
   g.total = round_up(o, 128);
   return g;
 }

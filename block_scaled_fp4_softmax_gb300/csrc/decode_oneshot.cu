@@ -473,25 +473,29 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   __threadfence();
   tc::named_sync(1, kCThreads);
   // combine: count this CTA's rows into each block of output rows it touches
-  // (one thread per down segment); the CTA that completes a block adds the
-  // block's k expert outputs in expert order
-  if (threadIdx.x < tb.nseg2) {
-    const int s = threadIdx.x;
-    const int t = tb.dp[s] / a.k, n0 = tb.dn0[s], n1r = n0 + tb.dn[s];
-    for (int b = n0 / g.blk; b * g.blk < n1r; ++b) {
-      const int lo = max(n0, b * g.blk), hi = min(n1r, (b + 1) * g.blk);
-      const unsigned rows = (unsigned)(min(a.H, (b + 1) * g.blk) - b * g.blk);
-      const unsigned target = (unsigned)a.k * rows;
-      unsigned* c = a.cnt + (size_t)t * kBlkStride + b;
-      const unsigned now = atomicAdd(c, (unsigned)(hi - lo)) + (unsigned)(hi - lo);
-      if (now == target) {
-        atomicExch(c, 0u);
-        tb.last[atomicAdd(&tb.nlast, 1)] = t * kBlkStride + b;
-      } else if (now > target) {
-        status_or(a.status, MOE_DEV_WORKSPACE);
+  // (one thread per (segment, block), all atomics in flight together); the
+  // CTA that completes a block adds the block's k expert outputs in expert
+  // order
+  {
+    int j = 0;
+    for (int s = 0; s < tb.nseg2; ++s) {
+      const int t = tb.dp[s] / a.k, n0 = tb.dn0[s], n1r = n0 + tb.dn[s];
+      for (int b = n0 / g.blk; b * g.blk < n1r; ++b, ++j) {
+        if (j != threadIdx.x) continue;
+        const int lo = max(n0, b * g.blk), hi = min(n1r, (b + 1) * g.blk);
+        const unsigned rows = (unsigned)(min(a.H, (b + 1) * g.blk) - b * g.blk);
+        const unsigned target = (unsigned)a.k * rows;
+        unsigned* c = a.cnt + (size_t)t * kBlkStride + b;
+        const unsigned now = atomicAdd(c, (unsigned)(hi - lo)) + (unsigned)(hi - lo);
+        if (now == target) {
+          atomicExch(c, 0u);
+          tb.last[atomicAdd(&tb.nlast, 1)] = t * kBlkStride + b;
+        } else if (now > target) {
+          status_or(a.status, MOE_DEV_WORKSPACE);
+        }
+        __threadfence();
       }
     }
-    __threadfence();
   }
   tc::named_sync(1, kCThreads);
   for (int l = 0; l < tb.nlast; ++l) {

@@ -139,7 +139,7 @@ class DecodeStack:
                               device=device)
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         self.setup_s = time.time() - t0
-        self.kernels_per_step = LAYERS * 2
+        self.kernels_per_step = LAYERS * 3
         self.ev = None
 
     def expert_bytes_per_step(self):
@@ -457,7 +457,7 @@ def run_ours(args):
                    "expert_bytes_per_step": wl.expert_bytes_per_step(),
                    "l2": "inputs larger than L2: 1.33 GB of distinct expert records per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph, 2 kernels per layer (cluster router with RMS chaining; streaming expert pass), programmatic dependent launch"},
+                   "launch": "CUDA graph, 3 kernels per layer (router logits with RMS chaining on every SM; top-k; one-shot expert pass), programmatic dependent launch"},
         "tokens_per_s": round(world * 1e3 / ms, 2),
         "hbm_frac": {"of_measured": round(value / world / peak, 4), "measured_gbs": peak,
                      "of_nominal_8000": round(value / world / 8000.0, 4)},

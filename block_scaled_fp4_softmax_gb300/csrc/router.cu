@@ -7,7 +7,6 @@
 // waits on the router's answer, so routing stays on the device here and no
 // index ever travels to the host.
 #include "common.cuh"
-#include "tcgen05.cuh"
 
 namespace {
 
@@ -185,9 +184,14 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ yr, int H, float eps,
                                                      float* part) {
   float acc = 0.0f;
-  for (int i = threadIdx.x; i < H; i += 256) {
-    const float v = yr[i];
-    acc = __fadd_rn(acc, __fmul_rn(v, v));
+  constexpr int kBatch = 8;  // loads in flight; the adds keep the order above
+  for (int i0 = threadIdx.x; i0 < H; i0 += 256 * kBatch) {
+    float v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) v[b] = i0 + 256 * b < H ? yr[i0 + 256 * b] : 0.0f;
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+      if (i0 + 256 * b < H) acc = __fadd_rn(acc, __fmul_rn(v[b], v[b]));
   }
   part[threadIdx.x] = acc;
   __syncthreads();
@@ -219,224 +223,157 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
 }
 
 // ---------------------------------------------------------------------------
-// Small-T router in one launch: a cluster of kCl CTAs.  Each CTA pulls its
-// contiguous slice of W_r rows into shared memory with one bulk copy issued
-// before it waits on the previous kernel (the weights never depend on it),
-// builds x (from x_bf16, or as RMS chaining of the previous layer's y), and
-// computes its experts' logits in the fixed order.  After a cluster barrier,
-// CTA 0 reads every CTA's logits through distributed shared memory and runs
-// the top-k + softmax per token.
+// Small-T router logits over the whole GPU.  CTA b owns experts
+// [b*epc, (b+1)*epc).  Before it waits on the previous kernel it pulls its
+// W_r rows into L2 (the weights never depend on that kernel); then it builds
+// x (from x_bf16, or as RMS chaining of the previous layer's y -- every CTA
+// computes the same fixed-order result, CTA 0 writes it out) and one warp
+// per (token, expert) computes the logit in the fixed order of
+// router_logits_kernel.  The top-k follows in topk_kernel.  The kernel needs
+// a few KB of shared memory, so its CTAs fit beside a running expert pass.
 // ---------------------------------------------------------------------------
-constexpr int kCl = 16;
-constexpr int kClThreads = 256;
-constexpr int kClMaxT = 4;
+constexpr int kGridThreads = 256;
+constexpr int kGridMaxXBytes = 40 * 1024;
 
-struct ClusterArgs {
+struct GridArgs {
   const uint16_t* x;    // [T, H] BF16, or NULL when y_prev is given
   const float* y_prev;  // [T, H] FP32 to RMS-normalise, or NULL
   float eps;
-  uint16_t* x_out;      // written by CTA 0 when y_prev is given (may be NULL otherwise)
+  uint16_t* x_out;      // written by CTA 0 when y_prev is given
   const uint16_t* wr;
   const float* bias;
-  int T, H, E, k, epc;  // experts per CTA
-  int32_t* idx;
-  float* weights;
+  int T, H, E, epc;     // experts per CTA
   float* logits;
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ float dsmem_ld_f32(const float* local_addr, uint32_t rank) {
-  uint32_t a = moe::tc::smem_u32(local_addr), ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-  return v;
-}
-
-template <int EPL>
-__device__ __forceinline__ void cluster_topk(const ClusterArgs& a, const float* lg, int t, int lane) {
-  unsigned long long cand[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    cand[i] = 0ull;
-    const int e = lane + 32 * i;
-    if (e < a.E) {
-      const uint32_t owner = (uint32_t)(e / a.epc);
-      const float v = dsmem_ld_f32(lg + t * a.epc + (e - (int)owner * a.epc), owner);
-      cand[i] = ((unsigned long long)ordered_key(v) << 32) | (unsigned long long)(~(uint32_t)e);
-    }
-  }
-  int my_e;
-  float my_l;
-  warp_select_topk<EPL>(cand, a.k, lane, my_e, my_l);
-  write_topk(lane, a.k, my_e, my_l, a.idx + (size_t)t * a.k, a.weights + (size_t)t * a.k);
-}
-
-__global__ void __launch_bounds__(kClThreads) router_cluster_kernel(ClusterArgs a) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  uint64_t* wbar = reinterpret_cast<uint64_t*>(sm);
-  float* part = reinterpret_cast<float*>(sm + 16);                   // [256]
-  float* lg = reinterpret_cast<float*>(sm + 16 + 256 * 8);           // [kClMaxT][epc]
-  uint16_t* xs = reinterpret_cast<uint16_t*>(lg + kClMaxT * a.epc);  // [T][H] BF16
-  uint16_t* ws = reinterpret_cast<uint16_t*>(
-      (reinterpret_cast<uintptr_t>(xs + (size_t)a.T * a.H) + 127) & ~(uintptr_t)127);  // [epc][H]
-  const uint32_t rank = cluster_ctarank();
-  const int e0 = (int)rank * a.epc;
+__global__ void __launch_bounds__(kGridThreads) router_grid_kernel(GridArgs a) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  float* part = reinterpret_cast<float*>(sm);             // [256]
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm + 1024);  // [T][H] BF16
+  const int e0 = blockIdx.x * a.epc;
   const int ne = max(0, min(a.epc, a.E - e0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  bool wok = true;
-
-  if (threadIdx.x == 0) {
-    moe::tc::mbar_init(wbar, 1);
-    moe::tc::mbar_fence_init();
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // one bulk copy per W_r row, spread over the lanes of warp 0
-    const uint32_t row_bytes = (uint32_t)a.H * 2;
-    if (lane == 0) moe::tc::mbar_arrive_expect_tx(wbar, (uint32_t)ne * row_bytes);
-    __syncwarp();
-    for (int q = lane; q < ne; q += 32)
-      moe::tc::bulk_g2s(moe::tc::smem_u32(ws + (size_t)q * a.H), a.wr + (size_t)(e0 + q) * a.H,
-                        row_bytes, wbar);
+  {
+    const char* wb = reinterpret_cast<const char*>(a.wr + (size_t)e0 * a.H);
+    const size_t bytes = (size_t)ne * a.H * 2;
+    for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)kGridThreads * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
   }
   moe::pdl_launch_dependents();
   moe::pdl_wait();
 
-  // x for every token
   for (int t = 0; t < a.T; ++t) {
     if (a.y_prev) {
       const float* yr = a.y_prev + (size_t)t * a.H;
       const float r = rms_inv_fixed_order(yr, a.H, a.eps, part);
-      for (int i = threadIdx.x; i < a.H; i += kClThreads) {
-        const uint16_t b = f32_to_bf16_bits(__fmul_rn(yr[i], r));
-        xs[(size_t)t * a.H + i] = b;
-        if (rank == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = b;
+      constexpr int kBatch = 8;
+      for (int i0 = threadIdx.x; i0 < a.H; i0 += kGridThreads * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) v[b] = i0 + kGridThreads * b < a.H ? yr[i0 + kGridThreads * b] : 0.0f;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int i = i0 + kGridThreads * b;
+          if (i < a.H) {
+            const uint16_t x16 = f32_to_bf16_bits(__fmul_rn(v[b], r));
+            xs[(size_t)t * a.H + i] = x16;
+            if (blockIdx.x == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = x16;
+          }
+        }
       }
     } else {
-      for (int i = threadIdx.x * 8; i < a.H; i += kClThreads * 8)
+      for (int i = threadIdx.x * 8; i < a.H; i += kGridThreads * 8)
         *reinterpret_cast<uint4*>(xs + (size_t)t * a.H + i) =
             __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + i));
     }
   }
   __syncthreads();
-  if (!moe::tc::mbar_wait(wbar, 0, moe::global_ns() + 2000000000ull)) wok = false;
 
-  // logits: warp -> expert, lane j -> chunks j, j+32, ... (fixed order)
+  // logits: task (token t, expert q) -> warp; lane j -> chunks j, j+32, ...
   const int nchunk = a.H >> 3;
-  for (int q = warp; q < ne; q += kClThreads / 32) {
-    float acc[kClMaxT];
+  for (int task = warp; task < a.T * ne; task += kGridThreads / 32) {
+    const int t = task / ne, q = task - t * ne;
+    const uint16_t* wrow = a.wr + (size_t)(e0 + q) * a.H;
+    const uint16_t* xrow = xs + (size_t)t * a.H;
+    float acc = 0.0f;
+    // up to kBatch of the lane's chunks in flight; accumulated in chunk order
+    constexpr int kBatch = 8;
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * kBatch) {
+      uint4 wv[kBatch];
 #pragma unroll
-    for (int t = 0; t < kClMaxT; ++t) acc[t] = 0.0f;
-    const uint16_t* wrow = ws + (size_t)q * a.H;
-    for (int c = lane; c < nchunk; c += 32) {
-      const uint4 wv = *reinterpret_cast<const uint4*>(wrow + 8 * c);
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+      for (int b = 0; b < kBatch; ++b) {
+        const int c = c0 + 32 * b;
+        wv[b] = c < nchunk ? __ldg(reinterpret_cast<const uint4*>(wrow + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-      for (int t = 0; t < kClMaxT; ++t) {
-        if (t < a.T) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * a.H + 8 * c);
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      for (int b = 0; b < kBatch; ++b) {
+        const int c = c0 + 32 * b;
+        if (c < nchunk) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 8 * c);
+          const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float xf = moe::bf16_bits_to_f32((i & 1) ? (xw[i >> 1] >> 16) : (xw[i >> 1] & 0xFFFFu));
             const float wf = moe::bf16_bits_to_f32((i & 1) ? (ww[i >> 1] >> 16) : (ww[i >> 1] & 0xFFFFu));
-            acc[t] = __fmaf_rn(xf, wf, acc[t]);
+            acc = __fmaf_rn(xf, wf, acc);
           }
         }
       }
     }
 #pragma unroll
-    for (int t = 0; t < kClMaxT; ++t) {
-      float v = acc[t];
-#pragma unroll
-      for (int d = 16; d > 0; d >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
-      if (t < a.T && lane == 0) {
-        const int e = e0 + q;
-        if (a.bias) v = __fadd_rn(v, a.bias[e]);
-        if (!wok) v = __uint_as_float(0x7FC00000u);
-        lg[t * a.epc + q] = v;
-        a.logits[(size_t)t * a.E + e] = v;
-      }
+    for (int d = 16; d > 0; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+    if (lane == 0) {
+      const int e = e0 + q;
+      a.logits[(size_t)t * a.E + e] = a.bias ? __fadd_rn(acc, a.bias[e]) : acc;
     }
   }
-  cluster_sync_all();
-
-  // top-k in CTA 0, one warp per token, candidates read over DSMEM
-  if (rank == 0 && warp < a.T) {
-    const int epl = (a.E + 31) / 32;
-    if (epl <= 1) cluster_topk<1>(a, lg, warp, lane);
-    else if (epl <= 2) cluster_topk<2>(a, lg, warp, lane);
-    else if (epl <= 4) cluster_topk<4>(a, lg, warp, lane);
-    else if (epl <= 8) cluster_topk<8>(a, lg, warp, lane);
-    else if (epl <= 16) cluster_topk<16>(a, lg, warp, lane);
-    else cluster_topk<32>(a, lg, warp, lane);
-  }
-  cluster_sync_all();  // keep every CTA's shared memory alive until CTA 0 is done
 }
 
-size_t cluster_smem(int T, int H, int epc) {
-  return 16 + 256 * 8 + (size_t)kClMaxT * epc * 4 + (size_t)T * H * 2 + 128 + (size_t)epc * H * 2;
-}
-
-int cluster_smem_limit() {
-  static int limit = -1;
-  if (limit < 0) {
+int sm_count_router() {
+  static int sms = 0;
+  if (sms == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      limit = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 0;
   }
-  return limit;
+  return sms;
 }
 
-bool cluster_fits(int T, int H, int E) {
-  const int epc = (E + kCl - 1) / kCl;
-  return T >= 1 && T <= kClMaxT && E <= 1024 && H % 8 == 0 &&
-         cluster_smem(T, H, epc) <= (size_t)cluster_smem_limit();
+bool grid_fits(int T, int H, int E) {
+  return T >= 1 && (size_t)T * H * 2 <= kGridMaxXBytes && E <= 1024 && H % 8 == 0 &&
+         sm_count_router() > 0;
 }
 
-int launch_cluster_router(const ClusterArgs& a0, cudaStream_t st) {
-  ClusterArgs a = a0;
-  a.epc = (a.E + kCl - 1) / kCl;
-  const size_t smem = cluster_smem(a.T, a.H, a.epc);
+int launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* weights, cudaStream_t st) {
+  const int threads = 256;
+  const dim3 grid((unsigned)(((long long)T * 32 + threads - 1) / threads));
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) return moe::launch_pdl(topk_kernel<1>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+  if (epl <= 2) return moe::launch_pdl(topk_kernel<2>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+  if (epl <= 4) return moe::launch_pdl(topk_kernel<4>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+  if (epl <= 8) return moe::launch_pdl(topk_kernel<8>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+  if (epl <= 16) return moe::launch_pdl(topk_kernel<16>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+  return moe::launch_pdl(topk_kernel<32>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+}
+
+// Logits on the whole GPU, then the top-k.
+int launch_grid_router(const GridArgs& a0, int k, int32_t* idx, float* weights, cudaStream_t st) {
+  GridArgs a = a0;
+  const int sms = sm_count_router();
+  a.epc = (a.E + sms - 1) / sms;
+  const int grid = (a.E + a.epc - 1) / a.epc;
+  const size_t smem = 1024 + (size_t)a.T * a.H * 2;
   static size_t granted = 0;
-  static bool nonportable = false;
-  if (!nonportable) {
-    if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+  if (smem > 48 * 1024 && smem > granted) {
+    if (cudaFuncSetAttribute(router_grid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
-      return MOE_ERR_CUDA;
-    nonportable = true;
-  }
-  if (smem > granted) {
-    if (cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
     granted = smem;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCl);
-  cfg.blockDim = dim3(kClThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, router_cluster_kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const int rc = moe::launch_pdl(router_grid_kernel, dim3(grid), dim3(kGridThreads), smem, st, a);
+  if (rc != MOE_OK) return rc;
+  return launch_topk(a.logits, a.T, a.E, k, idx, weights, st);
 }
 
 }  // namespace
@@ -450,19 +387,16 @@ extern "C" int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, 
   if (!moe::aligned16(x_bf16) || !moe::aligned16(wr_bf16)) return MOE_ERR_ALIGNMENT;
   if (T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cluster_fits(T, H, E)) {
-    ClusterArgs a = {};
+  if (grid_fits(T, H, E)) {
+    GridArgs a = {};
     a.x = x_bf16;
     a.wr = wr_bf16;
     a.bias = bias;
     a.T = T;
     a.H = H;
     a.E = E;
-    a.k = k;
-    a.idx = idx;
-    a.weights = weights;
     a.logits = logits;
-    return launch_cluster_router(a, st);
+    return launch_grid_router(a, k, idx, weights, st);
   }
   const int threads = 256;
   int rc;
@@ -476,15 +410,7 @@ extern "C" int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, 
                          dim3(threads), 0, st, x_bf16, wr_bf16, bias, T, H, E, logits);
   }
   if (rc != MOE_OK) return rc;
-  const dim3 grid((unsigned)(((long long)T * 32 + threads - 1) / threads));
-  const int epl = (E + 31) / 32;
-  if (epl <= 1) rc = moe::launch_pdl(topk_kernel<1>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  else if (epl <= 2) rc = moe::launch_pdl(topk_kernel<2>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  else if (epl <= 4) rc = moe::launch_pdl(topk_kernel<4>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  else if (epl <= 8) rc = moe::launch_pdl(topk_kernel<8>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  else if (epl <= 16) rc = moe::launch_pdl(topk_kernel<16>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  else rc = moe::launch_pdl(topk_kernel<32>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  return rc;
+  return launch_topk(logits, T, E, k, idx, weights, st);
 }
 
 extern "C" int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16_t* x_bf16,
@@ -506,8 +432,8 @@ extern "C" int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double
   if (!moe::aligned16(wr_bf16) || !moe::aligned16(x_out)) return MOE_ERR_ALIGNMENT;
   if (T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cluster_fits(T, H, E)) {
-    ClusterArgs a = {};
+  if (grid_fits(T, H, E)) {
+    GridArgs a = {};
     a.y_prev = y_prev;
     a.eps = (float)eps;
     a.x_out = x_out;
@@ -516,11 +442,8 @@ extern "C" int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double
     a.T = T;
     a.H = H;
     a.E = E;
-    a.k = k;
-    a.idx = idx;
-    a.weights = weights;
     a.logits = logits;
-    return launch_cluster_router(a, st);
+    return launch_grid_router(a, k, idx, weights, st);
   }
   int rc = moe_rmsnorm_bf16(y_prev, T, H, eps, x_out, stream);
   if (rc != MOE_OK) return rc;

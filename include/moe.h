@@ -132,8 +132,10 @@ int moe_rmsnorm_bf16(const float* y, int T, int H, double eps, uint16_t* x_bf16,
 
 /* Layer chaining fused with the router, for stacked decode: x = RMS chaining
  * of y_prev exactly as moe_rmsnorm_bf16 computes it (written to x_out), then
- * moe_router_topk on that x.  Same outputs, same limits; for T <= 4 with a
- * router slice that fits in shared memory it is a single cluster launch. */
+ * moe_router_topk on that x.  Same outputs, same limits; when x takes at
+ * most 40 KB (T*H*2 bytes) it is two launches: the logits on every SM (W_r
+ * rows pulled into L2 before the wait on the previous kernel), then the
+ * top-k. */
 int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps, uint16_t* x_out,
                             const uint16_t* wr_bf16, const float* bias, int E, int k,
                             int32_t* idx, float* weights, float* logits, void* stream);

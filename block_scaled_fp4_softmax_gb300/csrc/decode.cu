@@ -785,15 +785,14 @@ int launch_stream(const st::Args& sa, cudaStream_t stream) {
 
 }  // namespace
 
-// Workspace: a header of counters (the one-shot kernel's 64-bit grid-barrier
-// counter at 0, the ring kernel's two barrier words at 128, the one-shot
-// kernel's combine counters at 256), then h [T*k][I] FP32, then the weighted
-// expert outputs [T*k][H] FP32 of the one-shot kernel.  The header sits at a
-// fixed place so that calls of any shape can share one workspace.
+// Workspace: a header (the one-shot kernel's 64-bit grid-barrier counter at
+// 0, the ring kernel's two barrier words at 128, the rest reserved), then h
+// [T*k][I] FP32.  The header sits at a fixed place so that calls of any shape
+// can share one workspace.
 constexpr size_t kRingBarrierOffset = 128;
 extern "C" size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s) {
   if (T <= 0 || k <= 0 || !moe::shape_ok(s)) return 0;
-  return moe::os::kHeaderBytes + (size_t)T * k * (s.inter + s.hidden) * sizeof(float);
+  return moe::os::kHeaderBytes + (size_t)T * k * s.inter * sizeof(float);
 }
 
 extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
@@ -823,9 +822,7 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
     oa.H = s.hidden;
     oa.I = s.inter;
     oa.bar = reinterpret_cast<unsigned long long*>(ws);
-    oa.cnt = reinterpret_cast<unsigned*>(ws + moe::os::kBarrierBytes);
     oa.hws = hws;
-    oa.part = hws + (size_t)T * k * s.inter;
     oa.y = y;
     oa.status = dev_status;
     return launch_decode_oneshot(oa, s.format, sm_count(), stream);

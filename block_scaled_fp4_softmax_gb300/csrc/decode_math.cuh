@@ -108,6 +108,27 @@ __device__ __forceinline__ float unit_dot_h2(uint4 q, uint32_t sbits, const uint
   return apply_scale<FMT>((acc[0] + acc[1]) + (l0.x + l0.y), (acc[2] + acc[3]) + (l1.x + l1.y), sbits);
 }
 
+// One unit against an FP32 operand stored as 4 quads of 8 floats, quad qq at
+// hq + qq * qstride floats; the e2m1 values are exact in FP32 and the
+// products are formed with packed FP32 FMAs.
+template <int FMT>
+__device__ __forceinline__ float unit_dot_f32(uint4 q, uint32_t sbits, const float* hq, int qstride) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const float4 h0 = *reinterpret_cast<const float4*>(hq + wi * qstride);
+    const float4 h1 = *reinterpret_cast<const float4*>(hq + wi * qstride + 4);
+    const float2 hv[4] = {make_float2(h0.x, h0.y), make_float2(h0.z, h0.w), make_float2(h1.x, h1.y),
+                          make_float2(h1.z, h1.w)};
+    uint32_t c[4];
+    cvt_e2m1x8(w[wi], c);
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) acc[wi >> 1] = ffma2(__half22float2(as_h2(c[bi])), hv[bi], acc[wi >> 1]);
+  }
+  return apply_scale<FMT>(acc[0].x + acc[0].y, acc[1].x + acc[1].y, sbits);
+}
+
 // Power-of-two exponent e with m * 2^e in [2^14, 2^15) for finite m > 0,
 // clamped to [-120, 120]; 0 for zero, infinity or NaN.  Scaling FP16
 // operands by 2^e and the FP32 sums by 2^-e is exact, so it changes no

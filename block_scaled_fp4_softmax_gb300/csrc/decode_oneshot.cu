@@ -38,23 +38,21 @@ struct Tab {
   float wts[kMaxPairs];
   float tsc[kMaxPairs];      // per token: 2^-e of the FP16 scale of x
   unsigned amax[kMaxPairs];  // max |.| as float bits (x per token, then h per segment)
-  float pw[kMaxSegs];        // per down segment: router weight * 2^-e of the FP16 scale of h
   int flags[4];              // [0] abort, [1] grid barrier passed
-  int npieces, nseg1, nseg2, nlast, ncopies;
+  int npieces, nseg1, nseg2, ncopies;
   int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];
   uint32_t poff[kMaxPieces];  // piece: gate rows at codes1 + poff, up rows right after
   int sp[kMaxSegs], si0[kMaxSegs], sq0[kMaxSegs], sn[kMaxSegs];
   uint32_t gwo[kMaxSegs], uwo[kMaxSegs];  // first gate / up scale byte of the segment in scales1
-  int dp[kMaxSegs], dn0[kMaxSegs], dz0[kMaxSegs], dn[kMaxSegs];
-  uint32_t dso[kMaxSegs];                 // first down scale byte of the segment in scales2
+  int dt[kMaxSegs], dn0[kMaxSegs], dz0[kMaxSegs], dn[kMaxSegs];  // down: token, rows
+  uint32_t dso[kMaxSegs][kMaxK];          // first down scale byte of (segment, expert) in scales2
   // bulk copies: shared-memory destination (bytes from the dynamic base),
   // source offset in the record, bytes, barrier, pair
   uint64_t csrc[kMaxCopies];
   uint32_t cdst[kMaxCopies], cbytes[kMaxCopies];
   uint8_t cbar[kMaxCopies], cpair[kMaxCopies];
-  int last[2 * kMaxSegs * 4];             // (token, block) pairs this CTA combines
 };
-static_assert(sizeof(Tab) <= 4096, "table region");
+static_assert(sizeof(Tab) <= 8192, "table region");
 
 struct Win {  // 16-byte aligned window [lo, lo + bytes) around a byte range
   size_t lo;
@@ -130,27 +128,32 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
   ns = 0;
   soff = 0;
   for (long long d = d0; d < d1 && ns < kMaxSegs;) {
-    const int p = (int)(d / g.H), n0 = (int)(d - (long long)p * g.H);
+    const int t = (int)(d / g.H), n0 = (int)(d - (long long)t * g.H);
     const int n = (int)min(d1 - d, (long long)(g.H - n0));
     const int z0 = (int)(d - d0);
-    tb.dp[ns] = p;
+    tb.dt[ns] = t;
     tb.dn0[ns] = n0;
     tb.dz0[ns] = z0;
     tb.dn[ns] = n;
-    for (int a = 0; a < n; a += rows_per_copy) {
-      const int m = min(rows_per_copy, n - a);
-      copy(g.off_codes2 + (size_t)(z0 + a) * drb, o.down + (size_t)(n0 + a) * drb, (uint32_t)(m * drb), kBarDown, p);
+    // rows [n0, n0 + n) of every expert of token t: codes at
+    // codes2 + (z0 * k + j * n) rows, then one scale window per expert
+    for (int j = 0; j < g.k; ++j) {
+      const int p = t * g.k + j;
+      for (int a = 0; a < n; a += rows_per_copy) {
+        const int m = min(rows_per_copy, n - a);
+        copy(g.off_codes2 + ((size_t)z0 * g.k + (size_t)j * n + a) * drb, o.down + (size_t)(n0 + a) * drb,
+             (uint32_t)(m * drb), kBarDown, p);
+      }
+      const Win dw = window(o.down_s + (size_t)n0 * dsb, (size_t)n * dsb);
+      tb.dso[ns][j] = soff + dw.delta;
+      copy(g.off_scales2 + soff, dw.lo, dw.bytes, kBarDown, p);
+      soff += dw.bytes;
     }
-    const Win dw = window(o.down_s + (size_t)n0 * dsb, (size_t)n * dsb);
-    tb.dso[ns] = soff + dw.delta;
-    copy(g.off_scales2 + soff, dw.lo, dw.bytes, kBarDown, p);
-    soff += dw.bytes;
     ++ns;
     d += n;
   }
   tb.nseg2 = ns;
   tb.ncopies = nc;
-  tb.nlast = 0;
   tb.flags[0] = 0;
   tb.flags[1] = 0;
 }
@@ -349,163 +352,98 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   }
   tc::named_sync(1, kCThreads);
 
-  // h of the down segments' pairs: per-pair max |h| (pass 1), then FP16 hi +
-  // lo quads [segment][4][I/32] of h * 2^e (pass 2); loads stay in registers
-  // between the passes when one batch covers them
+  // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats
+  // per 32-element unit: element i of local pair lp at
+  // lp * hstride + (((i & 31) >> 3) * I/32 + (i >> 5)) * 8 + (i & 7)
   const long long d0 = (long long)blockIdx.x * g.D / g.grid, d1 = (long long)(blockIdx.x + 1) * g.D / g.grid;
   const int nz = (int)(d1 - d0);
-  uint4* hhi = act;
-  uint4* hlo = act + (size_t)g.segs2 * 4 * updr;
+  const int t_lo = nz > 0 ? tb.dt[0] : 0;
+  const int nlp = nz > 0 ? (tb.dt[tb.nseg2 - 1] - t_lo + 1) * a.k : 0;
+  float* hs = reinterpret_cast<float*>(act);
   const bool have_h = tb.flags[1] != 0;
-  {
-    const int n8 = tb.nseg2 * (a.I / 8);
+  if (have_h) {
+    const int n8 = nlp * (a.I / 8);
+    const float4* src = reinterpret_cast<const float4*>(a.hws + (size_t)t_lo * a.k * a.I);
     constexpr int kB = 4;
-    const bool keep = n8 <= kB * kCThreads;
-    float4 v[kB][2];
-    auto load = [&](int b0) {
+    for (int b0 = threadIdx.x; b0 < n8; b0 += kB * kCThreads) {
+      float4 v[kB][2];
 #pragma unroll
       for (int m = 0; m < kB; ++m) {
-        const int e8 = b0 + m * kCThreads + lane;
+        const int e8 = b0 + m * kCThreads;
         if (e8 < n8) {
-          const int s = e8 / (a.I / 8), i = (e8 - s * (a.I / 8)) * 8;
-          const float4* src = reinterpret_cast<const float4*>(a.hws + (size_t)tb.dp[s] * a.I + i);
-          v[m][0] = __ldcg(src);
-          v[m][1] = __ldcg(src + 1);
+          v[m][0] = __ldcg(src + 2 * e8);
+          v[m][1] = __ldcg(src + 2 * e8 + 1);
         }
       }
-    };
-    if (have_h) {
-      for (int b0 = warp * 32; b0 < n8; b0 += kB * kCThreads) {
-        load(b0);
 #pragma unroll
-        for (int m = 0; m < kB; ++m) {
-          const int e8 = b0 + m * kCThreads + lane;
-          unsigned mx = 0u;
-          int key = -1;
-          if (e8 < n8) {
-            const float f[8] = {v[m][0].x, v[m][0].y, v[m][0].z, v[m][0].w,
-                                v[m][1].x, v[m][1].y, v[m][1].z, v[m][1].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx = max(mx, __float_as_uint(f[i]) & 0x7FFFFFFFu);
-            key = e8 / (a.I / 8);
-          }
-          if (dm::group_max(key, mx)) atomicMax(&tb.amax[key], mx);
-        }
-      }
-    }
-    tc::named_sync(1, kCThreads);
-    if (threadIdx.x < tb.nseg2)
-      tb.pw[threadIdx.x] = tb.wts[tb.dp[threadIdx.x]] *
-                           dm::pow2f(-dm::f16_shift(__uint_as_float(tb.amax[threadIdx.x])));
-    if (have_h) {
-      for (int b0 = warp * 32; b0 < n8; b0 += kB * kCThreads) {
-        if (!keep) load(b0);
-#pragma unroll
-        for (int m = 0; m < kB; ++m) {
-          const int e8 = b0 + m * kCThreads + lane;
-          if (e8 < n8) {
-            const int s = e8 / (a.I / 8), i = (e8 - s * (a.I / 8)) * 8;
-            const float sc = dm::pow2f(dm::f16_shift(__uint_as_float(tb.amax[s])));
-            const float f[8] = {v[m][0].x * sc, v[m][0].y * sc, v[m][0].z * sc, v[m][0].w * sc,
-                                v[m][1].x * sc, v[m][1].y * sc, v[m][1].z * sc, v[m][1].w * sc};
-            uint32_t hv[4], lv[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const __half h0 = __float2half_rn(f[2 * e2]), h1 = __float2half_rn(f[2 * e2 + 1]);
-              hv[e2] = dm::pack_h2(__half2float(h0), __half2float(h1));
-              lv[e2] = dm::pack_h2(f[2 * e2] - __half2float(h0), f[2 * e2 + 1] - __half2float(h1));
-            }
-            const size_t at = (size_t)s * 4 * updr + ((i & 31) >> 3) * updr + (i >> 5);
-            hhi[at] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            hlo[at] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-          }
+      for (int m = 0; m < kB; ++m) {
+        const int e8 = b0 + m * kCThreads;
+        if (e8 < n8) {
+          const int lp = e8 / (a.I / 8), i = (e8 - lp * (a.I / 8)) * 8;
+          float* dst = hs + (size_t)lp * g.hstride + (((i & 31) >> 3) * updr + (i >> 5)) * 8;
+          *reinterpret_cast<float4*>(dst) = v[m][0];
+          *reinterpret_cast<float4*>(dst + 4) = v[m][1];
         }
       }
     }
   }
   tc::named_sync(1, kCThreads);
 
-  // down: each down row to a group of L lanes (L a power of two), lane sub of
-  // the group taking units sub, sub + L, ...; the group's sum is reduced over
-  // its lanes in a fixed order and the row's weighted output goes to global
-  // scratch.  32 / L rows per warp pass, passes round-robin over the warps.
+  // down: task (row z, expert j) -> a group of L lanes (L a power of two),
+  // lane sub of the group taking units sub, sub + L, ...; the group's sum is
+  // reduced over its lanes in a fixed order and, times the router weight,
+  // kept per (row, expert).  32 / L tasks per warp pass, passes round-robin.
   constexpr int kUnitsPerLane = 5;
   int L = 1;
   while (L < 32 && L * kUnitsPerLane < updr) L <<= 1;
-  const int rows_per_pass = 32 / L;
-  const int npass = (nz + rows_per_pass - 1) / rows_per_pass;
+  const int tasks_per_pass = 32 / L;
+  const int ntask = nz * a.k;
+  const int npass = (ntask + tasks_per_pass - 1) / tasks_per_pass;
   const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], tb, a.status);
   const int sub = lane & (L - 1);
-  int ds = 0;  // a lane's segment only grows, as its rows do
+  float* part = reinterpret_cast<float*>(smem + g.off_part);  // [row][expert]
   for (int ps = warp; ps < npass; ps += kCWarps) {
-    const int z = ps * rows_per_pass + lane / L;
+    const int task = ps * tasks_per_pass + lane / L;
     float v = 0.f;
-    if (z < nz) {
-      while (ds + 1 < tb.nseg2 && tb.dz0[ds + 1] <= z) ++ds;
-      if (!down_in || !tb.recs[tb.dp[ds]]) {
+    int z = 0, j = 0, s = 0, p = 0;
+    if (task < ntask) {
+      z = task / a.k;
+      j = task - z * a.k;
+      while (s + 1 < tb.nseg2 && tb.dz0[s + 1] <= z) ++s;
+      p = tb.dt[s] * a.k + j;
+      if (!down_in || !tb.recs[p]) {
         v = __uint_as_float(0x7FC00000u);
       } else {
-        const uint8_t* crow = codes2 + (size_t)z * (a.I / 2);
-        const uint8_t* srow = scales2 + tb.dso[ds] + (size_t)(z - tb.dz0[ds]) * (a.I / G);
-        const uint4* hs = hhi + (size_t)ds * 4 * updr;
-        const uint4* ls = hlo + (size_t)ds * 4 * updr;
+        const int zr = z - tb.dz0[s];
+        const uint8_t* crow = codes2 + ((size_t)tb.dz0[s] * a.k + (size_t)j * tb.dn[s] + zr) * (a.I / 2);
+        const uint8_t* srow = scales2 + tb.dso[s][j] + (size_t)zr * (a.I / G);
+        const float* hq = hs + (size_t)((tb.dt[s] - t_lo) * a.k + j) * g.hstride;
         if constexpr (UPDR > 0) {
           constexpr int kL = [] { int l = 1; while (l < 32 && l * kUnitsPerLane < UPDR) l <<= 1; return l; }();
 #pragma unroll
           for (int m = 0; m < (UPDR + kL - 1) / kL; ++m) {
             const int u = sub + kL * m;
             if (u < UPDR)
-              v += dm::unit_dot_h2<FMT, UPDR>(*reinterpret_cast<const uint4*>(crow + 16 * u),
-                                              dm::scale_bits<FMT>(srow + sstep * u), hs + u, ls + u, UPDR);
+              v += dm::unit_dot_f32<FMT>(*reinterpret_cast<const uint4*>(crow + 16 * u),
+                                         dm::scale_bits<FMT>(srow + sstep * u), hq + 8 * u, 8 * UPDR);
           }
         } else {
           for (int u = sub; u < updr; u += L)
-            v += dm::unit_dot_h2<FMT, 0>(*reinterpret_cast<const uint4*>(crow + 16 * u),
-                                         dm::scale_bits<FMT>(srow + sstep * u), hs + u, ls + u, updr);
+            v += dm::unit_dot_f32<FMT>(*reinterpret_cast<const uint4*>(crow + 16 * u),
+                                       dm::scale_bits<FMT>(srow + sstep * u), hq + 8 * u, 8 * updr);
         }
       }
     }
     for (int d = L >> 1; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-    if (z < nz && sub == 0)
-      a.part[(size_t)tb.dp[ds] * a.H + tb.dn0[ds] + (z - tb.dz0[ds])] =
-          *abort_flag ? __uint_as_float(0x7FC00000u) : tb.pw[ds] * v;
-  }
-  __threadfence();
-  tc::named_sync(1, kCThreads);
-  // combine: count this CTA's rows into each block of output rows it touches
-  // (one thread per (segment, block), all atomics in flight together); the
-  // CTA that completes a block adds the block's k expert outputs in expert
-  // order
-  {
-    int j = 0;
-    for (int s = 0; s < tb.nseg2; ++s) {
-      const int t = tb.dp[s] / a.k, n0 = tb.dn0[s], n1r = n0 + tb.dn[s];
-      for (int b = n0 / g.blk; b * g.blk < n1r; ++b, ++j) {
-        if (j != threadIdx.x) continue;
-        const int lo = max(n0, b * g.blk), hi = min(n1r, (b + 1) * g.blk);
-        const unsigned rows = (unsigned)(min(a.H, (b + 1) * g.blk) - b * g.blk);
-        const unsigned target = (unsigned)a.k * rows;
-        unsigned* c = a.cnt + (size_t)t * kBlkStride + b;
-        const unsigned now = atomicAdd(c, (unsigned)(hi - lo)) + (unsigned)(hi - lo);
-        if (now == target) {
-          atomicExch(c, 0u);
-          tb.last[atomicAdd(&tb.nlast, 1)] = t * kBlkStride + b;
-        } else if (now > target) {
-          status_or(a.status, MOE_DEV_WORKSPACE);
-        }
-        __threadfence();
-      }
-    }
+    if (task < ntask && sub == 0) part[task] = tb.wts[p] * v;
   }
   tc::named_sync(1, kCThreads);
-  for (int l = 0; l < tb.nlast; ++l) {
-    const int t = tb.last[l] / kBlkStride, b = tb.last[l] % kBlkStride;
-    const int n_hi = min(a.H, (b + 1) * g.blk);
-    for (int n = b * g.blk + threadIdx.x; n < n_hi; n += kCThreads) {
-      float v = 0.f;
-      for (int j = 0; j < a.k; ++j) v += __ldcg(a.part + (size_t)(t * a.k + j) * a.H + n);
-      a.y[(size_t)t * a.H + n] = v;
-    }
+  // each output row: its k weighted expert outputs in expert order
+  const bool failed = *abort_flag != 0;
+  for (int z = threadIdx.x; z < nz; z += kCThreads) {
+    float v = 0.f;
+    for (int jj = 0; jj < a.k; ++jj) v += part[(size_t)z * a.k + jj];
+    a.y[d0 + z] = failed ? __uint_as_float(0x7FC00000u) : v;
   }
   __syncthreads();
 }
@@ -545,9 +483,7 @@ bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t s
   const Geo g = make_geo(T, k, H, I, fmt == MOE_FMT_NVFP4 ? 16 : 32, grid);
   if (g.total + 1024 > smem_limit) return false;
   if (g.segs1 > kMaxSegs || g.segs2 > kMaxSegs || max_pieces(g) > kMaxPieces) return false;
-  if (g.nblk > kBlkStride) return false;
-  // blocks one CTA can complete: those its down rows touch
-  if (g.rows2 / g.blk + 2 * g.segs2 > (int)(sizeof(((Tab*)nullptr)->last) / sizeof(int))) return false;
+  if (g.copies > kMaxCopies || k > kMaxK) return false;
   return true;
 }
 

@@ -6,11 +6,12 @@
 //  - gate/up: the P*I row pairs (pair p = t*k + j, row i) in order, an equal
 //    share per CTA; a share is cut into segments (one pair each) and the
 //    segments into pieces of np rows;
-//  - down: the P*H rows (pair p, output row n) in order, an equal share per
-//    CTA, cut into segments (one pair each).
-// Every byte of a CTA's share is requested with a handful of large TMA bulk
-// copies at kernel entry (the copy engine of an SM completes only a few
-// copies per microsecond, so few and large is what keeps HBM busy).
+//  - down: the T*H output rows (token t, row n) in order, an equal share per
+//    CTA, with all k experts of each row, so every output row is finished by
+//    one CTA; a share is cut into segments (one token each).
+// Every byte of a CTA's share is requested with large TMA bulk copies at
+// kernel entry (the copy engine of an SM completes only a few copies per
+// microsecond, so few and large is what keeps HBM busy).
 #pragma once
 
 #include <stddef.h>
@@ -25,26 +26,26 @@ constexpr int kCThreads = kCWarps * 32;
 constexpr int kMaxPairs = 64;
 constexpr int kMaxPieces = 16;    // gate/up pieces of one CTA
 constexpr int kMaxSegs = 4;       // segments of one CTA, per phase
-constexpr int kMaxCopies = 48;    // bulk copies of one CTA
+constexpr int kMaxCopies = 96;    // bulk copies of one CTA
+constexpr int kMaxK = 32;         // experts per token
 constexpr int kPieceBytes = 16384;  // target bytes of one matrix in one piece
 constexpr uint32_t kMaxCopy = 32768;
-constexpr int kBlkStride = 64;    // combine counters per token
-constexpr size_t kBarrierBytes = 256;                        // grid-barrier counter
-constexpr size_t kCounterBytes = (size_t)64 * kBlkStride * 4;  // combine counters
+constexpr size_t kBarrierBytes = 256;  // grid-barrier counter
+constexpr size_t kCounterBytes = 16384;  // reserved (kept so the workspace layout stays fixed)
 constexpr size_t kHeaderBytes = kBarrierBytes + kCounterBytes;
 
 __host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Geo {
   int T, k, H, I, G, grid;
-  long long R1, D;    // gate/up row pairs, down rows
+  long long R1, D;    // gate/up row pairs, output rows
   int rows1, rows2;   // most rows of one CTA, per phase
   int segs1, segs2;   // most segments of one CTA, per phase
   int np;             // rows per gate/up piece
   int copies;         // most bulk copies of one CTA
-  int blk, nblk;      // combine block rows, blocks per token
+  int hstride;        // floats per pair in the staged h (4 quads x I/32 units x 8, padded)
   // shared-memory regions (bytes from the start of dynamic shared memory)
-  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, total;
+  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, off_part, total;
 };
 
 __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid) {
@@ -52,37 +53,36 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   g.T = T; g.k = k; g.H = H; g.I = I; g.G = G; g.grid = grid;
   const long long P = (long long)T * k;
   g.R1 = P * I;
-  g.D = P * H;
+  g.D = (long long)T * H;
   g.rows1 = (int)((g.R1 + grid - 1) / grid);
   g.rows2 = (int)((g.D + grid - 1) / grid);
   const long long s1 = (g.rows1 - 1) / I + 2, s2 = (g.rows2 - 1) / H + 2;
   g.segs1 = (int)(s1 < P ? s1 : P);
-  g.segs2 = (int)(s2 < P ? s2 : P);
+  g.segs2 = (int)(s2 < T ? s2 : T);
   g.np = kPieceBytes / (H / 2);
   if (g.np < 1) g.np = 1;
   const int rows_per_copy = (int)(kMaxCopy / (I / 2));
   g.copies = 2 * ((g.rows1 + g.np - 1) / g.np + g.segs1) + 2 * g.segs1 +
-             (g.rows2 + rows_per_copy - 1) / rows_per_copy + 2 * g.segs2;
-  int blk = (H + 63) / 64;
-  blk = blk < 128 ? 128 : blk;
-  g.blk = (blk + 31) / 32 * 32;
-  g.nblk = (H + g.blk - 1) / g.blk;
+             k * ((g.rows2 + rows_per_copy - 1) / rows_per_copy + 2 * g.segs2);
+  g.hstride = 4 * (I / 32) * 8 + 4;
   size_t o = 0;
   g.off_bar = o;                                  // mbarriers: pieces, scales, down
   o += (kMaxPieces + 2) * 8;
   g.off_tab = o = round_up(o, 16);                // tables, weights, scales, flags
-  o += 4096;
+  o += 8192;
   g.off_codes1 = o = round_up(o, 128);
   o += (size_t)g.rows1 * H;                       // gate + up codes
   g.off_scales1 = o = round_up(o, 128);
   o += 2 * ((size_t)g.rows1 * (H / G) + 32 * (size_t)g.segs1);
   g.off_codes2 = o = round_up(o, 128);
-  o += (size_t)g.rows2 * (I / 2);
+  o += (size_t)g.rows2 * k * (I / 2);              // down codes, [segment][expert][row]
   g.off_scales2 = o = round_up(o, 128);
-  o += (size_t)g.rows2 * (I / G) + 32 * (size_t)g.segs2;
+  o += (size_t)g.rows2 * k * (I / G) + 32 * (size_t)g.segs2 * k;
   g.off_act = o = round_up(o, 128);
-  const size_t a1 = (size_t)T * H * 2, a2 = (size_t)g.segs2 * I * 4;
-  o += a1 > a2 ? a1 : a2;
+  const size_t a1 = (size_t)T * H * 2, a2 = (size_t)g.segs2 * k * g.hstride * 4;
+  o += a1 > a2 ? a1 : a2;                         // x (FP16), then h (FP32)
+  g.off_part = o = round_up(o, 128);
+  o += (size_t)g.rows2 * k * 4;                   // weighted expert outputs per row
   g.total = round_up(o, 128);
   return g;
 }
@@ -105,9 +105,7 @@ struct DecodeOneshotArgs {
   const void* const* ptrs;
   int E, H, I;
   unsigned long long* bar;  // grid-barrier counter (workspace start)
-  unsigned* cnt;            // combine counters [64][kBlkStride]
   float* hws;               // [P][I] SwiGLU intermediate
-  float* part;              // [P][H] weighted expert outputs
   float* y;
   int32_t* status;
 };

@@ -25,7 +25,6 @@ DEV_MISALIGNED = 2
 DEV_BAD_INDEX = 4
 DEV_TIMEOUT = 8
 DEV_FP16_RANGE = 16
-DEV_WORKSPACE = 32
 
 EXPORTS = (
     "moe_expert_record_bytes",

@@ -61,9 +61,7 @@ enum {
   MOE_DEV_MISALIGNED = 2,  /* a selected expert's record was not 16-byte aligned */
   MOE_DEV_BAD_INDEX = 4,   /* an expert index was outside [0, E) */
   MOE_DEV_TIMEOUT = 8,     /* a bounded wait inside a kernel gave up */
-  MOE_DEV_FP16_RANGE = 16, /* prompt path, NVFP4: an activation's magnitude is >= 65520 */
-  MOE_DEV_WORKSPACE = 32   /* decode: the workspace's counters were not as a completed call
-                              leaves them (not zero-filled, or reused after a timeout) */
+  MOE_DEV_FP16_RANGE = 16  /* prompt path, NVFP4: an activation's magnitude is >= 65520 */
 };
 
 /* Expert shape: hidden size H, intermediate size I, record format.
@@ -141,13 +139,12 @@ int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps, uint1
                             int32_t* idx, float* weights, float* logits, void* stream);
 
 /* Workspace bytes moe_experts_decode needs for T tokens, k experts each:
- * 16,640 bytes of grid-barrier and combine counters, then the FP32 SwiGLU
- * intermediate [T*k][I] and the FP32 weighted expert outputs [T*k][H].
- * Zero-fill it before its first use.  Every call that completes leaves the
- * counters in a state the next call accepts, so one zeroed workspace serves
- * any number of calls, of any shape, on one stream; calls that overlap in
- * time need separate workspaces.  After a call that reported
- * MOE_DEV_TIMEOUT or MOE_DEV_WORKSPACE, zero it again. */
+ * 16,640 bytes of grid-barrier counters, then the FP32 SwiGLU intermediate
+ * [T*k][I].  Zero-fill it before its first use.  Every call that completes
+ * leaves the counters in a state the next call accepts, so one zeroed
+ * workspace serves any number of calls, of any shape, on one stream; calls
+ * that overlap in time need separate workspaces.  After a call that reported
+ * MOE_DEV_TIMEOUT, zero it again. */
 size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s);
 
 /* Decode path: the experts of T tokens (T*k small, GEMV shaped), HBM bound

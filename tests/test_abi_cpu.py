@@ -79,5 +79,5 @@ def test_argument_validation_before_any_cuda_call(lib):
                                   1 << 20, None, None) == 3
     assert lib.fp8_rowscale_gemv(one, one, one, 4, 24, one, None) == 3
     assert lib.fp4_pack_expert(one, one, vp(20), s, one, None) == 2
-    # counters header, then h [T*k][I] and the weighted expert outputs [T*k][H]
-    assert moe.moe_experts_decode_workspace(1, 10, s) == 16640 + 10 * (640 + 2560) * 4
+    # counters header, then h [T*k][I]
+    assert moe.moe_experts_decode_workspace(1, 10, s) == 16640 + 10 * 640 * 4

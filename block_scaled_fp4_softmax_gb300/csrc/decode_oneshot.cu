@@ -5,22 +5,21 @@
 // SwiGLU expert kernel; the sum over the k experts weighted by the
 // renormalised router probabilities).
 //
-//  1. Prologue.  Warp 15 reads the routed records and issues every TMA bulk
-//     copy of this CTA's share at once; warps 0-14 stage x as FP16 (scaled per
-//     token by a power of two, which is exact).
+//  1. Prologue.  Before the wait for the previous kernel every CTA plans its
+//     bulk copies; then warp 15 reads the routed records and its lanes issue
+//     every copy of the CTA's share at once (the copy engine of an SM
+//     completes only a few copies per microsecond, so the copies are few and
+//     large); warps 0-14 stage x as FP16, scaled per token by a power of two
+//     (exact).
 //  2. gate/up + SwiGLU: row pair q of the CTA -> warp q % 15, as soon as its
 //     piece has landed; h = silu(g) * u goes to global scratch.
 //  3. Grid barrier (one arrival on a counter that only grows).
-//  4. down: h of the CTA's down pairs staged as FP16 hi + lo (scaled per pair
-//     by a power of two); the units (16 code bytes) of the CTA's down rows
-//     are cut into 32-unit slices, slice s -> warp s % 15, one unit per lane,
-//     and a segmented scan leaves one partial per (row, slice); each row's
-//     partials are added in order and the row's weighted output goes to
-//     global scratch.
-//  5. Combine: per block of output rows, the CTA whose contribution completes
-//     the block (counted with one atomic per block) adds the k weighted
-//     expert outputs in expert order and writes y.  Every sum has a fixed
-//     order, so y is bit-reproducible.
+//  4. down: the CTA owns whole output rows.  h of its tokens' pairs is staged
+//     as FP32; task (row, expert) -> a group of lanes, each lane a few units
+//     (16 code bytes = 32 elements) with packed FP32 FMAs, the group reduced
+//     by shuffles; each row adds its k weighted expert outputs in expert
+//     order and writes y.  Every sum has a fixed order, so y is
+//     bit-reproducible.
 #include <algorithm>
 
 #include "common.cuh"

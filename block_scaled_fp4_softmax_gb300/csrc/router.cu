@@ -125,11 +125,11 @@ __device__ __forceinline__ void warp_select_topk(const unsigned long long (&cand
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
       if (cand[i] < prev && cand[i] > best) best = cand[i];
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
-      best = o > best ? o : best;
-    }
+    // warp maximum of the 64-bit keys: the high words first, then the low
+    // words among the lanes that hold the highest high word
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+    best = ((unsigned long long)hi << 32) | lo;
     prev = best;
     if (lane == r) {
       my_e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));

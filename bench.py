@@ -139,26 +139,28 @@ class DecodeStack:
                               device=device)
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         self.setup_s = time.time() - t0
-        self.kernels_per_step = LAYERS * 3
+        self.kernels_per_step = LAYERS
         self.ev = None
 
     def expert_bytes_per_step(self):
         return LAYERS * K_TOP * self.rec_bytes
 
     def run_layers(self, timing_events=None):
-        """One token through the 48 layers: layer 0 routes x0; every later
-        layer RMS-chains the previous output inside its router launch."""
+        """One token through the 48 layers, one launch per layer: layer 0
+        routes x0; every later layer RMS-chains the previous output inside
+        its launch (y is overwritten in place)."""
         moe = self.moe
         for L in range(LAYERS):
-            if L == 0:
-                moe.moe_router_topk(self.x, self.wr[L], None, K_TOP, self.idx, self.w, self.logits)
-            else:
-                moe.moe_rmsnorm_router_topk(self.y, self.wr[L], None, K_TOP, 1e-6, self.x, self.idx,
-                                            self.w, self.logits)
             if timing_events is not None:
                 timing_events[L][0].record()
-            moe.moe_experts_decode(self.x, self.idx, self.w, self.ptrs[L], self.s, self.y, self.ws,
-                                   self.st)
+            if L == 0:
+                moe.moe_decode_layer(self.wr[L], None, K_TOP, self.ptrs[L], self.s, x=self.x, idx=self.idx,
+                                     weights=self.w, logits=self.logits, y=self.y, workspace=self.ws,
+                                     dev_status=self.st)
+            else:
+                moe.moe_decode_layer(self.wr[L], None, K_TOP, self.ptrs[L], self.s, y_prev=self.y, eps=1e-6,
+                                     x_out=self.x, idx=self.idx, weights=self.w, logits=self.logits, y=self.y,
+                                     workspace=self.ws, dev_status=self.st)
             if timing_events is not None:
                 timing_events[L][1].record()
 
@@ -412,7 +414,7 @@ def run_ours(args):
         wall = (time.perf_counter() - t0) / e_steps
         e2e = {"value": round(wl.expert_bytes_per_step() / wall / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4,
-               "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 96 per token"}
+               "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 48 per token (moe_decode_layer)"}
 
     prompt = None
     if not args.no_prompt:
@@ -434,7 +436,10 @@ def run_ours(args):
 
     peak, peak_kind = _peaks()
     value = wl.expert_bytes_per_step() * world / (ms / 1e3) / 1e9
-    per_launch_bytes = K_TOP * wl.rec_bytes + H * 2 + H * 4 + K_TOP * I * 4 * 2
+    # one launch reads its 10 expert records and the router rows (W_r, E x H
+    # BF16), reads y_prev and writes x and y, writes and reads h and the logits
+    per_launch_bytes = (K_TOP * wl.rec_bytes + E * H * 2 + H * 4 + H * 2 + H * 4 + K_TOP * I * 4 * 2
+                        + E * 4 * 2)
     achieved = per_launch_bytes / (kern_ms / 1e3) / 1e9
     out = {
         "metric": METRIC,
@@ -457,16 +462,16 @@ def run_ours(args):
                    "expert_bytes_per_step": wl.expert_bytes_per_step(),
                    "l2": "inputs larger than L2: 1.33 GB of distinct expert records per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph, 3 kernels per layer (router logits with RMS chaining on every SM; top-k; one-shot expert pass), programmatic dependent launch"},
+                   "launch": "CUDA graph, 1 kernel per layer (moe_decode_layer: RMS chaining, router logits and top-k, then the one-shot expert pass, in one launch), programmatic dependent launch"},
         "tokens_per_s": round(world * 1e3 / ms, 2),
         "hbm_frac": {"of_measured": round(value / world / peak, 4), "measured_gbs": peak,
                      "of_nominal_8000": round(value / world / 8000.0, 4)},
-        "roofline": {"bound": "hbm", "kernel": "moe_experts_decode: oneshot_kernel (one launch: TMA bulk copies, gate/up, grid barrier, down, last-arriver combine)",
+        "roofline": {"bound": "hbm", "kernel": "moe_decode_layer: oneshot_kernel (router logits + top-k, grid barrier, TMA bulk copies, gate/up, grid barrier, down)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "peak_kind": peak_kind + " (burst copy)",
                      "frac": round(achieved / peak, 4),
                      "bytes_per_launch": per_launch_bytes, "avg_launch_us": round(kern_ms * 1e3, 3),
-                     "traffic": _traffic_from_profiles("moe_experts_decode")},
+                     "traffic": _traffic_from_profiles("moe_decode_layer")},
         "gpu_launches": wl.kernels_per_step * steps,
         "clocks": clocks,
         "e2e": e2e,
@@ -584,8 +589,9 @@ def run_reference(args):
 
 
 def run_profile_case(args):
-    """A small case of one kernel family for ncu: the decode layer on a 64-expert
-    pool (177 MB of records, larger than L2), or the prompt layer."""
+    """A small case of one kernel family for ncu: one decode layer (a 512-expert
+    router over a 64-record pool, 177 MB of records, larger than L2), or the
+    prompt layer."""
     import torch
 
     from block_scaled_fp4_softmax_gb300 import build, moe, synth
@@ -599,14 +605,14 @@ def run_profile_case(args):
         for e in range(nE):
             g, up, d = synth.expert_weights(H, I, synth.expert_seed(0, 0, e), device=dev)
             moe.fp4_pack_expert(g, up, d, s, record=pool[e])
-        ptrs = moe.pointer_table([pool[e] for e in range(nE)])
-        wr = synth.router_weights(nE, H, synth.seed_of(0, 0, synth.T_ROUTER), device=dev)
+        # a 512-expert router over the 64 records (expert e -> record e % 64)
+        ptrs = moe.pointer_table([pool[e % nE] for e in range(E)])
+        wr = synth.router_weights(E, H, synth.seed_of(0, 0, synth.T_ROUTER), device=dev)
         ws = torch.zeros(moe.moe_experts_decode_workspace(1, K_TOP, s), dtype=torch.uint8, device=dev)
         y = torch.empty(1, H, dtype=torch.float32, device=dev)
         for i in range(args.warmup + args.steps):
             x = synth.activations(1, H, synth.seed_of(0, 50 + i, synth.T_X), device=dev)
-            idx, w, _ = moe.moe_router_topk(x, wr, None, K_TOP)
-            moe.moe_experts_decode(x, idx, w, ptrs, s, y, ws)
+            moe.moe_decode_layer(wr, None, K_TOP, ptrs, s, x=x, y=y, workspace=ws)
         torch.cuda.synchronize()
     else:
         pl = PromptLayer(torch, moe, synth, dev)

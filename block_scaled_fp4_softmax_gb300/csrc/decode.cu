@@ -811,7 +811,7 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
   if (decode_oneshot_fits(T, k, s.hidden, s.inter, s.format, sm_count(), (size_t)stream_smem_limit())) {
-    DecodeOneshotArgs oa;
+    DecodeOneshotArgs oa = {};
     oa.x = x_bf16;
     oa.idx = idx;
     oa.w = weights;
@@ -855,6 +855,51 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
                                         s.inter, y, hws, dev_status, st);
   return launch_decode<MOE_FMT_MXFP4>(x_bf16, idx, weights, T, k, expert_ptrs, E, s.hidden,
                                       s.inter, y, hws, dev_status, st);
+}
+
+// One decode layer in one launch: the router (RMS chaining of the previous
+// layer's output or the given x, logits, top-k) and the expert pass of the
+// one-shot kernel, with a grid barrier between them.
+extern "C" int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int T, double eps,
+                                uint16_t* x_out, const uint16_t* wr_bf16, const float* bias, int E, int k,
+                                int32_t* idx, float* weights, float* logits,
+                                const void* const* expert_ptrs, moe_expert_shape s, float* y,
+                                void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if ((x_bf16 == nullptr) == (y_prev == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (y_prev && !x_out) return MOE_ERR_INVALID_ARG;
+  if (!wr_bf16 || !idx || !weights || !logits || !expert_ptrs || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || E <= 0 || k <= 0 || k > E || k > 32 || !(eps >= 0.0)) return MOE_ERR_INVALID_ARG;
+  if (!moe::shape_ok(s) || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_experts_decode_workspace(T, k, s)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((x_bf16 && !moe::aligned16(x_bf16)) || (x_out && !moe::aligned16(x_out)) || !moe::aligned16(wr_bf16) ||
+      !moe::aligned16(workspace))
+    return MOE_ERR_ALIGNMENT;
+  if (!decode_oneshot_fits(T, k, s.hidden, s.inter, s.format, sm_count(), (size_t)stream_smem_limit(), true))
+    return MOE_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeOneshotArgs oa = {};
+  oa.x = x_bf16;
+  oa.T = T;
+  oa.k = k;
+  oa.ptrs = expert_ptrs;
+  oa.E = E;
+  oa.H = s.hidden;
+  oa.I = s.inter;
+  oa.bar = reinterpret_cast<unsigned long long*>(ws);
+  oa.hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
+  oa.y = y;
+  oa.status = dev_status;
+  oa.y_prev = y_prev;
+  oa.eps = (float)eps;
+  oa.x_out = x_out;
+  oa.wr = wr_bf16;
+  oa.bias = bias;
+  oa.logits = logits;
+  oa.idx_out = idx;
+  oa.w_out = weights;
+  return launch_decode_oneshot(oa, s.format, sm_count(), stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -25,6 +25,7 @@
 #include "common.cuh"
 #include "decode_math.cuh"
 #include "decode_oneshot.h"
+#include "router_math.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -37,7 +38,7 @@ struct Tab {
   float wts[kMaxPairs];
   float tsc[kMaxPairs];      // per token: 2^-e of the FP16 scale of x
   unsigned amax[kMaxPairs];  // max |.| as float bits (x per token, then h per segment)
-  int flags[4];              // [0] abort, [1] grid barrier passed
+  int flags[4];              // [0] abort, [1] grid barrier passed, [2] router barrier passed
   int npieces, nseg1, nseg2, ncopies;
   int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];
   uint32_t poff[kMaxPieces];  // piece: gate rows at codes1 + poff, up rows right after
@@ -168,13 +169,40 @@ __device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status) {
   return false;
 }
 
+// Grid barrier, called by one thread per CTA: one arrival on a counter that
+// only grows; this launch's CTAs wait for the next multiple of the grid size
+// (consecutive barriers of a launch share the counter).  False on timeout,
+// which also flags the launch.
+__device__ bool grid_sync_thread(unsigned long long* bar, Tab& tb, int32_t* status) {
+  volatile int* abort_flag = tb.flags;
+  int good = !*abort_flag;
+  if (good) {
+    unsigned long long old;
+    asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(bar) : "memory");
+    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+    const uint64_t dl = global_ns() + kWaitNs;
+    while (dm::ld_acquire_u64(bar) < target) {
+      if (global_ns() > dl) {
+        good = 0;
+        break;
+      }
+    }
+  }
+  if (!good) {
+    *abort_flag = 1;
+    status_or(status, MOE_DEV_TIMEOUT);
+  }
+  return good;
+}
+
 template <int FMT, int UPR, int UPDR>
 __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   pdl_launch_dependents();
   constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
-  const Geo g = make_geo(a.T, a.k, a.H, a.I, G, gridDim.x);
+  const bool fused = a.wr != nullptr;
+  const Geo g = make_geo(a.T, a.k, a.H, a.I, G, gridDim.x, fused);
   const RecordOffsets o = record_offsets(a.H, a.I, FMT);
   const int upr = UPR > 0 ? UPR : a.H >> 5;
   const int updr = UPDR > 0 ? UPDR : a.I >> 5;
@@ -199,14 +227,82 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // the pointer table does not depend on the previous kernel: warm L2 with it
   for (int i = threadIdx.x; i < (a.E * 8 + 127) / 128; i += kThreads)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.ptrs) + (size_t)i * 128));
+  // router rows of this CTA's experts (fused launch): W_r does not depend on
+  // the previous kernel either
+  const int epc = (a.E + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int re0 = blockIdx.x * epc, rne = fused ? max(0, min(epc, a.E - re0)) : 0;
+  {
+    const char* wb = fused ? reinterpret_cast<const char*>(a.wr + (size_t)re0 * a.H) : nullptr;
+    for (size_t off = (size_t)threadIdx.x * 128; off < (size_t)rne * a.H * 2; off += (size_t)kThreads * 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
+  }
   __syncthreads();
   pdl_wait();
 
+  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
+  if (fused) {
+    // ---------------------------------------------------------- router
+    // x = RMS chaining of y_prev (or x itself), the logits of this CTA's
+    // experts, a grid barrier, then every CTA takes the top-k of all logits
+    // itself; the same fixed orders as the router kernels, so the same bits
+    float* rpart = reinterpret_cast<float*>(smem + g.off_xb);
+    for (int t = 0; t < a.T; ++t) {
+      if (a.y_prev) {
+        const float* yr = a.y_prev + (size_t)t * a.H;
+        const float r = rt::rms_inv_fixed_order(yr, a.H, a.eps, rpart);
+        for (int i = threadIdx.x; i < a.H; i += kThreads) {
+          const uint16_t x16 = rt::f32_to_bf16_bits(__fmul_rn(yr[i], r));
+          xb[(size_t)t * a.H + i] = x16;
+          if (blockIdx.x == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = x16;
+        }
+      } else {
+        for (int i = threadIdx.x * 8; i < a.H; i += kThreads * 8) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + i));
+          *reinterpret_cast<uint4*>(xb + (size_t)t * a.H + i) = v;
+          if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(a.x_out + (size_t)t * a.H + i) = v;
+        }
+      }
+    }
+    __syncthreads();
+    for (int task = warp; task < a.T * rne; task += kThreads / 32) {
+      const int t = task / rne, q = task - t * rne;
+      const float v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
+      if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, tb, a.status);
+    __syncthreads();
+    const bool have_logits = tb.flags[2] != 0;
+    unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
+    for (int t = 0; t < a.T; ++t) {
+      int my_e = 0;
+      float my_l = 0.0f;
+      if (have_logits) rt::topk_block<kThreads / 32>(a.logits + (size_t)t * a.E, a.E, a.k, fin, my_e, my_l);
+      if (warp == 0) {
+        const float wgt = rt::topk_weight(lane, a.k, my_l);
+        if (lane < a.k) {
+          const int p = t * a.k + lane;
+          tb.recs[p] = have_logits ? dm::checked_record(my_e, a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr)
+                                   : nullptr;
+          tb.wts[p] = wgt;
+          if (blockIdx.x == 0) {
+            a.idx_out[p] = my_e;
+            a.w_out[p] = wgt;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
   if (warp == kCWarps) {
     // ------------------------------------------------------------ loader
-    for (int p = lane; p < P; p += 32) {
-      tb.recs[p] = dm::checked_record(a.idx[p], a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr);
-      tb.wts[p] = a.w[p];
+    if (!fused) {
+      for (int p = lane; p < P; p += 32) {
+        tb.recs[p] = dm::checked_record(a.idx[p], a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr);
+        tb.wts[p] = a.w[p];
+      }
     }
     __syncwarp();
     asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");  // records are in place
@@ -233,14 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // (exact: BF16 has 8 significant bits and the scaled values lie in FP16's
   // normal range)
   const int nx8 = a.T * a.H / 8;
-  const uint4* xg = reinterpret_cast<const uint4*>(a.x);
+  const uint4* xg = reinterpret_cast<const uint4*>(fused ? xb : a.x);
   uint4 xr = make_uint4(0u, 0u, 0u, 0u);
   for (int b = warp * 32; b < nx8; b += kCThreads) {
     const int q = b + lane;
     unsigned m = 0u;
     int key = -1;
     if (q < nx8) {
-      const uint4 v = __ldg(xg + q);
+      const uint4 v = fused ? xg[q] : __ldg(xg + q);
       if (b == warp * 32) xr = v;
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -254,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   for (int b = warp * 32; b < nx8; b += kCThreads) {
     const int q = b + lane;
     if (q < nx8) {
-      const uint4 v = b == warp * 32 ? xr : __ldg(xg + q);
+      const uint4 v = b == warp * 32 ? xr : (fused ? xg[q] : __ldg(xg + q));
       const int t = q * 8 / a.H, hh = q * 8 - t * a.H;
       const float sc = dm::pow2f(dm::f16_shift(__uint_as_float(tb.amax[t])));
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -329,26 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // counter that only grows; this launch's CTAs wait for the next multiple of
   // the grid size
   tc::named_sync(1, kCThreads);
-  if (threadIdx.x == 0) {
-    int good = !*abort_flag;
-    if (good) {
-      unsigned long long old;
-      asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(a.bar) : "memory");
-      const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
-      const uint64_t dl = global_ns() + kWaitNs;
-      while (dm::ld_acquire_u64(a.bar) < target) {
-        if (global_ns() > dl) {
-          good = 0;
-          break;
-        }
-      }
-    }
-    if (!good) {
-      *abort_flag = 1;
-      status_or(a.status, MOE_DEV_TIMEOUT);
-    }
-    tb.flags[1] = good;
-  }
+  if (threadIdx.x == 0) tb.flags[1] = grid_sync_thread(a.bar, tb, a.status);
   tc::named_sync(1, kCThreads);
 
   // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats
@@ -467,7 +544,7 @@ int launch_shape(const DecodeOneshotArgs& a, int grid, size_t smem, cudaStream_t
 
 template <int FMT>
 int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
-  const Geo g = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid);
+  const Geo g = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid, a.wr != nullptr);
   // the row strides are compile-time constants for the decode model shape
   if (a.H == 2560 && a.I == 640) return launch_shape<FMT, 80, 20>(a, grid, g.total, stream);
   return launch_shape<FMT, 0, 0>(a, grid, g.total, stream);
@@ -476,10 +553,10 @@ int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
 }  // namespace os
 }  // namespace moe
 
-bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit) {
+bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit, bool fused) {
   using namespace moe::os;
   if (grid <= 0 || T <= 0 || k <= 0 || (long long)T * k > kMaxPairs) return false;
-  const Geo g = make_geo(T, k, H, I, fmt == MOE_FMT_NVFP4 ? 16 : 32, grid);
+  const Geo g = make_geo(T, k, H, I, fmt == MOE_FMT_NVFP4 ? 16 : 32, grid, fused);
   if (g.total + 1024 > smem_limit) return false;
   if (g.segs1 > kMaxSegs || g.segs2 > kMaxSegs || max_pieces(g) > kMaxPieces) return false;
   if (g.copies > kMaxCopies || k > kMaxK) return false;

@@ -45,10 +45,12 @@ struct Geo {
   int copies;         // most bulk copies of one CTA
   int hstride;        // floats per pair in the staged h (4 quads x I/32 units x 8, padded)
   // shared-memory regions (bytes from the start of dynamic shared memory)
-  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, off_part, total;
+  size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, off_part, off_xb, total;
 };
 
-__host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid) {
+// fused: the launch also runs the router (256 RMS partial sums, 512 top-k
+// finalists and the BF16 x get a region of their own).
+__host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid, bool fused = false) {
   Geo g;
   g.T = T; g.k = k; g.H = H; g.I = I; g.G = G; g.grid = grid;
   const long long P = (long long)T * k;
@@ -83,6 +85,8 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   o += a1 > a2 ? a1 : a2;                         // x (FP16), then h (FP32)
   g.off_part = o = round_up(o, 128);
   o += (size_t)g.rows2 * k * 4;                   // weighted expert outputs per row
+  g.off_xb = o = round_up(o, 128);
+  if (fused) o += 1024 + 4096 + (size_t)T * H * 2;  // RMS partial sums, top-k finalists, x (BF16)
   g.total = round_up(o, 128);
   return g;
 }
@@ -95,7 +99,8 @@ __host__ __device__ inline int max_pieces(const Geo& g) { return (g.rows1 + g.np
 
 // One-shot decode expert pass: true when the shape fits (the caller then
 // launches it with launch_decode_oneshot).
-bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit);
+bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit,
+                         bool fused = false);
 
 struct DecodeOneshotArgs {
   const uint16_t* x;
@@ -108,5 +113,16 @@ struct DecodeOneshotArgs {
   float* hws;               // [P][I] SwiGLU intermediate
   float* y;
   int32_t* status;
+  // router, when the launch runs the whole layer (wr != NULL): x = RMS
+  // chaining of y_prev (or x itself when y_prev is NULL), written to x_out;
+  // logits of all E experts; top-k written to idx_out / w_out
+  const float* y_prev;
+  float eps;
+  uint16_t* x_out;
+  const uint16_t* wr;
+  const float* bias;
+  float* logits;
+  int32_t* idx_out;
+  float* w_out;
 };
 int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream);

@@ -7,6 +7,7 @@
 // waits on the router's answer, so routing stays on the device here and no
 // index ever travels to the host.
 #include "common.cuh"
+#include "router_math.cuh"
 
 namespace {
 
@@ -93,123 +94,36 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Top-k.  One warp per token.  Each candidate gets a 64-bit key
-// (ordered logit bits << 32 | ~expert) so that the maximum is the larger logit
-// and, on equal logits, the lower expert index.  NaN ranks below -inf, -0
-// counts as +0.  k rounds of warp arg-max pick the experts in order.
+// Top-k.  One warp per token: candidates keyed by (ordered logit, ~expert),
+// k rounds of warp arg-max (moe::rt::warp_select_topk), weights renormalised
+// over the picks.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t ordered_key(float v) {
-  if (v != v) return 1u;
-  if (v == 0.0f) v = 0.0f;
-  const uint32_t b = __float_as_uint(v);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_to_float(uint32_t k) {
-  if (k == 1u) return __uint_as_float(0x7FC00000u);
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// Selects the k best of the lanes' candidates (composite keys, unique): round
-// r takes the largest key below round r-1's winner, so nothing is ever
-// removed and the candidate array stays in registers.  Lane r ends with
-// expert r and its logit.
-template <int EPL>
-__device__ __forceinline__ void warp_select_topk(const unsigned long long (&cand)[EPL], int k,
-                                                 int lane, int& my_e, float& my_l) {
-  unsigned long long prev = ~0ull;
-  my_e = 0;
-  my_l = 0.0f;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (cand[i] < prev && cand[i] > best) best = cand[i];
-    // warp maximum of the 64-bit keys: the high words first, then the low
-    // words among the lanes that hold the highest high word
-    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
-    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
-    best = ((unsigned long long)hi << 32) | lo;
-    prev = best;
-    if (lane == r) {
-      my_e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
-      my_l = key_to_float((uint32_t)(best >> 32));
-    }
-  }
-}
-
-// Writes idx/weights of one token from the selection above.
-__device__ __forceinline__ void write_topk(int lane, int k, int my_e, float my_l, int32_t* idx,
-                                           float* weights) {
-  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-  const float ex = lane < k ? expf(my_l - l0) : 0.0f;
-  const float sum = moe::warp_sum(ex);
-  if (lane < k) {
-    idx[lane] = my_e;
-    weights[lane] = __fdiv_rn(ex, sum);
-  }
-}
-
-template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E,
-                                                   int k, int32_t* __restrict__ idx,
-                                                   float* __restrict__ weights) {
+// One block of kTopkThreads per token: every warp picks the k best of its
+// share of the candidates, then warp 0 the k best of those.
+constexpr int kTopkThreads = 512;
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                            int k, int32_t* __restrict__ idx,
+                                                            float* __restrict__ weights) {
+  __shared__ unsigned long long fin[kTopkThreads];
   moe::pdl_launch_dependents();
   moe::pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
-  unsigned long long cand[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    cand[i] = 0ull;
-    if (e < E) {
-      const uint32_t key = ordered_key(logits[(size_t)t * E + e]);
-      cand[i] = ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)e);
+  const int lane = threadIdx.x & 31, t = blockIdx.x;
+  int my_e = 0;
+  float my_l = 0.0f;
+  moe::rt::topk_block<kTopkThreads / 32>(logits + (size_t)t * E, E, k, fin, my_e, my_l);
+  if (threadIdx.x < 32) {
+    const float w = moe::rt::topk_weight(lane, k, my_l);
+    if (lane < k) {
+      idx[(size_t)t * k + lane] = my_e;
+      weights[(size_t)t * k + lane] = w;
     }
   }
-  int my_e;
-  float my_l;
-  warp_select_topk<EPL>(cand, k, lane, my_e, my_l);
-  write_topk(lane, k, my_e, my_l, idx + (size_t)t * k, weights + (size_t)t * k);
 }
 
 // ---------------------------------------------------------------------------
-// RMS chaining in FP32, one fixed order (so the BF16 result is reproducible):
-// thread t of 256 sums y[t + 256 m]^2 for m ascending (square rounded, then
-// added), a pairwise tree combines the 256 partial sums, mean = sum / H,
-// r = 1 / sqrt(mean + eps) with IEEE sqrt and divide, x = BF16_rn(y * r).
+// RMS chaining in FP32 in one fixed order (moe::rt::rms_inv_fixed_order),
+// x = BF16_rn(y * r).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ yr, int H, float eps,
-                                                     float* part) {
-  float acc = 0.0f;
-  constexpr int kBatch = 8;  // loads in flight; the adds keep the order above
-  for (int i0 = threadIdx.x; i0 < H; i0 += 256 * kBatch) {
-    float v[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) v[b] = i0 + 256 * b < H ? yr[i0 + 256 * b] : 0.0f;
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b)
-      if (i0 + 256 * b < H) acc = __fadd_rn(acc, __fmul_rn(v[b], v[b]));
-  }
-  part[threadIdx.x] = acc;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) part[threadIdx.x] = __fadd_rn(part[threadIdx.x], part[threadIdx.x + w]);
-    __syncthreads();
-  }
-  const float mean = __fdiv_rn(part[0], (float)H);
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-  __syncthreads();  // part[] may be reused by the caller
-  return r;
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
-  const __nv_bfloat16 b = __float2bfloat16_rn(v);
-  return *reinterpret_cast<const uint16_t*>(&b);
-}
-
 __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restrict__ y, int H,
                                                            float eps,
                                                            uint16_t* __restrict__ x) {
@@ -218,8 +132,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
   moe::pdl_wait();
   const int t = blockIdx.x;
   const float* yr = y + (size_t)t * H;
-  const float r = rms_inv_fixed_order(yr, H, eps, part);
-  for (int i = threadIdx.x; i < H; i += 256) x[(size_t)t * H + i] = f32_to_bf16_bits(__fmul_rn(yr[i], r));
+  const float r = moe::rt::rms_inv_fixed_order(yr, H, eps, part);
+  for (int i = threadIdx.x; i < H; i += 256) x[(size_t)t * H + i] = moe::rt::f32_to_bf16_bits(__fmul_rn(yr[i], r));
 }
 
 // ---------------------------------------------------------------------------
@@ -265,7 +179,7 @@ __global__ void __launch_bounds__(kGridThreads) router_grid_kernel(GridArgs a) {
   for (int t = 0; t < a.T; ++t) {
     if (a.y_prev) {
       const float* yr = a.y_prev + (size_t)t * a.H;
-      const float r = rms_inv_fixed_order(yr, a.H, a.eps, part);
+      const float r = moe::rt::rms_inv_fixed_order(yr, a.H, a.eps, part);
       constexpr int kBatch = 8;
       for (int i0 = threadIdx.x; i0 < a.H; i0 += kGridThreads * kBatch) {
         float v[kBatch];
@@ -275,7 +189,7 @@ __global__ void __launch_bounds__(kGridThreads) router_grid_kernel(GridArgs a) {
         for (int b = 0; b < kBatch; ++b) {
           const int i = i0 + kGridThreads * b;
           if (i < a.H) {
-            const uint16_t x16 = f32_to_bf16_bits(__fmul_rn(v[b], r));
+            const uint16_t x16 = moe::rt::f32_to_bf16_bits(__fmul_rn(v[b], r));
             xs[(size_t)t * a.H + i] = x16;
             if (blockIdx.x == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = x16;
           }
@@ -289,39 +203,10 @@ __global__ void __launch_bounds__(kGridThreads) router_grid_kernel(GridArgs a) {
   }
   __syncthreads();
 
-  // logits: task (token t, expert q) -> warp; lane j -> chunks j, j+32, ...
-  const int nchunk = a.H >> 3;
+  // logits: task (token t, expert q) -> warp, in the fixed order
   for (int task = warp; task < a.T * ne; task += kGridThreads / 32) {
     const int t = task / ne, q = task - t * ne;
-    const uint16_t* wrow = a.wr + (size_t)(e0 + q) * a.H;
-    const uint16_t* xrow = xs + (size_t)t * a.H;
-    float acc = 0.0f;
-    // up to kBatch of the lane's chunks in flight; accumulated in chunk order
-    constexpr int kBatch = 8;
-    for (int c0 = lane; c0 < nchunk; c0 += 32 * kBatch) {
-      uint4 wv[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int c = c0 + 32 * b;
-        wv[b] = c < nchunk ? __ldg(reinterpret_cast<const uint4*>(wrow + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int c = c0 + 32 * b;
-        if (c < nchunk) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 8 * c);
-          const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float xf = moe::bf16_bits_to_f32((i & 1) ? (xw[i >> 1] >> 16) : (xw[i >> 1] & 0xFFFFu));
-            const float wf = moe::bf16_bits_to_f32((i & 1) ? (ww[i >> 1] >> 16) : (ww[i >> 1] & 0xFFFFu));
-            acc = __fmaf_rn(xf, wf, acc);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+    const float acc = moe::rt::logit_dot(xs + (size_t)t * a.H, a.wr + (size_t)(e0 + q) * a.H, a.H, lane);
     if (lane == 0) {
       const int e = e0 + q;
       a.logits[(size_t)t * a.E + e] = a.bias ? __fadd_rn(acc, a.bias[e]) : acc;
@@ -346,15 +231,7 @@ bool grid_fits(int T, int H, int E) {
 }
 
 int launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* weights, cudaStream_t st) {
-  const int threads = 256;
-  const dim3 grid((unsigned)(((long long)T * 32 + threads - 1) / threads));
-  const int epl = (E + 31) / 32;
-  if (epl <= 1) return moe::launch_pdl(topk_kernel<1>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  if (epl <= 2) return moe::launch_pdl(topk_kernel<2>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  if (epl <= 4) return moe::launch_pdl(topk_kernel<4>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  if (epl <= 8) return moe::launch_pdl(topk_kernel<8>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  if (epl <= 16) return moe::launch_pdl(topk_kernel<16>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
-  return moe::launch_pdl(topk_kernel<32>, grid, dim3(threads), 0, st, logits, T, E, k, idx, weights);
+  return moe::launch_pdl(topk_kernel, dim3(T), dim3(kTopkThreads), 0, st, logits, T, E, k, idx, weights);
 }
 
 // Logits on the whole GPU, then the top-k.

@@ -1,0 +1,217 @@
+// Router arithmetic shared by the router kernels and the fused decode layer:
+// the fixed summation orders that make logits, the top-k choice and the RMS
+// chaining reproducible bit for bit ("Running a 133 GB MoE model on an 8 GB
+// GPU at 11 tokens/s by streaming experts from NVMe", section "Why this
+// model": top-10 of 512 experts per layer, weights renormalised over the
+// chosen ones).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace rt {
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
+}
+
+// RMS chaining in FP32, one fixed order: thread t of 256 sums y[t + 256 m]^2
+// for m ascending (square rounded, then added), a pairwise tree combines the
+// 256 partial sums, mean = sum / H, r = 1 / sqrt(mean + eps) with IEEE sqrt
+// and divide.  Every thread of the block calls it (blockDim >= 256); threads
+// from 256 on only take part in the barriers.  part: 256 floats of shared
+// memory.
+__device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ yr, int H, float eps,
+                                                     float* part) {
+  if (threadIdx.x < 256) {
+    float acc = 0.0f;
+    constexpr int kBatch = 8;  // loads in flight; the adds keep the order above
+    for (int i0 = threadIdx.x; i0 < H; i0 += 256 * kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) v[b] = i0 + 256 * b < H ? yr[i0 + 256 * b] : 0.0f;
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b)
+        if (i0 + 256 * b < H) acc = __fadd_rn(acc, __fmul_rn(v[b], v[b]));
+    }
+    part[threadIdx.x] = acc;
+  }
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] = __fadd_rn(part[threadIdx.x], part[threadIdx.x + w]);
+    __syncthreads();
+  }
+  const float mean = __fdiv_rn(part[0], (float)H);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+  __syncthreads();  // part[] may be reused by the caller
+  return r;
+}
+
+// One logit without bias, by one warp: lane j walks the chunks of 8 elements
+// c = j, j+32, j+64, ... (ascending), elements inside a chunk in order, one
+// FMA each (the BF16 x BF16 product is exact, so the FMA is the FP32 add of
+// the exact product); the 32 lane sums are combined with an xor butterfly
+// d = 16, 8, 4, 2, 1.  x_row may be in shared or global memory; w_row is read
+// through the read-only path.  Every lane returns the logit.
+__device__ __forceinline__ float logit_dot(const uint16_t* x_row, const uint16_t* __restrict__ w_row, int H,
+                                           int lane) {
+  const int nchunk = H >> 3;
+  float acc = 0.0f;
+  constexpr int kBatch = 10;  // chunks of a lane in flight; accumulated in chunk order
+  for (int c0 = lane; c0 < nchunk; c0 += 32 * kBatch) {
+    uint4 wv[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int c = c0 + 32 * b;
+      wv[b] = c < nchunk ? __ldg(reinterpret_cast<const uint4*>(w_row + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int c = c0 + 32 * b;
+      if (c < nchunk) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x_row + 8 * c);
+        const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float xf = bf16_bits_to_f32((i & 1) ? (xw[i >> 1] >> 16) : (xw[i >> 1] & 0xFFFFu));
+          const float wf = bf16_bits_to_f32((i & 1) ? (ww[i >> 1] >> 16) : (ww[i >> 1] & 0xFFFFu));
+          acc = __fmaf_rn(xf, wf, acc);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+  return acc;
+}
+
+// Top-k keys: (ordered logit bits << 32 | ~expert), so the maximum is the
+// larger logit and, on equal logits, the lower expert index.  NaN ranks below
+// -inf, -0 counts as +0.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  if (v != v) return 1u;
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  if (k == 1u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Selects the k best of the lanes' candidates (composite keys, unique): round
+// r takes the largest key below round r-1's winner, so nothing is ever
+// removed and the candidate array stays in registers.  Lane r ends with
+// expert r and its logit.
+template <int EPL>
+__device__ __forceinline__ void warp_select_topk(const unsigned long long (&cand)[EPL], int k, int lane,
+                                                 int& my_e, float& my_l) {
+  unsigned long long prev = ~0ull;
+  my_e = 0;
+  my_l = 0.0f;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (cand[i] < prev && cand[i] > best) best = cand[i];
+    // warp maximum of the 64-bit keys: the high words first, then the low
+    // words among the lanes that hold the highest high word
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+    best = ((unsigned long long)hi << 32) | lo;
+    prev = best;
+    if (lane == r) {
+      my_e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
+      my_l = key_to_float((uint32_t)(best >> 32));
+    }
+  }
+}
+
+// Renormalised softmax weight of lane r's pick (lanes >= k get 0).
+__device__ __forceinline__ float topk_weight(int lane, int k, float my_l) {
+  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane < k ? expf(my_l - l0) : 0.0f;
+  const float sum = warp_sum(ex);
+  return lane < k ? __fdiv_rn(ex, sum) : 0.0f;
+}
+
+// Candidates of one token from its E logits (global memory, read through L2),
+// then the selection above.
+template <int EPL>
+__device__ __forceinline__ void topk_from_logits(const float* lrow, int E, int k, int lane, int& my_e,
+                                                 float& my_l) {
+  unsigned long long cand[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    cand[i] = 0ull;
+    if (e < E) {
+      const uint32_t key = ordered_key(__ldcg(lrow + e));
+      cand[i] = ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)e);
+    }
+  }
+  warp_select_topk<EPL>(cand, k, lane, my_e, my_l);
+}
+
+// The same for any E <= 1024.
+__device__ __forceinline__ void topk_any(const float* lrow, int E, int k, int lane, int& my_e, float& my_l) {
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) topk_from_logits<1>(lrow, E, k, lane, my_e, my_l);
+  else if (epl <= 2) topk_from_logits<2>(lrow, E, k, lane, my_e, my_l);
+  else if (epl <= 4) topk_from_logits<4>(lrow, E, k, lane, my_e, my_l);
+  else if (epl <= 8) topk_from_logits<8>(lrow, E, k, lane, my_e, my_l);
+  else if (epl <= 16) topk_from_logits<16>(lrow, E, k, lane, my_e, my_l);
+  else topk_from_logits<32>(lrow, E, k, lane, my_e, my_l);
+}
+
+// Top-k of one token's E <= 1024 logits by a whole block of NW warps: every
+// warp selects the k best of its candidates (expert e = warp * 32 + lane +
+// 32 * NW * m), then warp 0 selects the k best of those NW * k finalists.
+// The k best of a union are the k best of the parts' k best (keys are
+// unique), so the picks and their order are exactly those of a single-warp
+// selection.  fin: NW * 32 keys of shared memory.  Every thread calls it;
+// warp 0, lane r < k, ends with pick r.
+template <int NW>
+__device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsigned long long* fin, int& my_e,
+                                           float& my_l) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kPer = (1024 + 32 * NW - 1) / (32 * NW);  // candidates per lane
+  unsigned long long cand[kPer];
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) {
+    const int e = warp * 32 + lane + 32 * NW * m;
+    cand[m] = 0ull;
+    if (e < E) cand[m] = ((unsigned long long)ordered_key(__ldcg(lrow + e)) << 32) | (unsigned long long)(~(uint32_t)e);
+  }
+  if (warp < NW) {
+    unsigned long long prev = ~0ull;
+    for (int r = 0; r < k; ++r) {  // the warp's r-th best key, kept by lane r
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int m = 0; m < kPer; ++m)
+        if (cand[m] < prev && cand[m] > best) best = cand[m];
+      const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+      const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+      best = ((unsigned long long)hi << 32) | lo;
+      prev = best;
+      if (lane == r) fin[warp * 32 + r] = best;
+    }
+    if (lane >= k) fin[warp * 32 + lane] = 0ull;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long c2[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) c2[i] = fin[i * 32 + lane];
+    warp_select_topk<NW>(c2, k, lane, my_e, my_l);
+  }
+  __syncthreads();  // fin[] may be reused by the caller
+}
+
+}  // namespace rt
+}  // namespace moe

@@ -35,6 +35,7 @@ EXPORTS = (
     "moe_rmsnorm_router_topk",
     "moe_experts_decode_workspace",
     "moe_experts_decode",
+    "moe_decode_layer",
     "moe_experts_decode_noalloc_limit",
     "moe_experts_decode_noalloc",
     "moe_bucket_workspace",
@@ -74,6 +75,8 @@ _SIGS = {
     "moe_experts_decode_workspace": (_sz, [_i, _i, ExpertShape]),
     "moe_experts_decode": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _sz,
                                 _vp, _vp]),
+    "moe_decode_layer": (_i, [_vp, _vp, _i, ctypes.c_double, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp,
+                              ExpertShape, _vp, _vp, _sz, _vp, _vp]),
     "moe_experts_decode_noalloc_limit": (_sz, []),
     "moe_experts_decode_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _vp]),
     "moe_bucket_workspace": (_sz, [_i, _i, _i]),
@@ -228,6 +231,45 @@ def pointer_table(records, device=None):
     addrs = [0 if r is None else r.data_ptr() for r in records]
     dev = device or next(r.device for r in records if r is not None)
     return torch.tensor(addrs, dtype=torch.int64, device=dev)
+
+
+def moe_decode_layer(wr, bias, k: int, ptrs, s: ExpertShape, x=None, y_prev=None, eps: float = 1e-6,
+                     x_out=None, idx=None, weights=None, logits=None, y=None, workspace=None,
+                     dev_status=None, stream=None):
+    """Router and expert pass of one decode layer in one launch; exactly one of
+    x (BF16) and y_prev (FP32, RMS-chained into x_out) is given.  Returns
+    (x_out, idx, weights, logits, y)."""
+    if (x is None) == (y_prev is None):
+        raise ValueError("give exactly one of x and y_prev")
+    src = x if x is not None else y_prev
+    if x is not None:
+        _cuda(x, "x", torch.bfloat16)
+    else:
+        _cuda(y_prev, "y_prev", torch.float32)
+    _cuda(wr, "wr", torch.bfloat16)
+    _cuda(ptrs, "expert_ptrs", torch.int64)
+    if bias is not None:
+        _cuda(bias, "bias", torch.float32)
+    T, H = src.shape
+    E = wr.shape[0]
+    dev = src.device
+    if x_out is None and y_prev is not None:
+        x_out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if idx is None:
+        idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(T, k, dtype=torch.float32, device=dev)
+    if logits is None:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    if y is None:
+        y = torch.empty(T, H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(max(moe_experts_decode_workspace(T, k, s), 16), dtype=torch.uint8, device=dev)
+    _check(load().moe_decode_layer(_ptr(x), _ptr(y_prev), T, float(eps), _ptr(x_out), _ptr(wr), _ptr(bias),
+                                   E, k, _ptr(idx), _ptr(weights), _ptr(logits), _ptr(ptrs), s, _ptr(y),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _ptr(dev_status), _stream(stream)), "moe_decode_layer")
+    return x_out, idx, weights, logits, y
 
 
 def moe_experts_decode(x, idx, weights, ptrs, s: ExpertShape, y=None, workspace=None,

@@ -168,6 +168,29 @@ int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* 
                        moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
                        int32_t* dev_status, void* stream);
 
+/* One decode layer in one launch (first page, "The engine", item 4, and
+ * "Where the time actually goes": the expert work of a layer waits on the
+ * router's answer, so router and experts share the launch and no index
+ * leaves the device).  Computes exactly what moe_rmsnorm_router_topk (or
+ * moe_router_topk when x_bf16 is given) followed by moe_experts_decode
+ * compute, with the same outputs bit for bit:
+ *  - exactly one of x_bf16 [T x H] (this layer's input) and y_prev [T x H]
+ *    FP32 (the previous layer's output, RMS-chained with eps into x_out,
+ *    which is then required) is non-NULL; x_out may be NULL with x_bf16;
+ *  - logits [T x E], idx / weights [T x k] as the router entries write them;
+ *  - y [T x H] as moe_experts_decode writes it; y may be the same buffer as
+ *    y_prev (every read of y_prev precedes every write of y).
+ * H = s.hidden; expert_ptrs holds E records; bias may be NULL.  The
+ * workspace is moe_experts_decode's (same size, same zero-fill rule).
+ * Shapes the one-shot expert pass does not cover (T*k > 64, or a per-SM
+ * share larger than shared memory) return MOE_ERR_UNSUPPORTED: use the two
+ * calls for those. */
+int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int T, double eps, uint16_t* x_out,
+                     const uint16_t* wr_bf16, const float* bias, int E, int k, int32_t* idx,
+                     float* weights, float* logits, const void* const* expert_ptrs,
+                     moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
+                     int32_t* dev_status, void* stream);
+
 /* Decode without allocation.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory on the decode
  * path, such as a plugin that a host framework hands only its input and

@@ -80,6 +80,27 @@ __device__ __forceinline__ float unit_dot_h(uint4 q, uint32_t sbits, const uint4
   return apply_scale<FMT>(acc[0] + acc[1], acc[2] + acc[3], sbits);
 }
 
+// The same with the activation quads already in registers (x[qq] = quad qq),
+// so that one load of x serves several rows.
+template <int FMT>
+__device__ __forceinline__ float unit_dot_hx(uint4 q, uint32_t sbits, const uint4 (&x)[4]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const uint32_t xv[4] = {x[wi].x, x[wi].y, x[wi].z, x[wi].w};
+    uint32_t h[4];
+    cvt_e2m1x8(w[wi], h);
+    const int a0 = (wi >> 1) * 2;
+#pragma unroll
+    for (int bi = 0; bi < 4; ++bi) {
+      acc[a0] = fma_h(h[bi], xv[bi], acc[a0]);
+      acc[a0 + 1] = fma_h(h[bi] >> 16, xv[bi] >> 16, acc[a0 + 1]);
+    }
+  }
+  return apply_scale<FMT>(acc[0] + acc[1], acc[2] + acc[3], sbits);
+}
+
 // The same against an FP32 operand carried as FP16 hi + lo parts.  The hi
 // products go to FP32 accumulators; the lo products, 2^-11 of the hi ones or
 // less, to FP16x2 accumulators, whose rounding stays below 2^-20 of the sum.

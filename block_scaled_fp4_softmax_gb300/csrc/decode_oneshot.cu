@@ -98,6 +98,7 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
     tb.sp[ns] = p;
     tb.si0[ns] = i0;
     tb.sq0[ns] = q0;
+    tb.sn[ns] = n;
     const Win gw = window(o.gate_s + (size_t)i0 * gsb, (size_t)n * gsb);
     tb.gwo[ns] = soff + gw.delta;
     copy(g.off_scales1 + soff, gw.lo, gw.bytes, kBarScales, p);
@@ -366,58 +367,93 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // barriers below)
   if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
 
-  // gate/up + SwiGLU: row pair q of this CTA -> warp q % 15
+  // gate/up + SwiGLU: warp w takes a contiguous block of the CTA's row pairs
+  // and works on up to kRows of them (rows of one pair) at a time, so that
+  // each load of x from shared memory serves them all.  Per row, the sums run
+  // in the same order as for a single row.
   const long long r0 = (long long)blockIdx.x * g.R1 / g.grid, r1 = (long long)(blockIdx.x + 1) * g.R1 / g.grid;
   const int n1 = (int)(r1 - r0);
+  constexpr int kRows = 3;
+  const int per_warp = (n1 + kCWarps - 1) / kCWarps;
+  const int q_end = min(n1, (warp + 1) * per_warp);
   bool scales_in = false;
-  for (int q = warp; q < n1; q += kCWarps) {
-    int pi = 0;
-    while (pi + 1 < tb.npieces && tb.pq0[pi + 1] <= q) ++pi;
-    const int s = tb.pseg[pi];
+  for (int qb = warp * per_warp; qb < q_end;) {
+    int s = 0;
+    while (s + 1 < tb.nseg1 && tb.sq0[s + 1] <= qb) ++s;
+    int pa = 0;
+    while (pa + 1 < tb.npieces && tb.pq0[pa + 1] <= qb) ++pa;
+    // rows of one segment, inside piece pa and the next piece
+    int room = tb.pq0[pa] + tb.pn[pa] - qb;
+    if (pa + 1 < tb.npieces && tb.pseg[pa + 1] == s) room += tb.pn[pa + 1];
+    const int nr = min(min(kRows, room), min(q_end, tb.sq0[s] + tb.sn[s]) - qb);
+    const int pb = qb + nr - 1 < tb.pq0[pa] + tb.pn[pa] ? pa : pa + 1;
     const int p = tb.sp[s], t = p / a.k;
-    const uint8_t* rec = tb.recs[p];
-    bool ok = rec != nullptr;
+    bool ok = tb.recs[p] != nullptr;
     if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status);
-    if (ok) ok = await(&bars[pi], tb, a.status);
-    float gs = 0.f, us = 0.f;
+    if (ok) ok = await(&bars[pa], tb, a.status);
+    if (ok && pb != pa) ok = await(&bars[pb], tb, a.status);
+    float gs[kRows], us[kRows];
+    uint32_t goff[kRows], uoff[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      gs[r] = 0.f;
+      us[r] = 0.f;
+      const int q = qb + min(r, nr - 1);
+      const int pi = q < tb.pq0[pa] + tb.pn[pa] ? pa : pb;
+      goff[r] = tb.poff[pi] + (uint32_t)(q - tb.pq0[pi]) * (uint32_t)(a.H / 2);
+      uoff[r] = goff[r] + (uint32_t)tb.pn[pi] * (uint32_t)(a.H / 2);
+    }
     if (ok) {
-      const uint8_t* grow = codes1 + tb.poff[pi] + (size_t)(q - tb.pq0[pi]) * (a.H / 2);
-      const uint8_t* urow = grow + (size_t)tb.pn[pi] * (a.H / 2);
-      const uint8_t* gsr = scales1 + tb.gwo[s] + (size_t)(q - tb.sq0[s]) * (a.H / G);
-      const uint8_t* usr = scales1 + tb.uwo[s] + (size_t)(q - tb.sq0[s]) * (a.H / G);
+      const uint8_t* gsr = scales1 + tb.gwo[s] + (size_t)(qb - tb.sq0[s]) * (a.H / G);
+      const uint8_t* usr = scales1 + tb.uwo[s] + (size_t)(qb - tb.sq0[s]) * (a.H / G);
       const uint4* xt = act + (size_t)t * 4 * upr;
+      auto unit = [&](int u) {  // unit u of every row of the batch: gate units, then up units
+        const bool is_up = u >= upr;
+        const int cix = is_up ? u - upr : u;
+        uint4 xv[4];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) xv[wi] = xt[wi * upr + cix];
+        const uint8_t* sb = (is_up ? usr : gsr) + sstep * cix;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          if (r < nr) {
+            const uint4 qv = *reinterpret_cast<const uint4*>(codes1 + (is_up ? uoff[r] : goff[r]) + 16 * cix);
+            const float d = dm::unit_dot_hx<FMT>(qv, dm::scale_bits<FMT>(sb + (size_t)r * (a.H / G)), xv);
+            if (is_up) us[r] += d;
+            else gs[r] += d;
+          }
+        }
+      };
       if constexpr (UPR > 0) {
 #pragma unroll
         for (int m = 0; m < (2 * UPR + 31) / 32; ++m) {
           const int u = lane + 32 * m;
-          if (u < 2 * UPR) {
-            const bool is_up = u >= UPR;
-            const int cix = is_up ? u - UPR : u;
-            const uint4 qv = *reinterpret_cast<const uint4*>((is_up ? urow : grow) + 16 * cix);
-            const float d = dm::unit_dot_h<FMT, UPR>(
-                qv, dm::scale_bits<FMT>((is_up ? usr : gsr) + sstep * cix), xt + cix, UPR);
-            if (is_up) us += d;
-            else gs += d;
-          }
+          if (u < 2 * UPR) unit(u);
         }
       } else {
-        for (int u = lane; u < 2 * upr; u += 32) {
-          const bool is_up = u >= upr;
-          const int cix = is_up ? u - upr : u;
-          const uint4 qv = *reinterpret_cast<const uint4*>((is_up ? urow : grow) + 16 * cix);
-          const float d = dm::unit_dot_h<FMT, 0>(
-              qv, dm::scale_bits<FMT>((is_up ? usr : gsr) + sstep * cix), xt + cix, upr);
-          if (is_up) us += d;
-          else gs += d;
-        }
+        for (int u = lane; u < 2 * upr; u += 32) unit(u);
       }
     }
     const float ts = tb.tsc[t];
-    gs = warp_sum(gs) * ts;
-    us = warp_sum(us) * ts;
-    if (lane == 0)
-      a.hws[(size_t)p * a.I + tb.si0[s] + (q - tb.sq0[s])] =
-          ok ? gs / (1.0f + expf(-gs)) * us : __uint_as_float(0x7FC00000u);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        gs[r] += __shfl_xor_sync(0xffffffffu, gs[r], d);
+        us[r] += __shfl_xor_sync(0xffffffffu, us[r], d);
+      }
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        if (r < nr) {
+          const float gv = gs[r] * ts, uv = us[r] * ts;
+          a.hws[(size_t)p * a.I + tb.si0[s] + (qb + r - tb.sq0[s])] =
+              ok ? gv / (1.0f + expf(-gv)) * uv : __uint_as_float(0x7FC00000u);
+        }
+      }
+    }
+    qb += nr;
   }
   __threadfence();
 

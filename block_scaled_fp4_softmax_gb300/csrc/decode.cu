@@ -876,7 +876,7 @@ extern "C" int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int
   if ((x_bf16 && !moe::aligned16(x_bf16)) || (x_out && !moe::aligned16(x_out)) || !moe::aligned16(wr_bf16) ||
       !moe::aligned16(workspace))
     return MOE_ERR_ALIGNMENT;
-  if (!decode_oneshot_fits(T, k, s.hidden, s.inter, s.format, sm_count(), (size_t)stream_smem_limit(), true))
+  if (!decode_oneshot_fits(T, k, s.hidden, s.inter, s.format, sm_count(), (size_t)stream_smem_limit(), true, E))
     return MOE_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeOneshotArgs oa = {};

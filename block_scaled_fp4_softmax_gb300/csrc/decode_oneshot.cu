@@ -68,9 +68,12 @@ __host__ __device__ inline Win window(size_t start, size_t len) {
 }
 
 // Barriers: [0, npieces) one per gate/up piece, kBarScales the gate/up scale
-// windows, kBarDown the down rows and their scale windows.  Each completes
-// once per launch (parity 0).
+// windows, kBarDown the down rows and their scale windows (all completed by
+// the loader warp's copies and its lane 0); kBarRouter the router rows and
+// the pointer table of a fused launch (thread 0).  Each completes once per
+// launch (parity 0).
 constexpr int kBarScales = kMaxPieces, kBarDown = kMaxPieces + 1, kNumBars = kMaxPieces + 2;
+constexpr int kBarRouter = kNumBars;
 
 // Plans CTA b: pieces, segments and bulk copies, and the arrival count of
 // each barrier (one per copy, plus one for the loader's lane 0).  No data
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
   const bool fused = a.wr != nullptr;
-  const Geo g = make_geo(a.T, a.k, a.H, a.I, G, gridDim.x, fused);
+  const Geo g = make_geo(a.T, a.k, a.H, a.I, G, gridDim.x, fused, a.E);
   const RecordOffsets o = record_offsets(a.H, a.I, FMT);
   const int upr = UPR > 0 ? UPR : a.H >> 5;
   const int updr = UPDR > 0 ? UPDR : a.I >> 5;
@@ -218,23 +221,35 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   uint4* act = reinterpret_cast<uint4*>(smem + g.off_act);
   volatile int* abort_flag = tb.flags;
 
+  // router rows of this CTA's experts (fused launch) and the pointer table:
+  // neither depends on the previous kernel, so they are fetched before the
+  // wait for it -- into shared memory (the x/h region, which they leave
+  // before x arrives there) when the plan has room, else into L2
+  const int epc = (a.E + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int re0 = blockIdx.x * epc, rne = fused ? max(0, min(epc, a.E - re0)) : 0;
+  const uint32_t wr_bytes = (uint32_t)rne * (uint32_t)a.H * 2u;
+  const bool rstaged = g.rstage != 0;
+  const bool pstaged = rstaged && (reinterpret_cast<uintptr_t>(a.ptrs) & 15u) == 0 && (a.E & 1) == 0;
   if (threadIdx.x == 0) {
     uint32_t counts[kNumBars];
     build_tables(g, blockIdx.x, o, tb, counts);
     for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], counts[i]);
+    if (rstaged) tc::mbar_init(&bars[kBarRouter], 1);
     tc::mbar_fence_init();
+    if (rstaged) {
+      const uint32_t ptr_bytes = pstaged ? (uint32_t)a.E * 8u : 0u;
+      tc::mbar_arrive_expect_tx(&bars[kBarRouter], wr_bytes + ptr_bytes);
+      if (wr_bytes) tc::bulk_g2s(tc::smem_u32(smem + g.off_act), a.wr + (size_t)re0 * a.H, wr_bytes, &bars[kBarRouter]);
+      if (ptr_bytes) tc::bulk_g2s(tc::smem_u32(smem + g.off_act + wr_bytes), a.ptrs, ptr_bytes, &bars[kBarRouter]);
+    }
   }
   if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
-  // the pointer table does not depend on the previous kernel: warm L2 with it
-  for (int i = threadIdx.x; i < (a.E * 8 + 127) / 128; i += kThreads)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.ptrs) + (size_t)i * 128));
-  // router rows of this CTA's experts (fused launch): W_r does not depend on
-  // the previous kernel either
-  const int epc = (a.E + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int re0 = blockIdx.x * epc, rne = fused ? max(0, min(epc, a.E - re0)) : 0;
-  {
+  if (!pstaged)
+    for (int i = threadIdx.x; i < (a.E * 8 + 127) / 128; i += kThreads)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.ptrs) + (size_t)i * 128));
+  if (!rstaged) {
     const char* wb = fused ? reinterpret_cast<const char*>(a.wr + (size_t)re0 * a.H) : nullptr;
-    for (size_t off = (size_t)threadIdx.x * 128; off < (size_t)rne * a.H * 2; off += (size_t)kThreads * 128)
+    for (size_t off = (size_t)threadIdx.x * 128; off < wr_bytes; off += (size_t)kThreads * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
   }
   __syncthreads();
@@ -265,9 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       }
     }
     __syncthreads();
+    const bool rin = !rstaged || await(&bars[kBarRouter], tb, a.status);
+    const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + g.off_act);
     for (int task = warp; task < a.T * rne; task += kThreads / 32) {
       const int t = task / rne, q = task - t * rne;
-      const float v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
+      float v;
+      if (rstaged) v = rin ? rt::logit_dot<true>(xb + (size_t)t * a.H, wsm + (size_t)q * a.H, a.H, lane)
+                           : __uint_as_float(0x7FC00000u);
+      else v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
       if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
     }
     __threadfence();
@@ -284,8 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
         const float wgt = rt::topk_weight(lane, a.k, my_l);
         if (lane < a.k) {
           const int p = t * a.k + lane;
-          tb.recs[p] = have_logits ? dm::checked_record(my_e, a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr)
-                                   : nullptr;
+          const void* const* pt =
+              pstaged ? reinterpret_cast<const void* const*>(smem + g.off_act + wr_bytes) : a.ptrs;
+          tb.recs[p] = have_logits && rin ? dm::checked_record(my_e, a.E, pt, blockIdx.x == 0 ? a.status : nullptr)
+                                          : nullptr;
           tb.wts[p] = wgt;
           if (blockIdx.x == 0) {
             a.idx_out[p] = my_e;
@@ -580,7 +602,7 @@ int launch_shape(const DecodeOneshotArgs& a, int grid, size_t smem, cudaStream_t
 
 template <int FMT>
 int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
-  const Geo g = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid, a.wr != nullptr);
+  const Geo g = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid, a.wr != nullptr, a.E);
   // the row strides are compile-time constants for the decode model shape
   if (a.H == 2560 && a.I == 640) return launch_shape<FMT, 80, 20>(a, grid, g.total, stream);
   return launch_shape<FMT, 0, 0>(a, grid, g.total, stream);
@@ -589,10 +611,10 @@ int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
 }  // namespace os
 }  // namespace moe
 
-bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit, bool fused) {
+bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit, bool fused, int E) {
   using namespace moe::os;
   if (grid <= 0 || T <= 0 || k <= 0 || (long long)T * k > kMaxPairs) return false;
-  const Geo g = make_geo(T, k, H, I, fmt == MOE_FMT_NVFP4 ? 16 : 32, grid, fused);
+  const Geo g = make_geo(T, k, H, I, fmt == MOE_FMT_NVFP4 ? 16 : 32, grid, fused, E);
   if (g.total + 1024 > smem_limit) return false;
   if (g.segs1 > kMaxSegs || g.segs2 > kMaxSegs || max_pieces(g) > kMaxPieces) return false;
   if (g.copies > kMaxCopies || k > kMaxK) return false;

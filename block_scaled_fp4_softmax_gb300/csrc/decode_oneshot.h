@@ -44,15 +44,21 @@ struct Geo {
   int np;             // rows per gate/up piece
   int copies;         // most bulk copies of one CTA
   int hstride;        // floats per pair in the staged h (4 quads x I/32 units x 8, padded)
+  int epc;            // router rows per CTA (fused launch)
+  int rstage;         // bytes of router operands staged in the x/h region (0: read from global memory)
   // shared-memory regions (bytes from the start of dynamic shared memory)
   size_t off_bar, off_tab, off_codes1, off_scales1, off_codes2, off_scales2, off_act, off_part, off_xb, total;
 };
 
-// fused: the launch also runs the router (256 RMS partial sums, 512 top-k
-// finalists and the BF16 x get a region of their own).
-__host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid, bool fused = false) {
+// fused: the launch also runs the router over E experts (256 RMS partial
+// sums, 512 top-k finalists and the BF16 x get a region of their own).  The
+// CTA's router rows and the expert pointer table are staged in the x/h
+// region, which they leave before x arrives there, when they fit in it.
+__host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int grid, bool fused = false,
+                                        int E = 0) {
   Geo g;
   g.T = T; g.k = k; g.H = H; g.I = I; g.G = G; g.grid = grid;
+  g.epc = fused && E > 0 ? (E + grid - 1) / grid : 0;
   const long long P = (long long)T * k;
   g.R1 = P * I;
   g.D = (long long)T * H;
@@ -68,8 +74,8 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
              k * ((g.rows2 + rows_per_copy - 1) / rows_per_copy + 2 * g.segs2);
   g.hstride = 4 * (I / 32) * 8 + 4;
   size_t o = 0;
-  g.off_bar = o;                                  // mbarriers: pieces, scales, down
-  o += (kMaxPieces + 2) * 8;
+  g.off_bar = o;                                  // mbarriers: pieces, scales, down, router
+  o += (kMaxPieces + 3) * 8;
   g.off_tab = o = round_up(o, 16);                // tables, weights, scales, flags
   o += 8192;
   g.off_codes1 = o = round_up(o, 128);
@@ -82,7 +88,10 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   o += (size_t)g.rows2 * k * (I / G) + 32 * (size_t)g.segs2 * k;
   g.off_act = o = round_up(o, 128);
   const size_t a1 = (size_t)T * H * 2, a2 = (size_t)g.segs2 * k * g.hstride * 4;
-  o += a1 > a2 ? a1 : a2;                         // x (FP16), then h (FP32)
+  const size_t act = a1 > a2 ? a1 : a2;
+  const size_t rs = (size_t)g.epc * H * 2 + round_up((size_t)E * 8, 16);
+  g.rstage = fused && E > 0 && rs <= act ? (int)rs : 0;
+  o += act;                                       // router rows + pointers, then x (FP16), then h (FP32)
   g.off_part = o = round_up(o, 128);
   o += (size_t)g.rows2 * k * 4;                   // weighted expert outputs per row
   g.off_xb = o = round_up(o, 128);
@@ -100,7 +109,7 @@ __host__ __device__ inline int max_pieces(const Geo& g) { return (g.rows1 + g.np
 // One-shot decode expert pass: true when the shape fits (the caller then
 // launches it with launch_decode_oneshot).
 bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit,
-                         bool fused = false);
+                         bool fused = false, int E = 0);
 
 struct DecodeOneshotArgs {
   const uint16_t* x;

@@ -55,8 +55,10 @@ __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ y
 // c = j, j+32, j+64, ... (ascending), elements inside a chunk in order, one
 // FMA each (the BF16 x BF16 product is exact, so the FMA is the FP32 add of
 // the exact product); the 32 lane sums are combined with an xor butterfly
-// d = 16, 8, 4, 2, 1.  x_row may be in shared or global memory; w_row is read
-// through the read-only path.  Every lane returns the logit.
+// d = 16, 8, 4, 2, 1.  x_row may be in shared or global memory; w_row is in
+// shared memory (W_SHARED) or read through the read-only path.  Every lane
+// returns the logit.
+template <bool W_SHARED = false>
 __device__ __forceinline__ float logit_dot(const uint16_t* x_row, const uint16_t* __restrict__ w_row, int H,
                                            int lane) {
   const int nchunk = H >> 3;
@@ -67,7 +69,8 @@ __device__ __forceinline__ float logit_dot(const uint16_t* x_row, const uint16_t
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int c = c0 + 32 * b;
-      wv[b] = c < nchunk ? __ldg(reinterpret_cast<const uint4*>(w_row + 8 * c)) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4* wp = reinterpret_cast<const uint4*>(w_row + 8 * c);
+      wv[b] = c < nchunk ? (W_SHARED ? *wp : __ldg(wp)) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
@@ -169,13 +172,15 @@ __device__ __forceinline__ void topk_any(const float* lrow, int E, int k, int la
   else topk_from_logits<32>(lrow, E, k, lane, my_e, my_l);
 }
 
-// Top-k of one token's E <= 1024 logits by a whole block of NW warps: every
-// warp selects the k best of its candidates (expert e = warp * 32 + lane +
-// 32 * NW * m), then warp 0 selects the k best of those NW * k finalists.
-// The k best of a union are the k best of the parts' k best (keys are
-// unique), so the picks and their order are exactly those of a single-warp
-// selection.  fin: NW * 32 keys of shared memory.  Every thread calls it;
-// warp 0, lane r < k, ends with pick r.
+// Top-k of one token's E <= 1024 logits by a whole block of NW <= 32 warps:
+// every warp selects the k best of its candidates (expert e = warp * 32 +
+// lane + 32 * NW * m) in descending order, then warp 0 merges those NW
+// sorted lists -- lane i holds the head of list i, each round takes the
+// largest head and the list it came from advances.  The k best of a union
+// are the k best of the parts' k best (keys are unique), so the picks and
+// their order are exactly those of a single-warp selection.  fin: NW * 32
+// keys of shared memory.  Every thread calls it; warp 0, lane r < k, ends
+// with pick r.
 template <int NW>
 __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsigned long long* fin, int& my_e,
                                            float& my_l) {
@@ -205,10 +210,23 @@ __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsi
   }
   __syncthreads();
   if (warp == 0) {
-    unsigned long long c2[NW];
-#pragma unroll
-    for (int i = 0; i < NW; ++i) c2[i] = fin[i * 32 + lane];
-    warp_select_topk<NW>(c2, k, lane, my_e, my_l);
+    int pos = 0;
+    unsigned long long head = lane < NW ? fin[lane * 32] : 0ull;
+    my_e = 0;
+    my_l = 0.0f;
+    for (int r = 0; r < k; ++r) {
+      const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(head >> 32));
+      const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(head >> 32) == hi ? (uint32_t)head : 0u);
+      const unsigned long long best = ((unsigned long long)hi << 32) | lo;
+      if (lane == r) {
+        my_e = (int)(~lo);
+        my_l = key_to_float(hi);
+      }
+      if (lane < NW && head == best) {  // real keys are nonzero, so one lane matches
+        ++pos;
+        head = pos < k ? fin[lane * 32 + pos] : 0ull;
+      }
+    }
   }
   __syncthreads();  // fin[] may be reused by the caller
 }

@@ -182,6 +182,10 @@ int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* 
  *    y_prev (every read of y_prev precedes every write of y).
  * H = s.hidden; expert_ptrs holds E records; bias may be NULL.  The
  * workspace is moe_experts_decode's (same size, same zero-fill rule).
+ * wr_bf16 and expert_ptrs are read as soon as the launch starts, before it
+ * waits for the previous kernel on the stream (programmatic dependent
+ * launch): they must not be written by a kernel that lets its dependents
+ * start before it ends.
  * Shapes the one-shot expert pass does not cover (T*k > 64, or a per-SM
  * share larger than shared memory) return MOE_ERR_UNSUPPORTED: use the two
  * calls for those. */

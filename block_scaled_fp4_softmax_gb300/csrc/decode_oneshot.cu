@@ -173,17 +173,21 @@ __device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status) {
   return false;
 }
 
-// Grid barrier, called by one thread per CTA: one arrival on a counter that
-// only grows; this launch's CTAs wait for the next multiple of the grid size
-// (consecutive barriers of a launch share the counter).  False on timeout,
-// which also flags the launch.
-__device__ bool grid_sync_thread(unsigned long long* bar, Tab& tb, int32_t* status) {
+// Grid barrier, called by one thread per CTA after a CTA-wide barrier: one
+// arrival on a counter that only grows (a release reduction, so the writes
+// of every thread of the CTA that precede the CTA-wide barrier are visible
+// to the CTAs that pass), then an acquire poll until the counter reaches
+// `target` = base + n * grid for the launch's n-th barrier.  base is the
+// counter at the start of the launch, rounded down to a multiple of the
+// grid: every earlier launch has passed all its barriers by then, and each
+// CTA reads the counter before its own first arrival, so fewer than grid
+// arrivals of this launch can precede the read.  False on timeout, which
+// also flags the launch.
+__device__ bool grid_sync_thread(unsigned long long* bar, unsigned long long target, Tab& tb, int32_t* status) {
   volatile int* abort_flag = tb.flags;
   int good = !*abort_flag;
   if (good) {
-    unsigned long long old;
-    asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(bar) : "memory");
-    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
     const uint64_t dl = global_ns() + kWaitNs;
     while (dm::ld_acquire_u64(bar) < target) {
       if (global_ns() > dl) {
@@ -254,6 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   }
   __syncthreads();
   pdl_wait();
+  // grid-barrier counter at the start of this launch (thread 0 arrives for
+  // the CTA; a relaxed load, first used at the first barrier, so it stalls
+  // nothing before)
+  unsigned long long bar_start = 0;
+  if (threadIdx.x == 0) bar_start = rt::ld_relaxed_u64(a.bar);
+  auto bar_target = [&](unsigned n) { return (bar_start / gridDim.x + n) * gridDim.x; };
 
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
   if (fused) {
@@ -290,9 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       else v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
       if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
     }
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, tb, a.status);
+    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, bar_target(1), tb, a.status);
     __syncthreads();
     const bool have_logits = tb.flags[2] != 0;
     unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
@@ -477,13 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     }
     qb += nr;
   }
-  __threadfence();
-
-  // grid barrier among the compute threads of every CTA: one arrival on a
-  // counter that only grows; this launch's CTAs wait for the next multiple of
-  // the grid size
+  // grid barrier among the compute threads of every CTA (the h rows written
+  // above are published by thread 0's release arrival)
   tc::named_sync(1, kCThreads);
-  if (threadIdx.x == 0) tb.flags[1] = grid_sync_thread(a.bar, tb, a.status);
+  if (threadIdx.x == 0)
+    tb.flags[1] = grid_sync_thread(a.bar, bar_target(fused ? 2u : 1u), tb, a.status);
   tc::named_sync(1, kCThreads);
 
   // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats

@@ -29,7 +29,7 @@ __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ y
                                                      float* part) {
   if (threadIdx.x < 256) {
     float acc = 0.0f;
-    constexpr int kBatch = 8;  // loads in flight; the adds keep the order above
+    constexpr int kBatch = 16;  // loads in flight (all of them up to H = 4096); the adds keep the order above
     for (int i0 = threadIdx.x; i0 < H; i0 += 256 * kBatch) {
       float v[kBatch];
 #pragma unroll
@@ -90,6 +90,12 @@ __device__ __forceinline__ float logit_dot(const uint16_t* x_row, const uint16_t
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
   return acc;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Top-k keys: (ordered logit bits << 32 | ~expert), so the maximum is the

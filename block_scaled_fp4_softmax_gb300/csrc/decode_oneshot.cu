@@ -75,10 +75,12 @@ __host__ __device__ inline Win window(size_t start, size_t len) {
 constexpr int kBarScales = kMaxPieces, kBarDown = kMaxPieces + 1, kNumBars = kMaxPieces + 2;
 constexpr int kBarRouter = kNumBars;
 
-// Plans CTA b: pieces, segments and bulk copies, and the arrival count of
-// each barrier (one per copy, plus one for the loader's lane 0).  No data
-// dependence: runs before the wait for the previous kernel.
-__device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& tb, uint32_t* counts) {
+// Plans CTA b: pieces, segments and bulk copies.  Every gate/up piece gets
+// two copies (gate rows, up rows); n_scale and n_down count the copies of
+// the gate/up scale barrier and of the down barrier.  No data dependence:
+// runs before the wait for the previous kernel.
+__device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& tb, uint32_t& n_scale,
+                             uint32_t& n_down) {
   int nc = 0;
   auto copy = [&](size_t dst, size_t src, uint32_t bytes, int bar, int pair) {
     tb.cdst[nc] = (uint32_t)dst;
@@ -86,17 +88,17 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
     tb.cbytes[nc] = bytes;
     tb.cbar[nc] = (uint8_t)bar;
     tb.cpair[nc] = (uint8_t)pair;
-    ++counts[bar];
     ++nc;
   };
-  for (int i = 0; i < kNumBars; ++i) counts[i] = 1;
+  n_scale = 0;
+  n_down = 0;
   const size_t gsb = (size_t)(g.H / g.G), dsb = (size_t)(g.I / g.G), rb = (size_t)(g.H / 2), drb = (size_t)(g.I / 2);
-  const long long r0 = (long long)b * g.R1 / g.grid, r1 = (long long)(b + 1) * g.R1 / g.grid;
+  const int r0 = share_lo(b, (int)g.R1, g.grid), r1 = share_lo(b + 1, (int)g.R1, g.grid);
   int np = 0, ns = 0;
   uint32_t coff = 0, soff = 0;
-  for (long long r = r0; r < r1 && ns < kMaxSegs;) {
-    const int p = (int)(r / g.I), i0 = (int)(r - (long long)p * g.I);
-    const int n = (int)min(r1 - r, (long long)(g.I - i0));
+  for (int r = r0; r < r1 && ns < kMaxSegs;) {
+    const int p = r / g.I, i0 = r - p * g.I;
+    const int n = min(r1 - r, g.I - i0);
     const int q0 = (int)(r - r0);
     tb.sp[ns] = p;
     tb.si0[ns] = i0;
@@ -110,6 +112,7 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
     tb.uwo[ns] = soff + uw.delta;
     copy(g.off_scales1 + soff, uw.lo, uw.bytes, kBarScales, p);
     soff += uw.bytes;
+    n_scale += 2;
     for (int a = 0; a < n && np < kMaxPieces; a += g.np) {
       const int m = min(g.np, n - a);
       tb.pq0[np] = q0 + a;
@@ -127,13 +130,13 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
   }
   tb.npieces = np;
   tb.nseg1 = ns;
-  const long long d0 = (long long)b * g.D / g.grid, d1 = (long long)(b + 1) * g.D / g.grid;
+  const int d0 = share_lo(b, (int)g.D, g.grid), d1 = share_lo(b + 1, (int)g.D, g.grid);
   const int rows_per_copy = (int)(kMaxCopy / drb);
   ns = 0;
   soff = 0;
-  for (long long d = d0; d < d1 && ns < kMaxSegs;) {
-    const int t = (int)(d / g.H), n0 = (int)(d - (long long)t * g.H);
-    const int n = (int)min(d1 - d, (long long)(g.H - n0));
+  for (int d = d0; d < d1 && ns < kMaxSegs;) {
+    const int t = d / g.H, n0 = d - t * g.H;
+    const int n = min(d1 - d, g.H - n0);
     const int z0 = (int)(d - d0);
     tb.dt[ns] = t;
     tb.dn0[ns] = n0;
@@ -147,11 +150,13 @@ __device__ void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& t
         const int m = min(rows_per_copy, n - a);
         copy(g.off_codes2 + ((size_t)z0 * g.k + (size_t)j * n + a) * drb, o.down + (size_t)(n0 + a) * drb,
              (uint32_t)(m * drb), kBarDown, p);
+        ++n_down;
       }
       const Win dw = window(o.down_s + (size_t)n0 * dsb, (size_t)n * dsb);
       tb.dso[ns][j] = soff + dw.delta;
       copy(g.off_scales2 + soff, dw.lo, dw.bytes, kBarDown, p);
       soff += dw.bytes;
+      ++n_down;
     }
     ++ns;
     d += n;
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
   const bool fused = a.wr != nullptr;
-  const Geo g = make_geo(a.T, a.k, a.H, a.I, G, gridDim.x, fused, a.E);
+  const Geo& g = a.geo;
   const RecordOffsets o = record_offsets(a.H, a.I, FMT);
   const int upr = UPR > 0 ? UPR : a.H >> 5;
   const int updr = UPDR > 0 ? UPDR : a.I >> 5;
@@ -235,9 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const bool rstaged = g.rstage != 0;
   const bool pstaged = rstaged && (reinterpret_cast<uintptr_t>(a.ptrs) & 15u) == 0 && (a.E & 1) == 0;
   if (threadIdx.x == 0) {
-    uint32_t counts[kNumBars];
-    build_tables(g, blockIdx.x, o, tb, counts);
-    for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], counts[i]);
+    // arrivals: one per copy, plus one by the loader's lane 0 on every barrier
+    uint32_t n_scale, n_down;
+    build_tables(g, blockIdx.x, o, tb, n_scale, n_down);
+    for (int i = 0; i < kMaxPieces; ++i) tc::mbar_init(&bars[i], i < tb.npieces ? 3u : 1u);
+    tc::mbar_init(&bars[kBarScales], n_scale + 1);
+    tc::mbar_init(&bars[kBarDown], n_down + 1);
     if (rstaged) tc::mbar_init(&bars[kBarRouter], 1);
     tc::mbar_fence_init();
     if (rstaged) {
@@ -402,8 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // and works on up to kRows of them (rows of one pair) at a time, so that
   // each load of x from shared memory serves them all.  Per row, the sums run
   // in the same order as for a single row.
-  const long long r0 = (long long)blockIdx.x * g.R1 / g.grid, r1 = (long long)(blockIdx.x + 1) * g.R1 / g.grid;
-  const int n1 = (int)(r1 - r0);
+  const int n1 = share_lo(blockIdx.x + 1, (int)g.R1, g.grid) - share_lo(blockIdx.x, (int)g.R1, g.grid);
   constexpr int kRows = 3;
   const int per_warp = (n1 + kCWarps - 1) / kCWarps;
   const int q_end = min(n1, (warp + 1) * per_warp);
@@ -496,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats
   // per 32-element unit: element i of local pair lp at
   // lp * hstride + (((i & 31) >> 3) * I/32 + (i >> 5)) * 8 + (i & 7)
-  const long long d0 = (long long)blockIdx.x * g.D / g.grid, d1 = (long long)(blockIdx.x + 1) * g.D / g.grid;
-  const int nz = (int)(d1 - d0);
+  const int d0 = share_lo(blockIdx.x, (int)g.D, g.grid), d1 = share_lo(blockIdx.x + 1, (int)g.D, g.grid);
+  const int nz = d1 - d0;
   const int t_lo = nz > 0 ? tb.dt[0] : 0;
   const int nlp = nz > 0 ? (tb.dt[tb.nseg2 - 1] - t_lo + 1) * a.k : 0;
   float* hs = reinterpret_cast<float*>(act);
@@ -609,10 +616,11 @@ int launch_shape(const DecodeOneshotArgs& a, int grid, size_t smem, cudaStream_t
 
 template <int FMT>
 int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
-  const Geo g = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid, a.wr != nullptr, a.E);
+  DecodeOneshotArgs b = a;
+  b.geo = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid, a.wr != nullptr, a.E);
   // the row strides are compile-time constants for the decode model shape
-  if (a.H == 2560 && a.I == 640) return launch_shape<FMT, 80, 20>(a, grid, g.total, stream);
-  return launch_shape<FMT, 0, 0>(a, grid, g.total, stream);
+  if (a.H == 2560 && a.I == 640) return launch_shape<FMT, 80, 20>(b, grid, b.geo.total, stream);
+  return launch_shape<FMT, 0, 0>(b, grid, b.geo.total, stream);
 }
 
 }  // namespace os
@@ -625,6 +633,7 @@ bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t s
   if (g.total + 1024 > smem_limit) return false;
   if (g.segs1 > kMaxSegs || g.segs2 > kMaxSegs || max_pieces(g) > kMaxPieces) return false;
   if (g.copies > kMaxCopies || k > kMaxK) return false;
+  if (g.R1 * grid >= (1LL << 31) || g.D * grid >= (1LL << 31)) return false;  // 32-bit shares
   return true;
 }
 

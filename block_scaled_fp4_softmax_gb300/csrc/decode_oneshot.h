@@ -100,6 +100,12 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   return g;
 }
 
+// First unit of CTA b's equal share of n units over `grid` CTAs (32-bit:
+// the plan only admits shapes with n * grid < 2^31).
+__host__ __device__ inline int share_lo(int b, int n, int grid) {
+  return (int)((unsigned)b * (unsigned)n / (unsigned)grid);
+}
+
 // Upper bound of the gate/up pieces of one CTA.
 __host__ __device__ inline int max_pieces(const Geo& g) { return (g.rows1 + g.np - 1) / g.np + g.segs1; }
 
@@ -133,5 +139,6 @@ struct DecodeOneshotArgs {
   float* logits;
   int32_t* idx_out;
   float* w_out;
+  moe::os::Geo geo;  // the plan's geometry, computed by the host for the launch's grid
 };
 int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream);

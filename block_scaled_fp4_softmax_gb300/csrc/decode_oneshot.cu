@@ -240,15 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const bool rstaged = g.rstage != 0;
   const bool pstaged = rstaged && (reinterpret_cast<uintptr_t>(a.ptrs) & 15u) == 0 && (a.E & 1) == 0;
   if (threadIdx.x == 0) {
-    // arrivals: one per copy, plus one by the loader's lane 0 on every barrier
-    uint32_t n_scale, n_down;
-    build_tables(g, blockIdx.x, o, tb, n_scale, n_down);
-    for (int i = 0; i < kMaxPieces; ++i) tc::mbar_init(&bars[i], i < tb.npieces ? 3u : 1u);
-    tc::mbar_init(&bars[kBarScales], n_scale + 1);
-    tc::mbar_init(&bars[kBarDown], n_down + 1);
-    if (rstaged) tc::mbar_init(&bars[kBarRouter], 1);
-    tc::mbar_fence_init();
+    tb.flags[0] = 0;
+    tb.flags[1] = 0;
     if (rstaged) {
+      tc::mbar_init(&bars[kBarRouter], 1);
+      tc::mbar_fence_init();
       const uint32_t ptr_bytes = pstaged ? (uint32_t)a.E * 8u : 0u;
       tc::mbar_arrive_expect_tx(&bars[kBarRouter], wr_bytes + ptr_bytes);
       if (wr_bytes) tc::bulk_g2s(tc::smem_u32(smem + g.off_act), a.wr + (size_t)re0 * a.H, wr_bytes, &bars[kBarRouter]);
@@ -265,87 +261,32 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
   }
   __syncthreads();
-  pdl_wait();
-  // grid-barrier counter at the start of this launch (thread 0 arrives for
-  // the CTA; a relaxed load, first used at the first barrier, so it stalls
-  // nothing before)
-  unsigned long long bar_start = 0;
-  if (threadIdx.x == 0) bar_start = rt::ld_relaxed_u64(a.bar);
-  auto bar_target = [&](unsigned n) { return (bar_start / gridDim.x + n) * gridDim.x; };
-
-  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
-  if (fused) {
-    // ---------------------------------------------------------- router
-    // x = RMS chaining of y_prev (or x itself), the logits of this CTA's
-    // experts, a grid barrier, then every CTA takes the top-k of all logits
-    // itself; the same fixed orders as the router kernels, so the same bits
-    float* rpart = reinterpret_cast<float*>(smem + g.off_xb);
-    for (int t = 0; t < a.T; ++t) {
-      if (a.y_prev) {
-        const float* yr = a.y_prev + (size_t)t * a.H;
-        const float r = rt::rms_inv_fixed_order(yr, a.H, a.eps, rpart);
-        for (int i = threadIdx.x; i < a.H; i += kThreads) {
-          const uint16_t x16 = rt::f32_to_bf16_bits(__fmul_rn(yr[i], r));
-          xb[(size_t)t * a.H + i] = x16;
-          if (blockIdx.x == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = x16;
-        }
-      } else {
-        for (int i = threadIdx.x * 8; i < a.H; i += kThreads * 8) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + i));
-          *reinterpret_cast<uint4*>(xb + (size_t)t * a.H + i) = v;
-          if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(a.x_out + (size_t)t * a.H + i) = v;
-        }
-      }
-    }
-    __syncthreads();
-    const bool rin = !rstaged || await(&bars[kBarRouter], tb, a.status);
-    const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + g.off_act);
-    for (int task = warp; task < a.T * rne; task += kThreads / 32) {
-      const int t = task / rne, q = task - t * rne;
-      float v;
-      if (rstaged) v = rin ? rt::logit_dot<true>(xb + (size_t)t * a.H, wsm + (size_t)q * a.H, a.H, lane)
-                           : __uint_as_float(0x7FC00000u);
-      else v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
-      if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, bar_target(1), tb, a.status);
-    __syncthreads();
-    const bool have_logits = tb.flags[2] != 0;
-    unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
-    for (int t = 0; t < a.T; ++t) {
-      int my_e = 0;
-      float my_l = 0.0f;
-      if (have_logits) rt::topk_block<kThreads / 32>(a.logits + (size_t)t * a.E, a.E, a.k, fin, my_e, my_l);
-      if (warp == 0) {
-        const float wgt = rt::topk_weight(lane, a.k, my_l);
-        if (lane < a.k) {
-          const int p = t * a.k + lane;
-          const void* const* pt =
-              pstaged ? reinterpret_cast<const void* const*>(smem + g.off_act + wr_bytes) : a.ptrs;
-          tb.recs[p] = have_logits && rin ? dm::checked_record(my_e, a.E, pt, blockIdx.x == 0 ? a.status : nullptr)
-                                          : nullptr;
-          tb.wts[p] = wgt;
-          if (blockIdx.x == 0) {
-            a.idx_out[p] = my_e;
-            a.w_out[p] = wgt;
-          }
-        }
-      }
-    }
-    __syncthreads();
-  }
 
   if (warp == kCWarps) {
     // ------------------------------------------------------------ loader
+    // The plan of the CTA's copies has no data dependence: lane 0 builds it
+    // (and the barriers' arrival counts: one per copy, plus one by lane 0 on
+    // every barrier) while, in a fused launch, warps 0-14 run the router.
+    if (lane == 0) {
+      uint32_t n_scale, n_down;
+      build_tables(g, blockIdx.x, o, tb, n_scale, n_down);
+      for (int i = 0; i < kMaxPieces; ++i) tc::mbar_init(&bars[i], i < tb.npieces ? 3u : 1u);
+      tc::mbar_init(&bars[kBarScales], n_scale + 1);
+      tc::mbar_init(&bars[kBarDown], n_down + 1);
+      tc::mbar_fence_init();
+    }
+    __syncwarp();
+    pdl_wait();
     if (!fused) {
       for (int p = lane; p < P; p += 32) {
         tb.recs[p] = dm::checked_record(a.idx[p], a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr);
         tb.wts[p] = a.w[p];
       }
+      __syncwarp();
+    } else {
+      asm volatile("bar.sync 3, %0;" ::"n"(kThreads) : "memory");  // the router's records are in place
     }
-    __syncwarp();
-    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");  // records are in place
+    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");  // barriers set up, records in place
     // one copy per lane; a copy of a missing record still arrives (0 bytes)
     const uint32_t base = tc::smem_u32(smem);
     for (int c = lane; c < tb.ncopies; c += 32) {
@@ -363,6 +304,81 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     __syncthreads();
     return;
   }
+
+  pdl_wait();
+  // grid-barrier counter at the start of this launch (thread 0 arrives for
+  // the CTA; a relaxed load, first used at the first barrier, so it stalls
+  // nothing before)
+  unsigned long long bar_start = 0;
+  if (threadIdx.x == 0) bar_start = rt::ld_relaxed_u64(a.bar);
+  auto bar_target = [&](unsigned n) { return (bar_start / gridDim.x + n) * gridDim.x; };
+
+  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
+  if (fused) {
+    // ---------------------------------------------------------- router
+    // x = RMS chaining of y_prev (or x itself), the logits of this CTA's
+    // experts, a grid barrier, then every CTA takes the top-k of all logits
+    // itself; the same fixed orders as the router kernels, so the same bits.
+    // Warps 0-14 (named barrier 4); the loader warp plans meanwhile and takes
+    // the records through named barrier 3.
+    float* rpart = reinterpret_cast<float*>(smem + g.off_xb);
+    for (int t = 0; t < a.T; ++t) {
+      if (a.y_prev) {
+        const float* yr = a.y_prev + (size_t)t * a.H;
+        const float r = rt::rms_inv_fixed_order<4, kCThreads>(yr, a.H, a.eps, rpart);
+        for (int i = threadIdx.x; i < a.H; i += kCThreads) {
+          const uint16_t x16 = rt::f32_to_bf16_bits(__fmul_rn(yr[i], r));
+          xb[(size_t)t * a.H + i] = x16;
+          if (blockIdx.x == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = x16;
+        }
+      } else {
+        for (int i = threadIdx.x * 8; i < a.H; i += kCThreads * 8) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + i));
+          *reinterpret_cast<uint4*>(xb + (size_t)t * a.H + i) = v;
+          if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(a.x_out + (size_t)t * a.H + i) = v;
+        }
+      }
+    }
+    tc::named_sync(4, kCThreads);
+    const bool rin = !rstaged || await(&bars[kBarRouter], tb, a.status);
+    const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + g.off_act);
+    for (int task = warp; task < a.T * rne; task += kCWarps) {
+      const int t = task / rne, q = task - t * rne;
+      float v;
+      if (rstaged) v = rin ? rt::logit_dot<true>(xb + (size_t)t * a.H, wsm + (size_t)q * a.H, a.H, lane)
+                           : __uint_as_float(0x7FC00000u);
+      else v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
+      if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
+    }
+    tc::named_sync(4, kCThreads);
+    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, bar_target(1), tb, a.status);
+    tc::named_sync(4, kCThreads);
+    const bool have_logits = tb.flags[2] != 0;
+    unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
+    for (int t = 0; t < a.T; ++t) {
+      int my_e = 0;
+      float my_l = 0.0f;
+      if (have_logits) rt::topk_block<kCWarps, 4>(a.logits + (size_t)t * a.E, a.E, a.k, fin, my_e, my_l);
+      if (warp == 0) {
+        const float wgt = rt::topk_weight(lane, a.k, my_l);
+        if (lane < a.k) {
+          const int p = t * a.k + lane;
+          const void* const* pt =
+              pstaged ? reinterpret_cast<const void* const*>(smem + g.off_act + wr_bytes) : a.ptrs;
+          tb.recs[p] = have_logits && rin ? dm::checked_record(my_e, a.E, pt, blockIdx.x == 0 ? a.status : nullptr)
+                                          : nullptr;
+          tb.wts[p] = wgt;
+          if (blockIdx.x == 0) {
+            a.idx_out[p] = my_e;
+            a.w_out[p] = wgt;
+          }
+        }
+      }
+    }
+    tc::named_sync(4, kCThreads);  // the staged pointers in the x/h region are no longer read
+    asm volatile("bar.arrive 3, %0;" ::"n"(kThreads) : "memory");  // records in place for the loader
+  }
+
 
   // ---------------------------------------------------------------- compute
   // x: per-token max |x| (pass 1), then FP16 quads [t][4][H/32] of x * 2^e

@@ -14,6 +14,14 @@
 namespace moe {
 namespace rt {
 
+// Barrier among the threads that run a router step: the whole block
+// (BAR < 0), or named barrier BAR over the first N threads.
+template <int BAR, int N>
+__device__ __forceinline__ void step_sync() {
+  if constexpr (BAR < 0) __syncthreads();
+  else asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
   const __nv_bfloat16 b = __float2bfloat16_rn(v);
   return *reinterpret_cast<const uint16_t*>(&b);
@@ -22,9 +30,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
 // RMS chaining in FP32, one fixed order: thread t of 256 sums y[t + 256 m]^2
 // for m ascending (square rounded, then added), a pairwise tree combines the
 // 256 partial sums, mean = sum / H, r = 1 / sqrt(mean + eps) with IEEE sqrt
-// and divide.  Every thread of the block calls it (blockDim >= 256); threads
-// from 256 on only take part in the barriers.  part: 256 floats of shared
-// memory.
+// and divide.  Every thread of the block (BAR < 0), or the first N >= 256
+// threads (named barrier BAR), calls it; threads from 256 on only take part
+// in the barriers.  part: 256 floats of shared memory.
+template <int BAR = -1, int N = 0>
 __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ yr, int H, float eps,
                                                      float* part) {
   if (threadIdx.x < 256) {
@@ -40,14 +49,14 @@ __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ y
     }
     part[threadIdx.x] = acc;
   }
-  __syncthreads();
+  step_sync<BAR, N>();
   for (int w = 128; w > 0; w >>= 1) {
     if (threadIdx.x < w) part[threadIdx.x] = __fadd_rn(part[threadIdx.x], part[threadIdx.x + w]);
-    __syncthreads();
+    step_sync<BAR, N>();
   }
   const float mean = __fdiv_rn(part[0], (float)H);
   const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-  __syncthreads();  // part[] may be reused by the caller
+  step_sync<BAR, N>();  // part[] may be reused by the caller
   return r;
 }
 
@@ -185,9 +194,10 @@ __device__ __forceinline__ void topk_any(const float* lrow, int E, int k, int la
 // largest head and the list it came from advances.  The k best of a union
 // are the k best of the parts' k best (keys are unique), so the picks and
 // their order are exactly those of a single-warp selection.  fin: NW * 32
-// keys of shared memory.  Every thread calls it; warp 0, lane r < k, ends
-// with pick r.
-template <int NW>
+// keys of shared memory.  Every thread of the block (BAR < 0; the block
+// has NW warps), or of the first NW warps (named barrier BAR), calls it;
+// warp 0, lane r < k, ends with pick r.
+template <int NW, int BAR = -1>
 __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsigned long long* fin, int& my_e,
                                            float& my_l) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,7 +224,7 @@ __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsi
     }
     if (lane >= k) fin[warp * 32 + lane] = 0ull;
   }
-  __syncthreads();
+  step_sync<BAR, NW * 32>();
   if (warp == 0) {
     int pos = 0;
     unsigned long long head = lane < NW ? fin[lane * 32] : 0ull;
@@ -234,7 +244,7 @@ __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsi
       }
     }
   }
-  __syncthreads();  // fin[] may be reused by the caller
+  step_sync<BAR, NW * 32>();  // fin[] may be reused by the caller
 }
 
 }  // namespace rt

@@ -132,3 +132,51 @@ def test_layer_rejects_shapes_outside_one_shot(pool64):
     x = synth.activations(8, H, 941).cuda()   # T*k = 80 > 64
     with pytest.raises(moe.MoeError):
         moe.moe_decode_layer(wr, None, k, pool64.ptrs, pool64.shape, x=x)
+
+
+@pytest.fixture(scope="module")
+def pool_wide():
+    return Pool(1000, 256, 128, 0, workload=6)
+
+
+def _tied_router(E, H, x, seed):
+    """Random BF16 router rows plus rows aligned with sign(x), each copied to a
+    second expert in another warp's candidate set, so that the top-k holds
+    exactly equal logits (ties go to the lower expert index)."""
+    wr = synth.router_weights(E, H, seed)
+    sx = torch.sign(x[0].float())
+    for scale, a, b in [(0.25, 3, 961), (0.125, 500, 998), (0.0625, 17, 480), (0.03125, 31, 992)]:
+        wr[a] = (sx * scale).to(torch.bfloat16)
+        wr[b] = wr[a]
+    return wr
+
+
+@pytest.mark.parametrize("k", [8, 24])
+def test_layer_wide_router_with_ties(pool_wide, k):
+    """E = 1000 needs three candidates per lane in the fused top-k (15 warps);
+    k = 8 reads the router rows through L2, k = 24 stages them in shared
+    memory.  Fused = two calls, bit for bit, and the picks are the oracle's."""
+    E, H = pool_wide.E, pool_wide.H
+    x = synth.activations(1, H, 960 + k)
+    wr = _tied_router(E, H, x, 961 + k)
+    ref = _two_calls(pool_wide, k, x=x.cuda(), wr=wr.cuda())
+    got = moe.moe_decode_layer(wr.cuda(), None, k, pool_wide.ptrs, pool_wide.shape, x=x.cuda())
+    torch.cuda.synchronize()
+    for r, g in zip(ref[1:], got[1:]):
+        assert _same(r, g)
+    ridx, _ = O.topk_softmax(O.router_logits(bits(x), bits(wr)), k)
+    assert np.array_equal(got[1].cpu().numpy(), ridx)
+    picks = set(ridx[0].tolist())
+    assert {3, 961, 500, 998} <= picks  # the tied pairs are both selected
+
+
+@pytest.mark.parametrize("k", [8, 24])
+def test_layer_wide_router_chained(pool_wide, k):
+    E, H = pool_wide.E, pool_wide.H
+    wr = synth.router_weights(E, H, 970 + k).cuda()
+    y_prev = torch.randn(1, H, device="cuda", generator=torch.Generator("cuda").manual_seed(97 + k)) * 0.5
+    ref = _two_calls(pool_wide, k, y_prev=y_prev, wr=wr)
+    got = moe.moe_decode_layer(wr, None, k, pool_wide.ptrs, pool_wide.shape, y_prev=y_prev)
+    torch.cuda.synchronize()
+    for r, g in zip(ref, got):
+        assert _same(r, g)

@@ -57,31 +57,8 @@ __device__ __forceinline__ uint32_t scale_bits(const uint8_t* sp) {
   return FMT == MOE_FMT_NVFP4 ? (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) : (uint32_t)sp[0];
 }
 
-// One unit against FP16 activations: quad qq of the unit (elements
-// 8qq..8qq+7 as 4 f16x2) at xq[qq * stride].
-template <int FMT, int STRIDE>
-__device__ __forceinline__ float unit_dot_h(uint4 q, uint32_t sbits, const uint4* xq, int stride_rt) {
-  const int stride = STRIDE > 0 ? STRIDE : stride_rt;
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd elements of each scale block
-#pragma unroll
-  for (int wi = 0; wi < 4; ++wi) {
-    const uint4 xv4 = xq[wi * stride];
-    const uint32_t xv[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
-    uint32_t h[4];
-    cvt_e2m1x8(w[wi], h);
-    const int a0 = (wi >> 1) * 2;
-#pragma unroll
-    for (int bi = 0; bi < 4; ++bi) {
-      acc[a0] = fma_h(h[bi], xv[bi], acc[a0]);
-      acc[a0 + 1] = fma_h(h[bi] >> 16, xv[bi] >> 16, acc[a0 + 1]);
-    }
-  }
-  return apply_scale<FMT>(acc[0] + acc[1], acc[2] + acc[3], sbits);
-}
-
-// The same with the activation quads already in registers (x[qq] = quad qq),
-// so that one load of x serves several rows.
+// One unit against FP16 activations held in registers (x[qq] = elements
+// 8qq .. 8qq + 7 as 4 f16x2), so that one load of x serves several rows.
 template <int FMT>
 __device__ __forceinline__ float unit_dot_hx(uint4 q, uint32_t sbits, const uint4 (&x)[4]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -99,34 +76,6 @@ __device__ __forceinline__ float unit_dot_hx(uint4 q, uint32_t sbits, const uint
     }
   }
   return apply_scale<FMT>(acc[0] + acc[1], acc[2] + acc[3], sbits);
-}
-
-// The same against an FP32 operand carried as FP16 hi + lo parts.  The hi
-// products go to FP32 accumulators; the lo products, 2^-11 of the hi ones or
-// less, to FP16x2 accumulators, whose rounding stays below 2^-20 of the sum.
-template <int FMT, int STRIDE>
-__device__ __forceinline__ float unit_dot_h2(uint4 q, uint32_t sbits, const uint4* hi, const uint4* lo,
-                                             int stride_rt) {
-  const int stride = STRIDE > 0 ? STRIDE : stride_rt;
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  __half2 la[2] = {__float2half2_rn(0.f), __float2half2_rn(0.f)};
-#pragma unroll
-  for (int wi = 0; wi < 4; ++wi) {
-    const uint4 h4 = hi[wi * stride], l4 = lo[wi * stride];
-    const uint32_t hv[4] = {h4.x, h4.y, h4.z, h4.w}, lv[4] = {l4.x, l4.y, l4.z, l4.w};
-    uint32_t c[4];
-    cvt_e2m1x8(w[wi], c);
-    const int a0 = (wi >> 1) * 2;
-#pragma unroll
-    for (int bi = 0; bi < 4; ++bi) {
-      acc[a0] = fma_h(c[bi], hv[bi], acc[a0]);
-      acc[a0 + 1] = fma_h(c[bi] >> 16, hv[bi] >> 16, acc[a0 + 1]);
-      la[wi >> 1] = __hfma2(as_h2(c[bi]), as_h2(lv[bi]), la[wi >> 1]);
-    }
-  }
-  const float2 l0 = __half22float2(la[0]), l1 = __half22float2(la[1]);
-  return apply_scale<FMT>((acc[0] + acc[1]) + (l0.x + l0.y), (acc[2] + acc[3]) + (l1.x + l1.y), sbits);
 }
 
 // One unit against an FP32 operand stored as 4 quads of 8 floats, quad qq at

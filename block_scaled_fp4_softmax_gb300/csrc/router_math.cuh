@@ -122,69 +122,12 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Selects the k best of the lanes' candidates (composite keys, unique): round
-// r takes the largest key below round r-1's winner, so nothing is ever
-// removed and the candidate array stays in registers.  Lane r ends with
-// expert r and its logit.
-template <int EPL>
-__device__ __forceinline__ void warp_select_topk(const unsigned long long (&cand)[EPL], int k, int lane,
-                                                 int& my_e, float& my_l) {
-  unsigned long long prev = ~0ull;
-  my_e = 0;
-  my_l = 0.0f;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (cand[i] < prev && cand[i] > best) best = cand[i];
-    // warp maximum of the 64-bit keys: the high words first, then the low
-    // words among the lanes that hold the highest high word
-    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
-    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
-    best = ((unsigned long long)hi << 32) | lo;
-    prev = best;
-    if (lane == r) {
-      my_e = (int)(~(uint32_t)(best & 0xFFFFFFFFull));
-      my_l = key_to_float((uint32_t)(best >> 32));
-    }
-  }
-}
-
 // Renormalised softmax weight of lane r's pick (lanes >= k get 0).
 __device__ __forceinline__ float topk_weight(int lane, int k, float my_l) {
   const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
   const float ex = lane < k ? expf(my_l - l0) : 0.0f;
   const float sum = warp_sum(ex);
   return lane < k ? __fdiv_rn(ex, sum) : 0.0f;
-}
-
-// Candidates of one token from its E logits (global memory, read through L2),
-// then the selection above.
-template <int EPL>
-__device__ __forceinline__ void topk_from_logits(const float* lrow, int E, int k, int lane, int& my_e,
-                                                 float& my_l) {
-  unsigned long long cand[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    cand[i] = 0ull;
-    if (e < E) {
-      const uint32_t key = ordered_key(__ldcg(lrow + e));
-      cand[i] = ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)e);
-    }
-  }
-  warp_select_topk<EPL>(cand, k, lane, my_e, my_l);
-}
-
-// The same for any E <= 1024.
-__device__ __forceinline__ void topk_any(const float* lrow, int E, int k, int lane, int& my_e, float& my_l) {
-  const int epl = (E + 31) / 32;
-  if (epl <= 1) topk_from_logits<1>(lrow, E, k, lane, my_e, my_l);
-  else if (epl <= 2) topk_from_logits<2>(lrow, E, k, lane, my_e, my_l);
-  else if (epl <= 4) topk_from_logits<4>(lrow, E, k, lane, my_e, my_l);
-  else if (epl <= 8) topk_from_logits<8>(lrow, E, k, lane, my_e, my_l);
-  else if (epl <= 16) topk_from_logits<16>(lrow, E, k, lane, my_e, my_l);
-  else topk_from_logits<32>(lrow, E, k, lane, my_e, my_l);
 }
 
 // Top-k of one token's E <= 1024 logits by a whole block of NW <= 32 warps:

@@ -50,10 +50,17 @@ __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ y
     part[threadIdx.x] = acc;
   }
   step_sync<BAR, N>();
-  for (int w = 128; w > 0; w >>= 1) {
+  for (int w = 128; w >= 32; w >>= 1) {
     if (threadIdx.x < w) part[threadIdx.x] = __fadd_rn(part[threadIdx.x], part[threadIdx.x + w]);
     step_sync<BAR, N>();
   }
+  if (threadIdx.x < 32) {  // the levels w = 16 .. 1 inside warp 0: lane t adds lane t + w
+    float v = part[threadIdx.x];
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, w));
+    if (threadIdx.x == 0) part[0] = v;
+  }
+  step_sync<BAR, N>();
   const float mean = __fdiv_rn(part[0], (float)H);
   const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
   step_sync<BAR, N>();  // part[] may be reused by the caller

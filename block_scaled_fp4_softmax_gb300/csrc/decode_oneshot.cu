@@ -5,16 +5,22 @@
 // SwiGLU expert kernel; the sum over the k experts weighted by the
 // renormalised router probabilities).
 //
-//  1. Prologue.  Before the wait for the previous kernel every CTA plans its
-//     bulk copies; then warp 15 reads the routed records and its lanes issue
-//     every copy of the CTA's share at once (the copy engine of an SM
-//     completes only a few copies per microsecond, so the copies are few and
-//     large); warps 0-14 stage x as FP16, scaled per token by a power of two
-//     (exact).
-//  2. gate/up + SwiGLU: row pair q of the CTA -> warp q % 15, as soon as its
-//     piece has landed; h = silu(g) * u goes to global scratch.
-//  3. Grid barrier (one arrival on a counter that only grows).
-//  4. down: the CTA owns whole output rows.  h of its tokens' pairs is staged
+//  0. Prologue, before the wait for the previous kernel: thread 0 bulk-copies
+//     the CTA's router rows and the expert pointer table into shared memory
+//     (a launch that runs the whole layer); warp 15, the loader, plans the
+//     CTA's share of the selected records and sets up the copy barriers.
+//  1. Router (whole-layer launch), warps 0-14: x = RMS chaining of the
+//     previous output (or x itself), the logits of the CTA's experts, a grid
+//     barrier, then every CTA takes the top-k of all logits itself.
+//  2. Copies: the loader's lanes issue every bulk copy of the CTA's share at
+//     once (the copy engine of an SM completes only a few copies per
+//     microsecond, so the copies are few and large); warps 0-14 stage x as
+//     FP16, scaled per token by a power of two (exact).
+//  3. gate/up + SwiGLU: each warp takes a contiguous block of the CTA's row
+//     pairs, up to three rows at a time, as soon as their piece has landed;
+//     h = silu(g) * u goes to global scratch.
+//  4. Grid barrier (one release arrival per CTA on a counter that only grows).
+//  5. down: the CTA owns whole output rows.  h of its tokens' pairs is staged
 //     as FP32; task (row, expert) -> a group of lanes, each lane a few units
 //     (16 code bytes = 32 elements) with packed FP32 FMAs, the group reduced
 //     by shuffles; each row adds its k weighted expert outputs in expert

@@ -94,12 +94,11 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Top-k.  One warp per token: candidates keyed by (ordered logit, ~expert),
-// k rounds of warp arg-max (moe::rt::warp_select_topk), weights renormalised
-// over the picks.
+// Top-k.  One block of kTopkThreads per token, candidates keyed by (ordered
+// logit, ~expert): every warp picks the k best of its share, warp 0 merges
+// those sorted lists (moe::rt::topk_block); weights renormalised over the
+// picks.
 // ---------------------------------------------------------------------------
-// One block of kTopkThreads per token: every warp picks the k best of its
-// share of the candidates, then warp 0 the k best of those.
 constexpr int kTopkThreads = 512;
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ logits, int T, int E,
                                                             int k, int32_t* __restrict__ idx,

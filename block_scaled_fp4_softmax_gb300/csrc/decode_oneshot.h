@@ -17,6 +17,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace moe {
 namespace os {
 
@@ -109,13 +111,161 @@ __host__ __device__ inline int share_lo(int b, int n, int grid) {
 // Upper bound of the gate/up pieces of one CTA.
 __host__ __device__ inline int max_pieces(const Geo& g) { return (g.rows1 + g.np - 1) / g.np + g.segs1; }
 
+__host__ __device__ inline int imin(int a, int b) { return a < b ? a : b; }
+
+// Per-CTA tables in shared memory: the routed records and weights, the plan
+// of pieces, segments and bulk copies, and a few flags.
+struct Tab {
+  const uint8_t* recs[kMaxPairs];
+  float wts[kMaxPairs];
+  float tsc[kMaxPairs];      // per token: 2^-e of the FP16 scale of x
+  unsigned amax[kMaxPairs];  // max |.| as float bits (x per token, then h per segment)
+  int flags[4];              // [0] abort, [1] grid barrier passed, [2] router barrier passed
+  int npieces, nseg1, nseg2, ncopies;
+  int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];
+  uint32_t poff[kMaxPieces];  // piece: gate rows at codes1 + poff, up rows right after
+  int sp[kMaxSegs], si0[kMaxSegs], sq0[kMaxSegs], sn[kMaxSegs];
+  uint32_t gwo[kMaxSegs], uwo[kMaxSegs];  // first gate / up scale byte of the segment in scales1
+  int dt[kMaxSegs], dn0[kMaxSegs], dz0[kMaxSegs], dn[kMaxSegs];  // down: token, rows
+  uint32_t dso[kMaxSegs][kMaxK];          // first down scale byte of (segment, expert) in scales2
+  // bulk copies: shared-memory destination (bytes from the dynamic base),
+  // source offset in the record, bytes, barrier, pair
+  uint64_t csrc[kMaxCopies];
+  uint32_t cdst[kMaxCopies], cbytes[kMaxCopies];
+  uint8_t cbar[kMaxCopies], cpair[kMaxCopies];
+};
+static_assert(sizeof(Tab) <= 8192, "table region");
+
+struct Win {  // 16-byte aligned window [lo, lo + bytes) around a byte range
+  size_t lo;
+  uint32_t bytes, delta;
+};
+__host__ __device__ inline Win window(size_t start, size_t len) {
+  Win w;
+  w.lo = start & ~(size_t)15;
+  const size_t hi = (start + len + 15) & ~(size_t)15;
+  w.bytes = (uint32_t)(hi - w.lo);
+  w.delta = (uint32_t)(start - w.lo);
+  return w;
+}
+
+// Barriers: [0, npieces) one per gate/up piece, kBarScales the gate/up scale
+// windows, kBarDown the down rows and their scale windows (all completed by
+// the loader warp's copies and its lane 0); kBarRouter the router rows and
+// the pointer table of a fused launch (thread 0).  Each completes once per
+// launch (parity 0).
+constexpr int kBarScales = kMaxPieces, kBarDown = kMaxPieces + 1, kNumBars = kMaxPieces + 2;
+constexpr int kBarRouter = kNumBars;
+
+// Plans CTA b: pieces, segments and bulk copies.  Every gate/up piece gets
+// two copies (gate rows, up rows); n_scale and n_down count the copies of
+// the gate/up scale barrier and of the down barrier.  No data dependence:
+// runs before the wait for the previous kernel.
+__host__ __device__ inline void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& tb, uint32_t& n_scale,
+                             uint32_t& n_down) {
+  int nc = 0;
+  auto copy = [&](size_t dst, size_t src, uint32_t bytes, int bar, int pair) {
+    tb.cdst[nc] = (uint32_t)dst;
+    tb.csrc[nc] = src;
+    tb.cbytes[nc] = bytes;
+    tb.cbar[nc] = (uint8_t)bar;
+    tb.cpair[nc] = (uint8_t)pair;
+    ++nc;
+  };
+  n_scale = 0;
+  n_down = 0;
+  const size_t gsb = (size_t)(g.H / g.G), dsb = (size_t)(g.I / g.G), rb = (size_t)(g.H / 2), drb = (size_t)(g.I / 2);
+  const int r0 = share_lo(b, (int)g.R1, g.grid), r1 = share_lo(b + 1, (int)g.R1, g.grid);
+  int np = 0, ns = 0;
+  uint32_t coff = 0, soff = 0;
+  for (int r = r0; r < r1 && ns < kMaxSegs;) {
+    const int p = r / g.I, i0 = r - p * g.I;
+    const int n = imin(r1 - r, g.I - i0);
+    const int q0 = (int)(r - r0);
+    tb.sp[ns] = p;
+    tb.si0[ns] = i0;
+    tb.sq0[ns] = q0;
+    tb.sn[ns] = n;
+    const Win gw = window(o.gate_s + (size_t)i0 * gsb, (size_t)n * gsb);
+    tb.gwo[ns] = soff + gw.delta;
+    copy(g.off_scales1 + soff, gw.lo, gw.bytes, kBarScales, p);
+    soff += gw.bytes;
+    const Win uw = window(o.up_s + (size_t)i0 * gsb, (size_t)n * gsb);
+    tb.uwo[ns] = soff + uw.delta;
+    copy(g.off_scales1 + soff, uw.lo, uw.bytes, kBarScales, p);
+    soff += uw.bytes;
+    n_scale += 2;
+    for (int a = 0; a < n && np < kMaxPieces; a += g.np) {
+      const int m = imin(g.np, n - a);
+      tb.pq0[np] = q0 + a;
+      tb.pn[np] = m;
+      tb.pseg[np] = ns;
+      tb.poff[np] = coff;
+      const uint32_t bytes = (uint32_t)(m * rb);
+      copy(g.off_codes1 + coff, o.gate + (size_t)(i0 + a) * rb, bytes, np, p);
+      copy(g.off_codes1 + coff + bytes, o.up + (size_t)(i0 + a) * rb, bytes, np, p);
+      coff += 2 * bytes;
+      ++np;
+    }
+    ++ns;
+    r += n;
+  }
+  tb.npieces = np;
+  tb.nseg1 = ns;
+  const int d0 = share_lo(b, (int)g.D, g.grid), d1 = share_lo(b + 1, (int)g.D, g.grid);
+  const int rows_per_copy = (int)(kMaxCopy / drb);
+  ns = 0;
+  soff = 0;
+  for (int d = d0; d < d1 && ns < kMaxSegs;) {
+    const int t = d / g.H, n0 = d - t * g.H;
+    const int n = imin(d1 - d, g.H - n0);
+    const int z0 = (int)(d - d0);
+    tb.dt[ns] = t;
+    tb.dn0[ns] = n0;
+    tb.dz0[ns] = z0;
+    tb.dn[ns] = n;
+    // rows [n0, n0 + n) of every expert of token t: codes at
+    // codes2 + (z0 * k + j * n) rows, then one scale window per expert
+    for (int j = 0; j < g.k; ++j) {
+      const int p = t * g.k + j;
+      for (int a = 0; a < n; a += rows_per_copy) {
+        const int m = imin(rows_per_copy, n - a);
+        copy(g.off_codes2 + ((size_t)z0 * g.k + (size_t)j * n + a) * drb, o.down + (size_t)(n0 + a) * drb,
+             (uint32_t)(m * drb), kBarDown, p);
+        ++n_down;
+      }
+      const Win dw = window(o.down_s + (size_t)n0 * dsb, (size_t)n * dsb);
+      tb.dso[ns][j] = soff + dw.delta;
+      copy(g.off_scales2 + soff, dw.lo, dw.bytes, kBarDown, p);
+      soff += dw.bytes;
+      ++n_down;
+    }
+    ++ns;
+    d += n;
+  }
+  tb.nseg2 = ns;
+  tb.ncopies = nc;
+  tb.flags[0] = 0;
+  tb.flags[1] = 0;
+}
+
+
 }  // namespace os
 }  // namespace moe
 
 // One-shot decode expert pass: true when the shape fits (the caller then
 // launches it with launch_decode_oneshot).
-bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit,
-                         bool fused = false, int E = 0);
+inline bool decode_oneshot_fits(int T, int k, int H, int I, int fmt, int grid, size_t smem_limit,
+                               bool fused = false, int E = 0) {
+  using namespace moe::os;
+  if (grid <= 0 || T <= 0 || k <= 0 || (long long)T * k > kMaxPairs) return false;
+  const Geo g = make_geo(T, k, H, I, fmt == MOE_FMT_NVFP4 ? 16 : 32, grid, fused, E);
+  if (g.total + 1024 > smem_limit) return false;
+  if (g.segs1 > kMaxSegs || g.segs2 > kMaxSegs || max_pieces(g) > kMaxPieces) return false;
+  if (g.copies > kMaxCopies || k > kMaxK) return false;
+  if (g.R1 * grid >= (1LL << 31) || g.D * grid >= (1LL << 31)) return false;  // 32-bit shares
+  return true;
+}
 
 struct DecodeOneshotArgs {
   const uint16_t* x;

@@ -160,7 +160,8 @@ constexpr int kBarRouter = kNumBars;
 // Plans CTA b: pieces, segments and bulk copies.  Every gate/up piece gets
 // two copies (gate rows, up rows); n_scale and n_down count the copies of
 // the gate/up scale barrier and of the down barrier.  No data dependence:
-// runs before the wait for the previous kernel.
+// runs while the router does.  Writes the plan fields of the table only
+// (never the flags, which the router may set meanwhile).
 __host__ __device__ inline void build_tables(const Geo& g, int b, const RecordOffsets& o, Tab& tb, uint32_t& n_scale,
                              uint32_t& n_down) {
   int nc = 0;
@@ -245,8 +246,6 @@ __host__ __device__ inline void build_tables(const Geo& g, int b, const RecordOf
   }
   tb.nseg2 = ns;
   tb.ncopies = nc;
-  tb.flags[0] = 0;
-  tb.flags[1] = 0;
 }
 
 

@@ -290,9 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     }
   }
   asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // x staged, records in place
-  // amax served x; the down phase reuses it for h (ordered by the named
-  // barriers below)
-  if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
 
   // gate/up + SwiGLU: warp w takes a contiguous block of the CTA's row pairs
   // and works on up to kRows of them (rows of one pair) at a time, so that

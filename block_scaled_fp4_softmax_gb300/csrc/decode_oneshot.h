@@ -119,7 +119,7 @@ struct Tab {
   const uint8_t* recs[kMaxPairs];
   float wts[kMaxPairs];
   float tsc[kMaxPairs];      // per token: 2^-e of the FP16 scale of x
-  unsigned amax[kMaxPairs];  // max |.| as float bits (x per token, then h per segment)
+  unsigned amax[kMaxPairs];  // max |x| of each token, as float bits
   int flags[4];              // [0] abort, [1] grid barrier passed, [2] router barrier passed
   int npieces, nseg1, nseg2, ncopies;
   int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];

@@ -444,18 +444,12 @@ def moe_layer_grouped_by_expert(x_bits, idx, weights, records, H: int, I: int, f
     return y.astype(np.float32)
 
 
-def rmsnorm_bf16(y, eps: float = 1e-6) -> np.ndarray:
-    """Layer-chaining glue for stacked decode: x_next = BF16(y * r) with
-    r = 1 / sqrt(mean(y^2) + eps) and no learnable weight.
-
-    The pages only say the next layer's input is the previous output,
-    RMS-normalised; the reading taken is FP32 arithmetic in one fixed order, so
-    the BF16 result is reproducible bit for bit: 256 strided partial sums
-    (partial t adds y[t + 256 m]^2 for m ascending, each square rounded, then
-    added), a pairwise tree partial[t] += partial[t + w] for w = 128, 64, ..., 1,
-    mean = sum / H, r = 1 / sqrt(mean + eps) with IEEE sqrt and divide, and
-    x = y * r rounded once to BF16 (ties to even).  Returns BF16 bit patterns
-    (uint16) [T, H]."""
+def rms_sumsq_fixed_order(y) -> np.ndarray:
+    """The FP32 sum of squares of each row of y in the one fixed order of the
+    RMS-chaining reading below: 256 strided partial sums (partial t adds
+    y[t + 256 m]^2 for m ascending, each square rounded to FP32, then added),
+    then a pairwise tree that adds partial t + w into partial t for
+    w = 128, 64, ..., 1.  Returns float32 [T]."""
     y = np.asarray(y, dtype=np.float32)
     T, H = y.shape
     part = np.zeros((T, 256), dtype=np.float32)
@@ -467,10 +461,42 @@ def rmsnorm_bf16(y, eps: float = 1e-6) -> np.ndarray:
     while w >= 1:
         part[:, :w] = part[:, :w] + part[:, w: 2 * w]
         w //= 2
-    mean = part[:, 0] / np.float32(H)
-    r = np.float32(1.0) / np.sqrt(mean + np.float32(eps))
+    return part[:, 0].copy()
+
+
+def rms_inv_fixed_order(y, eps: float = 1e-6) -> np.ndarray:
+    """The FP32 factor r = 1 / sqrt(mean(y^2) + eps) of each row of y: the
+    fixed-order sum of squares, mean = sum / H, then IEEE sqrt and divide;
+    eps is rounded to FP32.  Returns float32 [T]."""
+    y = np.asarray(y, dtype=np.float32)
+    mean = rms_sumsq_fixed_order(y) / np.float32(y.shape[1])
+    return np.float32(1.0) / np.sqrt(mean + np.float32(eps))
+
+
+def rmsnorm_bf16(y, eps: float = 1e-6) -> np.ndarray:
+    """Layer-chaining glue for stacked decode: x_next = BF16(y * r) with
+    r = 1 / sqrt(mean(y^2) + eps) and no learnable weight.
+
+    The pages only say the next layer's input is the previous output,
+    RMS-normalised (Qwen page, "Why this model": 48 layers in a row).  The
+    reading taken is FP32 arithmetic in one fixed order (rms_inv_fixed_order),
+    so that the BF16 x -- and with it the next layer's routing -- is
+    reproducible bit for bit; x = y * r is rounded once to BF16 (ties to
+    even).  rmsnorm_bf16_f64 is the plain definition it approximates, within
+    one BF16 unit.  Returns BF16 bit patterns (uint16) [T, H]."""
+    y = np.asarray(y, dtype=np.float32)
+    r = rms_inv_fixed_order(y, eps)
     x = y * r[:, None]
     return bf16_round_bits(x.astype(np.float64))
+
+
+def rmsnorm_bf16_f64(y, eps: float = 1e-6) -> np.ndarray:
+    """The plain definition of the RMS chaining: x = BF16(y / sqrt(mean(y^2)
+    + eps)) with the mean, the root and the quotient in float64 and a single
+    rounding to BF16.  Returns BF16 bit patterns (uint16) [T, H]."""
+    y = np.asarray(y, dtype=np.float64)
+    ms = np.mean(y * y, axis=1, keepdims=True)
+    return bf16_round_bits(y / np.sqrt(ms + float(eps)))
 
 
 # ---------------------------------------------------------------------------

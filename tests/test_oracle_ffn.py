@@ -1,6 +1,7 @@
 """Pins for the oracle's expert FFN, bucketing, RMS chaining and FP8 GEMV
 (CPU only)."""
 import math
+import struct
 
 import numpy as np
 import pytest
@@ -189,17 +190,107 @@ def test_bucketing_brute_force():
     assert list(pairs) == want
 
 
-def test_rmsnorm_close_to_torch_float64_then_bf16():
+def _f32(v):
+    """A Python float rounded to FP32 (round to nearest even)."""
+    return struct.unpack("<f", struct.pack("<f", v))[0]
+
+
+def _bf16_bits_of_f32(v):
+    """FP32 value -> BF16 bit pattern, ties to even, from the FP32 bits."""
+    u = struct.unpack("<I", struct.pack("<f", v))[0]
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) & 0xFFFF
+
+
+def _rms_rows_brute_force(y, eps, nparts=256, stride=True, tree="halves"):
+    """The fixed FP32 order of the RMS chaining written out with Python floats
+    rounded to FP32 after every operation.  The default arguments are the
+    documented reading; the others plant plausible mistakes (a contiguous split
+    instead of a strided one, another partial count, adjacent pairing in the
+    tree) so that a test can show the pin catches them."""
+    T, H = y.shape
+    sums, rs, xs = [], [], []
+    for t in range(T):
+        row = [float(v) for v in y[t]]
+        part = [0.0] * nparts
+        if stride:
+            for i in range(H):
+                part[i % nparts] = _f32(part[i % nparts] + _f32(row[i] * row[i]))
+        else:
+            per = -(-H // nparts)
+            for i in range(H):
+                part[i // per] = _f32(part[i // per] + _f32(row[i] * row[i]))
+        w = nparts // 2
+        while w >= 1:
+            if tree == "halves":
+                part = [_f32(part[j] + part[j + w]) if j < w else part[j] for j in range(nparts)]
+            else:  # adjacent pairs, then the survivors packed to the front
+                part = [_f32(part[2 * j] + part[2 * j + 1]) for j in range(w)] + [0.0] * (nparts - w)
+            w //= 2
+        mean = _f32(part[0] / float(H))
+        r = _f32(1.0 / _f32(math.sqrt(_f32(mean + _f32(eps)))))
+        sums.append(part[0])
+        rs.append(r)
+        xs.append([_bf16_bits_of_f32(_f32(v * r)) for v in row])
+    return (np.array(sums, dtype=np.float32), np.array(rs, dtype=np.float32),
+            np.array(xs, dtype=np.uint16))
+
+
+def _rms_inputs():
+    # widths of the Qwen- and DeepSeek-shaped layers and a ragged one (not a
+    # multiple of 256); magnitudes spread over several binades so that the
+    # order of the FP32 additions shows in the last bits of the sum
+    rng = np.random.default_rng(31)
+    out = []
+    for H in (2560, 4096, 1000):
+        y = rng.standard_normal((6, H)) * np.exp2(rng.integers(-1, 2, (6, H)))
+        out.append(y.astype(np.float32))
+    return out
+
+
+def test_rms_fixed_order_brute_force():
+    for y in _rms_inputs():
+        s_want, r_want, x_want = _rms_rows_brute_force(y, 1e-6)
+        assert np.array_equal(O.rms_sumsq_fixed_order(y).view(np.uint32), s_want.view(np.uint32))
+        assert np.array_equal(O.rms_inv_fixed_order(y, 1e-6).view(np.uint32), r_want.view(np.uint32))
+        assert np.array_equal(O.rmsnorm_bf16(y, 1e-6), x_want)
+
+
+def test_rms_pin_catches_planted_order_mistakes():
+    # each planted order gives another FP32 sum of squares on at least one
+    # row, so the brute-force pin above would fail an oracle that used it
+    ys = _rms_inputs()
+    for kw in ({"stride": False}, {"nparts": 128}, {"nparts": 512}, {"tree": "adjacent"}):
+        differs = 0
+        for y in ys:
+            s_bad, _, _ = _rms_rows_brute_force(y, 1e-6, **kw)
+            differs += int(np.sum(O.rms_sumsq_fixed_order(y).view(np.uint32) != s_bad.view(np.uint32)))
+        assert differs >= 2, kw
+
+
+def test_rmsnorm_within_one_bf16_unit_of_the_definition():
+    # the fixed FP32 order against the float64 definition: the FP32 factor r
+    # is within a few FP32 units of the exact one, so x moves across a BF16
+    # rounding point only rarely, and then by one unit
     rng = np.random.default_rng(10)
+    for H in (2560, 4096):
+        y = (rng.standard_normal((8, H)) * 0.3).astype(np.float32)
+        got = O.rmsnorm_bf16(y, 1e-6)
+        want = O.rmsnorm_bf16_f64(y, 1e-6)
+        diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+        assert diff.max() <= 1 and np.count_nonzero(diff) <= 8
+        r = O.rms_inv_fixed_order(y, 1e-6).astype(np.float64)
+        y64 = y.astype(np.float64)
+        r_exact = 1.0 / np.sqrt(np.mean(y64 * y64, axis=1) + 1e-6)
+        assert np.all(np.abs(r / r_exact - 1.0) <= 16 * 2.0 ** -24)
+
+
+def test_rmsnorm_definition_matches_torch_float64():
+    # the float64 definition against torch's own RMS norm in float64
+    rng = np.random.default_rng(13)
     y = (rng.standard_normal((4, 2560)) * 0.3).astype(np.float32)
-    got = O.rmsnorm_bf16(y, 1e-6)
     ref = torch.nn.functional.rms_norm(torch.from_numpy(y).double(), (2560,), eps=1e-6)
-    want = O.bf16_round_bits(ref.numpy())
-    # FP32 rounding of r moves a value across a BF16 tie only very rarely, and
-    # then by one unit in the last place
-    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
-    assert diff.max() <= 1 and np.count_nonzero(diff) <= 2
-    xs = O.bf16_bits_to_f32(got).astype(np.float64)
+    assert np.array_equal(O.rmsnorm_bf16_f64(y, 1e-6), O.bf16_round_bits(ref.numpy()))
+    xs = O.bf16_bits_to_f32(O.rmsnorm_bf16(y, 1e-6)).astype(np.float64)
     assert np.allclose(np.sqrt(np.mean(xs * xs, axis=1)), 1.0, atol=1e-2)
 
 

@@ -8,6 +8,14 @@ layer's output, RMS-normalised.  A step runs router -> experts -> RMS chaining
 for all 48 layers.  The metric is expert GB/s: the bytes of the records the
 step selects divided by the step time, and its fraction of the HBM roofline.
 
+The same run also measures the four other workloads, each under its own key
+of the JSON line with its own roofline and oracle sample: ``config0`` (one
+layer, one token, 64 experts), ``prompt`` (2451 tokens through one layer,
+Zipf-skewed routing over 512 experts, the tensor-core path), ``config3``
+(DeepSeek-shaped MXFP4 layer, 384 experts of 18,800,640 bytes, top-6, 40
+calls with the L2 flushed between calls) and ``config4`` (32 tokens through
+the 48-layer stack).
+
 ``--impl reference`` times the CPU oracle (float64 numpy) on a bounded sample
 of the same workload instead.
 
@@ -184,6 +192,41 @@ class DecodeStack:
         return g, ev
 
 
+def speculative_routing(torch, moe, wl, tokens=16):
+    """Hit rate of speculative next-layer routing on the decode stack: layer
+    L+1's router applied to layer L's input, against layer L+1's actual
+    top-k (the pages guess the next layer's experts this way to start their
+    copies early).  Reported for k guesses and for 16 guesses (fraction of the
+    true top-k covered).  Random router weights have no layer-to-layer
+    structure, so the expected rate is about k / E."""
+    hits, hits16, n = 0, 0, 0
+    for s in range(tokens):
+        xs, idxs = [], []
+        wl.x.copy_(wl.x0[s % wl.x0.shape[0]:s % wl.x0.shape[0] + 1])
+        for L in range(LAYERS):
+            if L == 0:
+                moe.moe_decode_layer(wl.wr[L], None, K_TOP, wl.ptrs[L], wl.s, x=wl.x, idx=wl.idx, weights=wl.w,
+                                     logits=wl.logits, y=wl.y, workspace=wl.ws, dev_status=wl.st)
+                xs.append(wl.x.clone())
+            else:
+                moe.moe_decode_layer(wl.wr[L], None, K_TOP, wl.ptrs[L], wl.s, y_prev=wl.y, eps=1e-6, x_out=wl.x,
+                                     idx=wl.idx, weights=wl.w, logits=wl.logits, y=wl.y, workspace=wl.ws,
+                                     dev_status=wl.st)
+                xs.append(wl.x.clone())
+            idxs.append(wl.idx.clone())
+        for L in range(LAYERS - 1):
+            g10, _, _ = moe.moe_router_topk(xs[L], wl.wr[L + 1], None, K_TOP)
+            g16, _, _ = moe.moe_router_topk(xs[L], wl.wr[L + 1], None, 16)
+            true = set(idxs[L + 1].flatten().tolist())
+            hits += len(true & set(g10.flatten().tolist()))
+            hits16 += len(true & set(g16.flatten().tolist()))
+            n += K_TOP
+    return {"tokens": tokens, "layer_pairs": tokens * (LAYERS - 1),
+            "hit_rate_top10": round(hits / n, 4), "coverage_top16": round(hits16 / n, 4),
+            "chance_k_over_E": round(K_TOP / E, 4),
+            "note": "router of layer L+1 on layer L's input vs layer L+1's own top-10; random router weights"}
+
+
 class PromptLayer:
     """Qwen-shaped prompt through one MoE layer: T=2451 tokens, 512 NVFP4
     experts, top-10 with a Zipf(1.1) router bias; a step is router + the
@@ -243,13 +286,276 @@ class PromptLayer:
         counts = torch.bincount(self.idx.flatten().long(), minlength=E)
         hit = int((counts > 0).sum().item())
         flops = 2.0 * self.T * K_TOP * 3 * H * I
+        P = self.T * K_TOP
+        # algorithmic bytes of the expert pass: every hit record once, X read,
+        # the BF16 SwiGLU intermediate written and read, Y written
+        nbytes = hit * self.pool.shape[1] + self.T * H * 2 + 2 * P * I * 2 + self.T * H * 4
+        peak, kind = _peaks()
+        achieved = nbytes / (ms_exp / 1e3) / 1e9
         return {"tokens_per_s": round(self.T / (ms / 1e3), 1), "ms_per_layer": round(ms, 4),
                 "expert_pass_ms": round(ms_exp, 4),
                 "expert_tflops": round(flops / (ms_exp / 1e3) / 1e12, 2),
                 "expert_weight_gbs": round(hit * self.pool.shape[1] / (ms_exp / 1e3) / 1e9, 1),
                 "experts_hit": hit, "max_tokens_per_expert": int(counts.max().item()),
                 "tokens": self.T, "dev_status": int(self.st.item()),
+                "roofline": {"bound": "hbm", "kernel": "moe_experts_grouped (bucketing + grouped_kernel phases 0 and 1)",
+                             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                             "peak_kind": kind + " (burst copy)", "frac": round(achieved / peak, 4),
+                             "bytes_per_call": nbytes, "flops_per_call": flops,
+                             "tensor_tflops": round(flops / (ms_exp / 1e3) / 1e12, 2),
+                             "note": "HBM floor at the measured peak vs the FP16/BF16 tensor floor: bytes bound"},
                 "l2": "flushed between steps by reading a 512 MB buffer"}
+
+
+def _l2_flusher(torch, device):
+    """A read sweep over 512 MB (four times the L2): evicts the L2 without
+    leaving dirty lines whose write-back would land in the next timed call."""
+    buf = torch.ones(512 << 18, dtype=torch.int32, device=device)
+    out = torch.zeros((), dtype=torch.int64, device=device)
+    return lambda: torch.sum(buf, 0, out=out)
+
+
+def _roofline(nbytes, seconds, kernel, unit_note):
+    peak, kind = _peaks()
+    achieved = nbytes / seconds / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "peak_kind": kind + " (burst copy)", "frac": round(achieved / peak, 4),
+            "bytes_per_launch": int(nbytes), "avg_launch_us": round(seconds * 1e6, 3), "per": unit_note}
+
+
+class SingleLayer:
+    """One MoE layer for one token: 64 NVFP4 experts (H=2560, I=640), top-10,
+    x ~ N(0,1) BF16, W_r ~ N(0,0.02).  One call = moe_decode_layer from x
+    (router + expert pass in one launch); a fresh token per call and the L2
+    flushed between calls."""
+
+    WORKLOAD, NE = 0, 64
+
+    def __init__(self, torch, moe, synth, device, calls):
+        self.torch, self.moe = torch, moe
+        self.s = moe.shape(H, I, moe.FMT_NVFP4)
+        self.rb = moe.moe_expert_record_bytes(self.s)
+        self.pool = torch.empty(self.NE, self.rb, dtype=torch.uint8, device=device)
+        for e in range(self.NE):
+            g, up, d = synth.expert_weights(H, I, synth.expert_seed(self.WORKLOAD, 0, e), device=device)
+            moe.fp4_pack_expert(g, up, d, self.s, record=self.pool[e])
+        self.ptrs = moe.pointer_table([self.pool[e] for e in range(self.NE)])
+        self.wr = synth.router_weights(self.NE, H, synth.seed_of(self.WORKLOAD, 0, synth.T_ROUTER), device=device)
+        self.xs = torch.cat([synth.activations(1, H, synth.seed_of(self.WORKLOAD, 100 + c, synth.T_X), device=device)
+                             for c in range(calls)])
+        self.idx = torch.empty(1, K_TOP, dtype=torch.int32, device=device)
+        self.w = torch.empty(1, K_TOP, dtype=torch.float32, device=device)
+        self.logits = torch.empty(1, self.NE, dtype=torch.float32, device=device)
+        self.y = torch.empty(1, H, dtype=torch.float32, device=device)
+        self.ws = torch.zeros(moe.moe_experts_decode_workspace(1, K_TOP, self.s), dtype=torch.uint8, device=device)
+        self.st = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flush = _l2_flusher(torch, device)
+
+    def call(self, c):
+        self.moe.moe_decode_layer(self.wr, None, K_TOP, self.ptrs, self.s, x=self.xs[c:c + 1], idx=self.idx,
+                                  weights=self.w, logits=self.logits, y=self.y, workspace=self.ws, dev_status=self.st)
+
+    def measure(self, calls, warm):
+        torch = self.torch
+        for c in range(warm):
+            self.call(c % self.xs.shape[0])
+        torch.cuda.synchronize()
+        tot = 0.0
+        for c in range(calls):
+            self.flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            self.call(c % self.xs.shape[0])
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        sec = tot / calls / 1e3
+        exp_bytes = K_TOP * self.rb
+        nbytes = exp_bytes + self.NE * H * 2 + H * 2 + H * 4 + 2 * K_TOP * I * 4 + 2 * self.NE * 4
+        return {"workload": "one MoE layer, one token: 64 NVFP4 experts (H=2560, I=640), top-10",
+                "value": round(exp_bytes / sec / 1e9, 2), "unit": "GB/s", "us_per_layer": round(sec * 1e6, 3),
+                "calls": calls, "l2": "flushed between calls (512 MB read sweep)",
+                "dev_status": int(self.st.item()),
+                "roofline": _roofline(nbytes, sec, "moe_decode_layer: oneshot_kernel", "one layer launch")}
+
+
+class DeepSeekCalls:
+    """DeepSeek-shaped layer: H=4096, I=2880, MXFP4 records of 18,800,640 B,
+    384 experts, top-6; one weight set reused for 40 sequential calls, each
+    with its own seeded router weights and token; L2 flushed between calls.
+    One call = moe_router_topk + moe_experts_decode (the shape's per-SM share
+    is larger than shared memory, so the expert pass is the ring kernel)."""
+
+    WORKLOAD, NE, HD, ID, KD, CALLS = 3, 384, 4096, 2880, 6, 40
+
+    def __init__(self, torch, moe, synth, device):
+        self.torch, self.moe = torch, moe
+        self.s = moe.shape(self.HD, self.ID, moe.FMT_MXFP4)
+        self.rb = moe.moe_expert_record_bytes(self.s)
+        self.pool = torch.empty(self.NE, self.rb, dtype=torch.uint8, device=device)
+        for e in range(self.NE):
+            g, up, d = synth.expert_weights(self.HD, self.ID, synth.expert_seed(self.WORKLOAD, 0, e), device=device)
+            moe.fp4_pack_expert(g, up, d, self.s, record=self.pool[e])
+        self.ptrs = moe.pointer_table([self.pool[e] for e in range(self.NE)])
+        self.wr = [synth.router_weights(self.NE, self.HD, synth.seed_of(self.WORKLOAD, c, synth.T_ROUTER),
+                                        device=device) for c in range(self.CALLS)]
+        self.xs = [synth.activations(1, self.HD, synth.seed_of(self.WORKLOAD, c, synth.T_X), device=device)
+                   for c in range(self.CALLS)]
+        self.idx = torch.empty(1, self.KD, dtype=torch.int32, device=device)
+        self.w = torch.empty(1, self.KD, dtype=torch.float32, device=device)
+        self.logits = torch.empty(1, self.NE, dtype=torch.float32, device=device)
+        self.y = torch.empty(1, self.HD, dtype=torch.float32, device=device)
+        self.ws = torch.zeros(moe.moe_experts_decode_workspace(1, self.KD, self.s), dtype=torch.uint8, device=device)
+        self.st = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flush = _l2_flusher(torch, device)
+
+    def router(self, c):
+        self.moe.moe_router_topk(self.xs[c], self.wr[c], None, self.KD, self.idx, self.w, self.logits)
+
+    def experts(self, c):
+        self.moe.moe_experts_decode(self.xs[c], self.idx, self.w, self.ptrs, self.s, self.y, self.ws, self.st)
+
+    def measure(self, warm):
+        torch = self.torch
+        for c in range(warm):
+            self.router(c % self.CALLS)
+            self.experts(c % self.CALLS)
+        torch.cuda.synchronize()
+        tot, tot_exp = 0.0, 0.0
+        for c in range(self.CALLS):
+            self.flush()
+            a, b, d = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record()
+            self.router(c)
+            b.record()
+            self.experts(c)
+            d.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(d)
+            tot_exp += b.elapsed_time(d)
+        sec, sec_exp = tot / self.CALLS / 1e3, tot_exp / self.CALLS / 1e3
+        exp_bytes = self.KD * self.rb
+        nbytes = exp_bytes + self.HD * 2 + self.HD * 4 + self.KD * self.ID * 4 * 2
+        return {"workload": "DeepSeek-shaped layer: 384 MXFP4 experts (H=4096, I=2880, 18,800,640 B), top-6, "
+                            "40 seeded calls on one weight set",
+                "value": round(exp_bytes / sec / 1e9, 2), "unit": "GB/s", "us_per_call": round(sec * 1e6, 3),
+                "us_expert_pass": round(sec_exp * 1e6, 3), "us_per_40_calls": round(40 * sec * 1e6, 1),
+                "expert_bytes_per_call": exp_bytes, "l2": "flushed between calls (512 MB read sweep)",
+                "dev_status": int(self.st.item()),
+                "roofline": _roofline(nbytes, sec_exp, "moe_experts_decode: stream_kernel (TMA ring)",
+                                      "one expert-pass launch")}
+
+
+class BatchedStack:
+    """32 tokens through the 48-layer stack of the decode pool (config of the
+    decode stack, 512 experts per layer, top-10): per layer the router (layer
+    0 from x, later layers RMS-chained from the previous output) and the
+    expert pass for all 32 tokens; one step = 48 layers, captured in a CUDA
+    graph.  Unique expert bytes per layer are counted from the routing."""
+
+    T = 32
+
+    def __init__(self, torch, moe, synth, stack, device, steps_total):
+        self.torch, self.moe, self.st_ = torch, moe, stack
+        T = self.T
+        self.x0 = [synth.activations(T, H, synth.seed_of(4, 100 + s, synth.T_X), device=device)
+                   for s in range(steps_total)]
+        self.x = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty(LAYERS, T, K_TOP, dtype=torch.int32, device=device)
+        self.w = torch.empty(T, K_TOP, dtype=torch.float32, device=device)
+        self.logits = torch.empty(T, E, dtype=torch.float32, device=device)
+        self.y = torch.empty(T, H, dtype=torch.float32, device=device)
+        self.ws = torch.zeros(moe.moe_experts_decode_workspace(T, K_TOP, stack.s), dtype=torch.uint8, device=device)
+        self.st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def run_layers(self):
+        moe, st = self.moe, self.st_
+        for L in range(LAYERS):
+            if L == 0:
+                moe.moe_router_topk(self.x, st.wr[L], None, K_TOP, self.idx[L], self.w, self.logits)
+            else:
+                moe.moe_rmsnorm_router_topk(self.y, st.wr[L], None, K_TOP, 1e-6, self.x, self.idx[L], self.w,
+                                            self.logits)
+            moe.moe_experts_decode(self.x, self.idx[L], self.w, st.ptrs[L], st.s, self.y, self.ws, self.st)
+
+    def measure(self, steps, warm):
+        torch = self.torch
+        self.x.copy_(self.x0[0])
+        self.run_layers()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self.run_layers()
+        for s in range(warm):
+            self.x.copy_(self.x0[s % len(self.x0)])
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        uniq = 0
+        a.record()
+        for s in range(steps):
+            self.x.copy_(self.x0[(warm + s) % len(self.x0)])
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        sec = a.elapsed_time(b) / steps / 1e3
+        # unique records of the last step's 48 layers (the routing of every step is of the same kind)
+        for L in range(LAYERS):
+            uniq += int(torch.unique(self.idx[L]).numel())
+        exp_bytes = uniq * self.st_.rec_bytes
+        del g
+        nbytes = exp_bytes + LAYERS * (E * H * 2 + self.T * H * (2 + 4 + 4) + 2 * self.T * K_TOP * I * 4)
+        return {"workload": "batched decode: 32 tokens x 48 layers x 512 NVFP4 experts, top-10",
+                "value": round(self.T / sec, 1), "unit": "tokens/s", "ms_per_step": round(sec * 1e3, 4),
+                "unique_experts_per_layer": round(uniq / LAYERS, 1), "expert_bytes_per_step": exp_bytes,
+                "expert_gbs": round(exp_bytes / sec / 1e9, 1),
+                "l2": "inputs larger than L2 (~0.66 GB of distinct records per layer)",
+                "launches_per_step": LAYERS * 5, "dev_status": int(self.st.item()),
+                "roofline": _roofline(nbytes, sec, "whole step (router kernels + two-kernel expert pass), "
+                                      "unique-record bytes", "one 48-layer step")}
+
+
+def measure_host_tier(torch, moe, synth, device, calls: int = 40):
+    """The host-memory expert tier: 64 NVFP4 experts (177 MB) in pinned host
+    memory, one token top-10 per call through moe_experts_decode_host (plain
+    loads over the device's address space: NVLink-C2C on a Grace machine);
+    the same records in HBM through the same call for comparison.  A fresh
+    token per call, L2 flushed between calls."""
+    s = moe.shape(H, I, moe.FMT_NVFP4)
+    rb = moe.moe_expert_record_bytes(s)
+    NE = 64
+    dev_pool = torch.empty(NE, rb, dtype=torch.uint8, device=device)
+    for e in range(NE):
+        g, up, d = synth.expert_weights(H, I, synth.expert_seed(0, 0, e), device=device)
+        moe.fp4_pack_expert(g, up, d, s, record=dev_pool[e])
+    host_pool = torch.empty(NE, rb, dtype=torch.uint8, pin_memory=True)
+    host_pool.copy_(dev_pool)
+    torch.cuda.synchronize()
+    tables = {"host": torch.tensor([host_pool[e].data_ptr() for e in range(NE)], dtype=torch.int64, device=device),
+              "hbm": moe.pointer_table([dev_pool[e] for e in range(NE)])}
+    wr = synth.router_weights(NE, H, synth.seed_of(0, 0, synth.T_ROUTER), device=device)
+    flush = _l2_flusher(torch, device)
+    ws = torch.zeros(moe.moe_experts_decode_workspace(1, K_TOP, s), dtype=torch.uint8, device=device)
+    y = torch.empty(1, H, dtype=torch.float32, device=device)
+    out = {}
+    for name, ptrs in tables.items():
+        tot = 0.0
+        for c in range(calls + 3):
+            x = synth.activations(1, H, synth.seed_of(0, 300 + c, synth.T_X), device=device)
+            idx, w, _ = moe.moe_router_topk(x, wr, None, K_TOP)
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            moe.moe_experts_decode_host(x, idx, w, ptrs, s, y, ws)
+            b.record()
+            torch.cuda.synchronize()
+            if c >= 3:
+                tot += a.elapsed_time(b)
+        sec = tot / calls / 1e3
+        out[name] = {"us_per_call": round(sec * 1e6, 2), "expert_gbs": round(K_TOP * rb / sec / 1e9, 1)}
+    del host_pool
+    return {"workload": "one token, top-10 of 64 NVFP4 experts (H=2560, I=640); records in pinned host memory vs HBM",
+            "entry": "moe_experts_decode_host (two kernels, plain 16-byte loads)", **out}
 
 
 def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
@@ -349,7 +655,16 @@ def run_ours(args):
         dist.barrier()
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
+    # the clock sampler polls every 200 ms: run the same step back to back for
+    # 1.5 s right before the timed region, so the clocks it records (over that
+    # run and the timed region) are those of this workload under load
+    t_soak = time.time()
+    n_soak = 0
+    while time.time() - t_soak < 1.5:
+        for _ in range(50):
+            one_step(n_soak % (steps + warm))
+            n_soak += 1
+        torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -359,6 +674,8 @@ def run_ours(args):
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = "a 1.5 s back-to-back run of the same step right before the timed region, and the region"
     ms = t_start.elapsed_time(t_end) / steps
     if world > 1:
         ms = max_over_ranks(ms, dist, dev)
@@ -421,6 +738,27 @@ def run_ours(args):
                "h2d_bytes_per_step": H * 2, "d2h_bytes_per_step": H * 4,
                "ms_per_step": round(wall * 1e3, 4), "api": "eager C-ABI calls, 48 per token (moe_decode_layer)"}
 
+    spec = None
+    if not args.no_others:
+        try:
+            spec = speculative_routing(torch, moe, wl)
+        except Exception as exc:  # report, do not hide
+            spec = {"error": repr(exc)[:300]}
+
+    # the other workloads, one key each
+    others = {}
+    if not args.no_others:
+        jobs = (("config4", lambda: BatchedStack(torch, moe, synth, wl, dev, 8).measure(max(3, min(steps, 10)), 3)),
+                ("host_tier", lambda: measure_host_tier(torch, moe, synth, dev)),
+                ("config0", lambda: SingleLayer(torch, moe, synth, dev, 64).measure(max(20, min(steps, 200)), 5)),
+                ("config3", lambda: DeepSeekCalls(torch, moe, synth, dev).measure(5)))
+        for key, job in jobs:
+            try:
+                others[key] = job()
+            except Exception as exc:  # report, do not hide
+                others[key] = {"error": repr(exc)[:300]}
+            torch.cuda.empty_cache()
+
     prompt = None
     if not args.no_prompt:
         del wl.slots
@@ -438,6 +776,7 @@ def run_ours(args):
             fp8 = measure_fp8_gemv(torch, moe, synth, dev)
         except Exception as exc:
             fp8 = {"error": repr(exc)[:300]}
+
 
     peak, peak_kind = _peaks()
     value = wl.expert_bytes_per_step() * world / (ms / 1e3) / 1e9
@@ -482,11 +821,22 @@ def run_ours(args):
         "e2e": e2e,
         "prompt": prompt,
         "fp8_gemv": fp8,
+        "speculative_routing": spec,
         "dev_status": st,
         "setup_s": round(wl.setup_s, 1),
     }
+    out.update(others)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        # the oracle on a bounded sample of each other workload, in that
+        # workload's unit
+        for key, fn in (("config0", cpu_baseline_config0), ("config3", cpu_baseline_config3),
+                        ("config4", cpu_baseline_config4), ("prompt", cpu_baseline_prompt)):
+            if isinstance(out.get(key), dict) and "error" not in out[key]:
+                try:
+                    out[key]["cpu_baseline"] = fn(args.cpu_seconds_other)
+                except Exception as exc:  # report, do not hide
+                    out[key]["cpu_baseline"] = {"error": repr(exc)[:300]}
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -552,6 +902,149 @@ def _cores():
         return int(n)
     except Exception:
         return os.cpu_count() or 1
+
+
+def _spawn_pool(n):
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    return cf.ProcessPoolExecutor(max_workers=min(n, os.cpu_count() or 2), mp_context=mp.get_context("spawn"))
+
+
+def _pack_seeded(args):
+    """Oracle packing of one seeded expert (spawned worker; untimed)."""
+    h, i, fmt, seed = args
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+    g, up, d = synth.expert_weights(h, i, seed)
+    return O.pack_expert(g.numpy(), up.numpy(), d.numpy(), fmt)
+
+
+def _bits_np(t):
+    import torch
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_baseline_config0(budget_s: float):
+    """The oracle on the one-layer workload: router over 64 experts + 10
+    experts for one token, per call; records packed outside the timed part."""
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+    wr = _bits_np(synth.router_weights(64, H, synth.seed_of(0, 0, synth.T_ROUTER)))
+    busy, calls, recs = 0.0, 0, {}
+    with _spawn_pool(K_TOP) as ex:
+        while busy < budget_s and calls < 64:
+            x = _bits_np(synth.activations(1, H, synth.seed_of(0, 100 + calls, synth.T_X)))
+            t0 = time.perf_counter()
+            idx, w = O.topk_softmax(O.router_logits(x, wr), K_TOP)
+            busy += time.perf_counter() - t0
+            need = [int(e) for e in idx.ravel() if int(e) not in recs]
+            for e, r in zip(need, ex.map(_pack_seeded, [(H, I, O.FMT_NVFP4, synth.expert_seed(0, 0, e)) for e in need])):
+                recs[e] = r
+            t0 = time.perf_counter()
+            O.moe_layer_decode(x, idx, w, recs, H, I, O.FMT_NVFP4)
+            busy += time.perf_counter() - t0
+            calls += 1
+    rb = O.record_bytes(H, I, O.FMT_NVFP4)
+    return {"value": round(calls * K_TOP * rb / busy / 1e9, 4), "unit": "GB/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{calls} one-token layer calls (router over 64 experts + 10 experts), float64 numpy; "
+                      "record packing untimed", "seconds": round(busy, 2)}
+
+
+def cpu_baseline_config3(budget_s: float):
+    """The oracle on the DeepSeek-shaped calls: router over 384 experts + 6
+    MXFP4 experts per call; records packed outside the timed part."""
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+    HD, ID, NE, KD = 4096, 2880, 384, 6
+    busy, calls = 0.0, 0
+    with _spawn_pool(KD) as ex:
+        while busy < budget_s and calls < 40:
+            wr = _bits_np(synth.router_weights(NE, HD, synth.seed_of(3, calls, synth.T_ROUTER)))
+            x = _bits_np(synth.activations(1, HD, synth.seed_of(3, calls, synth.T_X)))
+            t0 = time.perf_counter()
+            idx, w = O.topk_softmax(O.router_logits(x, wr), KD)
+            busy += time.perf_counter() - t0
+            sel = [int(e) for e in idx.ravel()]
+            recs = dict(zip(sel, ex.map(_pack_seeded, [(HD, ID, O.FMT_MXFP4, synth.expert_seed(3, 0, e)) for e in sel])))
+            t0 = time.perf_counter()
+            O.moe_layer_decode(x, idx, w, recs, HD, ID, O.FMT_MXFP4)
+            busy += time.perf_counter() - t0
+            calls += 1
+    rb = O.record_bytes(HD, ID, O.FMT_MXFP4)
+    return {"value": round(calls * KD * rb / busy / 1e9, 4), "unit": "GB/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{calls} of the 40 DeepSeek-shaped calls (router over 384 + 6 MXFP4 experts), float64 numpy; "
+                      "record packing untimed", "seconds": round(busy, 2)}
+
+
+def cpu_baseline_config4(budget_s: float):
+    """The oracle on the batched stack: tokens of layer 0 of a 32-token batch,
+    one at a time (router + 10 experts each), until the budget is used; the
+    unit is tokens per second through one layer, divided by the 48 layers."""
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+    wr = _bits_np(synth.router_weights(E, H, synth.seed_of(WORKLOAD_ID, 0, synth.T_ROUTER)))
+    rng = np.random.default_rng(synth.seed_of(WORKLOAD_ID, 0, synth.T_PERM))
+    choice = rng.permutation(UNIQUE_EXPERTS)[:E]
+    xs = _bits_np(synth.activations(32, H, synth.seed_of(4, 100, synth.T_X)))
+    busy, done = 0.0, 0
+    with _spawn_pool(K_TOP) as ex:
+        while busy < budget_s and done < 32:
+            x = xs[done:done + 1]
+            t0 = time.perf_counter()
+            idx, w = O.topk_softmax(O.router_logits(x, wr), K_TOP)
+            busy += time.perf_counter() - t0
+            sel = [int(e) for e in idx.ravel()]
+            recs = dict(zip(sel, ex.map(_pack_seeded, [(H, I, O.FMT_NVFP4, synth.expert_seed(WORKLOAD_ID, 0, int(choice[e])))
+                                                       for e in sel])))
+            t0 = time.perf_counter()
+            O.moe_layer_decode(x, idx, w, recs, H, I, O.FMT_NVFP4)
+            busy += time.perf_counter() - t0
+            done += 1
+    return {"value": round(done / busy / LAYERS, 5), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{done} tokens of one layer of the 32-token batch (router + 10 experts each), float64 numpy, "
+                      "rate divided by 48 layers; record packing untimed", "seconds": round(busy, 2)}
+
+
+def cpu_baseline_prompt(budget_s: float):
+    """The oracle on the prompt layer: its expert-by-expert form on a sample
+    of the hit experts (each with all of its tokens), scaled to all hit
+    experts, plus the router logits of a token sample scaled to 2451 tokens."""
+    import torch
+    from block_scaled_fp4_softmax_gb300 import synth
+    from oracle import oracle as O
+    T = PromptLayer.T
+    x = _bits_np(synth.activations(T, H, synth.seed_of(2, 0, synth.T_X)))
+    wr = _bits_np(synth.router_weights(E, H, synth.seed_of(2, 0, synth.T_ROUTER)))
+    bias = synth.zipf_bias(E, synth.seed_of(2, 0, synth.T_BIAS)).numpy()
+    # routing of all tokens (untimed; the logits are timed on a sample below)
+    lg = (O.bf16_bits_to_f32(x).astype(np.float64) @ O.bf16_bits_to_f32(wr).astype(np.float64).T) + bias
+    idx = np.argsort(-lg, axis=1, kind="stable")[:, :K_TOP].astype(np.int32)
+    w = np.full(idx.shape, 1.0 / K_TOP)
+    hit = np.unique(idx)
+    rng = np.random.default_rng(5)
+    t0 = time.perf_counter()
+    O.router_logits(x[:64], wr, bias)
+    t_router = (time.perf_counter() - t0) * T / 64
+    busy, n = 0.0, 0
+    order = rng.permutation(hit)
+    with _spawn_pool(8) as ex:
+        while busy < budget_s and n < len(order):
+            batch = [int(e) for e in order[n:n + 4]]
+            recs = dict(zip(batch, ex.map(_pack_seeded, [(H, I, O.FMT_NVFP4, synth.expert_seed(2, 0, e)) for e in batch])))
+            for e in batch:
+                toks = np.nonzero((idx == e).any(axis=1))[0]
+                idx_e = np.full((len(toks), 1), e, dtype=np.int32)
+                w_e = np.full((len(toks), 1), 1.0 / K_TOP)
+                t0 = time.perf_counter()
+                O.moe_layer_grouped_by_expert(x[toks], idx_e, w_e, recs, H, I, O.FMT_NVFP4)
+                busy += time.perf_counter() - t0
+                n += 1
+    est = t_router + busy * len(hit) / n
+    return {"value": round(T / est, 2), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{n} of {len(hit)} hit experts (each with all its tokens) through the oracle's "
+                      "expert-by-expert form, scaled to all hit experts, plus router logits of 64 tokens "
+                      "scaled to 2451; float64 numpy; record packing untimed",
+            "seconds": round(busy, 2)}
 
 
 def cpu_baseline(budget_s: float):
@@ -630,12 +1123,14 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prompt", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the one-layer, DeepSeek-shaped and batched workloads")
+    ap.add_argument("--cpu-seconds-other", type=float, default=6.0)
     ap.add_argument("--profile-case", choices=("none", "decode_layer", "prompt_layer"), default="none",
                     help="small fixed case for ncu captures (no JSON line)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -141,10 +141,9 @@ extern "C" int moe_bucket_by_expert(const int32_t* idx, int T, int k, int E, int
   int32_t* seg_counts = reinterpret_cast<int32_t*>(workspace);
   int32_t* seg_base = seg_counts + (size_t)S * E;
   const size_t hsmem = (size_t)E * sizeof(int32_t);
-  if (hsmem > 48 * 1024) {
-    cudaFuncSetAttribute(seg_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem);
-    cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem);
-  }
+  static moe::SmemGrant g_hist, g_scatter;
+  if (!moe::grant_smem(seg_hist_kernel, hsmem, g_hist) || !moe::grant_smem(scatter_kernel, hsmem, g_scatter))
+    return MOE_ERR_CUDA;
   seg_hist_kernel<<<S, 256, hsmem, st>>>(idx, (int)P, E, seg_counts, dev_status);
   scan_kernel<<<1, 1024, 0, st>>>(seg_counts, S, E, counts, offsets, seg_base);
   scatter_kernel<<<S, 32, hsmem, st>>>(idx, (int)P, E, seg_base, pairs);

@@ -6,6 +6,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "moe.h"
 
 namespace moe {
@@ -44,6 +47,84 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Per-device facts and kernel attributes.  A process may drive several GPUs
+// (one per thread, or one after another), so everything that depends on the
+// device -- its SM count, its shared-memory limit, and the dynamic
+// shared-memory size a kernel was allowed on it -- is kept per device id.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+inline std::mutex& host_mutex() {
+  static std::mutex m;
+  return m;
+}
+
+inline int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+struct DeviceInfo {
+  int sms;         // streaming multiprocessors
+  int smem_optin;  // largest dynamic shared memory one block may opt in to
+};
+
+// The current device's facts, looked up once per device; {0, 0} when there
+// is no usable device.
+inline DeviceInfo device_info() {
+  static std::atomic<int> sms[kMaxDevices], smem[kMaxDevices];
+  const int d = current_device();
+  if (d < 0) return DeviceInfo{0, 0};
+  int a = sms[d].load(std::memory_order_acquire);
+  if (a == 0) {
+    std::lock_guard<std::mutex> lock(host_mutex());
+    int n = 0, m = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess)
+      return DeviceInfo{0, 0};
+    smem[d].store(m, std::memory_order_relaxed);
+    sms[d].store(n, std::memory_order_release);
+    a = n;
+  }
+  return DeviceInfo{a, smem[d].load(std::memory_order_relaxed)};
+}
+
+// Dynamic shared memory granted to one kernel, per device.
+struct SmemGrant {
+  std::atomic<size_t> bytes[kMaxDevices];
+};
+
+// Raises `kernel`'s dynamic shared-memory limit on the current device to
+// `bytes` unless an earlier call already did; the attribute call is made once
+// per (kernel, device, size increase), so later launches can be captured in
+// a graph.  With `threads` > 0 the kernel runs a grid-wide barrier over one
+// CTA per SM, which needs every CTA resident at once: the grant then also
+// checks that one CTA of `threads` threads and `bytes` bytes fits on an SM
+// (it returns false otherwise).  Kernels of other streams, processes (MPS) or
+// green contexts that hold SMs can still keep CTAs waiting; the barrier waits
+// are bounded and report MOE_DEV_TIMEOUT then.
+template <typename K>
+inline bool grant_smem(K kernel, size_t bytes, SmemGrant& g, int threads = 0) {
+  const int d = current_device();
+  if (d < 0) return false;
+  const size_t key = bytes + 1;  // 0 means "nothing checked yet", also for small sizes
+  if (key <= g.bytes[d].load(std::memory_order_acquire)) return true;
+  std::lock_guard<std::mutex> lock(host_mutex());
+  if (key <= g.bytes[d].load(std::memory_order_relaxed)) return true;
+  if (bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+    return false;
+  if (threads > 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, bytes) != cudaSuccess || n < 1)
+      return false;
+  }
+  g.bytes[d].store(key, std::memory_order_release);
+  return true;
 }
 
 // ---------------------------------------------------------------------------

@@ -700,25 +700,15 @@ inline size_t smem_bytes(int T, int k, int H, int I, int sms, int slots, int slo
 
 }  // namespace st
 
-template <typename K>
-bool ensure_smem(K kernel, size_t bytes, size_t* granted) {
-  if (bytes <= 48 * 1024 || bytes <= *granted) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-      cudaSuccess)
-    return false;
-  *granted = bytes;
-  return true;
-}
-
 template <int FMT>
 int launch_decode(const uint16_t* x, const int32_t* idx, const float* w, int T, int k,
                   const void* const* ptrs, int E, int H, int I, float* y, float* hws,
                   int32_t* st, cudaStream_t stream) {
   const size_t smem1 = (size_t)H * sizeof(float);
   const size_t smem2 = (size_t)k * I * sizeof(float);
-  static size_t granted1 = 0, granted2 = 0;
-  if (!ensure_smem(decode_gateup_kernel<FMT>, smem1, &granted1) ||
-      !ensure_smem(decode_down_kernel<FMT>, smem2, &granted2))
+  static moe::SmemGrant granted1, granted2;
+  if (!moe::grant_smem(decode_gateup_kernel<FMT>, smem1, granted1) ||
+      !moe::grant_smem(decode_down_kernel<FMT>, smem2, granted2))
     return MOE_ERR_CUDA;
   dim3 g1((I + 7) / 8, T * k);
   decode_gateup_kernel<FMT><<<g1, kThreads, smem1, stream>>>(x, idx, k, ptrs, E, H, I, hws, st);
@@ -727,27 +717,9 @@ int launch_decode(const uint16_t* x, const int32_t* idx, const float* w, int T, 
   return moe::launch_status();
 }
 
-int stream_smem_limit() {
-  static int limit = 0;
-  if (limit == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      limit = 0;
-  }
-  return limit;
-}
+int stream_smem_limit() { return moe::device_info().smem_optin; }
 
-int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 0;
-  }
-  return sms;
-}
+int sm_count() { return moe::device_info().sms; }
 
 // The streaming kernel takes T*k <= 64 pairs when at least 16 ring slots fit
 // next to the activations.
@@ -765,8 +737,8 @@ int stream_slots(int T, int k, int H, int I, int fmt, int* slot_bytes) {
 
 template <int FMT, int UPR, int UPDR>
 int launch_stream_shape(const st::Args& sa, size_t smem, int sms, cudaStream_t stream) {
-  static size_t granted = 0;
-  if (!ensure_smem(st::stream_kernel<FMT, UPR, UPDR>, smem, &granted)) return MOE_ERR_CUDA;
+  static moe::SmemGrant granted;
+  if (!moe::grant_smem(st::stream_kernel<FMT, UPR, UPDR>, smem, granted, st::kThreads)) return MOE_ERR_CUDA;
   return moe::launch_pdl(st::stream_kernel<FMT, UPR, UPDR>, dim3(sms), dim3(st::kThreads), smem,
                          stream, sa);
 }
@@ -795,18 +767,40 @@ extern "C" size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s)
   return moe::os::kHeaderBytes + (size_t)T * k * s.inter * sizeof(float);
 }
 
-extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
-                                  int T, int k, const void* const* expert_ptrs, int E,
-                                  moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
-                                  int32_t* dev_status, void* stream) {
+// The argument checks of moe_experts_decode that do not involve the
+// workspace (shared with the allocation-free entry point, which runs them
+// before it touches its scratch).
+static int decode_check_args(const uint16_t* x_bf16, const int32_t* idx, const float* weights, int T, int k,
+                             const void* const* expert_ptrs, int E, const moe_expert_shape& s, const float* y) {
   if (!x_bf16 || !idx || !weights || !expert_ptrs || !y) return MOE_ERR_INVALID_ARG;
   if (T < 0 || k <= 0 || k > 32 || E <= 0) return MOE_ERR_INVALID_ARG;
   if (!moe::shape_ok(s)) return MOE_ERR_UNSUPPORTED;
   if ((long long)T * k > 4096 || (long long)k * s.inter > 49152) return MOE_ERR_UNSUPPORTED;
+  if (!moe::aligned16(x_bf16)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+static int decode_launch(const uint16_t* x_bf16, const int32_t* idx, const float* weights, int T, int k,
+                         const void* const* expert_ptrs, int E, const moe_expert_shape& s, float* y,
+                         void* workspace, int32_t* dev_status, void* stream);
+
+extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
+                                  int T, int k, const void* const* expert_ptrs, int E,
+                                  moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
+                                  int32_t* dev_status, void* stream) {
+  const int rc = decode_check_args(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y);
+  if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
   if (!workspace) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < moe_experts_decode_workspace(T, k, s)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (!moe::aligned16(x_bf16) || !moe::aligned16(workspace)) return MOE_ERR_ALIGNMENT;
+  if (!moe::aligned16(workspace)) return MOE_ERR_ALIGNMENT;
+  return decode_launch(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y, workspace, dev_status, stream);
+}
+
+static int decode_launch(const uint16_t* x_bf16, const int32_t* idx, const float* weights, int T, int k,
+                         const void* const* expert_ptrs, int E, const moe_expert_shape& s, float* y,
+                         void* workspace, int32_t* dev_status, void* stream) {
+  if (sm_count() <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
@@ -855,6 +849,31 @@ extern "C" int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, co
                                         s.inter, y, hws, dev_status, st);
   return launch_decode<MOE_FMT_MXFP4>(x_bf16, idx, weights, T, k, expert_ptrs, E, s.hidden,
                                       s.inter, y, hws, dev_status, st);
+}
+
+// Decode with records in host memory (the host tier): the same expert pass
+// with plain 16-byte loads only, which read system memory through the
+// device's address space (pinned host memory on a system with unified
+// addressing, or any memory a Grace CPU and the GPU share over NVLink-C2C),
+// so the records need not be in HBM.  The two-kernel path computes it.
+extern "C" int moe_experts_decode_host(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
+                                       int T, int k, const void* const* expert_ptrs, int E,
+                                       moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
+                                       int32_t* dev_status, void* stream) {
+  const int rc = decode_check_args(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_experts_decode_workspace(T, k, s)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!moe::aligned16(workspace)) return MOE_ERR_ALIGNMENT;
+  if (sm_count() <= 0) return MOE_ERR_CUDA;
+  float* hws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + moe::os::kHeaderBytes);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (s.format == MOE_FMT_NVFP4)
+    return launch_decode<MOE_FMT_NVFP4>(x_bf16, idx, weights, T, k, expert_ptrs, E, s.hidden, s.inter, y, hws,
+                                        dev_status, st);
+  return launch_decode<MOE_FMT_MXFP4>(x_bf16, idx, weights, T, k, expert_ptrs, E, s.hidden, s.inter, y, hws,
+                                      dev_status, st);
 }
 
 // One decode layer in one launch: the router (RMS chaining of the previous
@@ -921,7 +940,7 @@ namespace {
 constexpr size_t kStaticScratchBytes = (size_t)2 << 20;  // 2 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = moe::kMaxDevices;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
@@ -950,19 +969,19 @@ extern "C" int moe_experts_decode_noalloc(const uint16_t* x_bf16, const int32_t*
                                           const void* const* expert_ptrs, int E,
                                           moe_expert_shape s, float* y, int32_t* dev_status,
                                           void* stream) {
-  if (!x_bf16 || !idx || !weights || !expert_ptrs || !y) return MOE_ERR_INVALID_ARG;
-  if (T < 0 || k <= 0 || k > 32 || E <= 0) return MOE_ERR_INVALID_ARG;
-  if (!moe::shape_ok(s)) return MOE_ERR_UNSUPPORTED;
+  // every check that moe_experts_decode makes comes first, so a rejected
+  // call leaves the shared array untouched and returns the same status
+  int rc = decode_check_args(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y);
+  if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
   const size_t need = moe_experts_decode_workspace(T, k, s);
   if (need == 0 || need > kStaticScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
-  const int rc = static_scratch(&scratch);
+  rc = static_scratch(&scratch);
   if (rc != MOE_OK) return rc;
   // The array keeps whatever the previous call left; its header of barrier
-  // and combine counters must start at zero.
+  // counters must start at zero.
   if (cudaMemsetAsync(scratch, 0, moe::os::kHeaderBytes, (cudaStream_t)stream) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return moe_experts_decode(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y, scratch,
-                            kStaticScratchBytes, dev_status, stream);
+  return decode_launch(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y, scratch, dev_status, stream);
 }

@@ -37,14 +37,12 @@
 namespace moe {
 namespace os {
 
-constexpr uint64_t kWaitNs = 2000000000ull;
-
-// Waits (bounded) for one barrier's parity-0 phase; on timeout flags the
-// launch and returns false.
-__device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status) {
+// Waits (bounded by wait_ns) for one barrier's parity-0 phase; on timeout
+// flags the launch and returns false.
+__device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status, uint64_t wait_ns) {
   volatile int* abort_flag = tb.flags;
   if (*abort_flag) return false;
-  if (tc::mbar_wait(bar, 0, tc::globaltimer() + kWaitNs)) return true;
+  if (tc::mbar_wait(bar, 0, tc::globaltimer() + wait_ns)) return true;
   *abort_flag = 1;
   status_or(status, MOE_DEV_TIMEOUT);
   return false;
@@ -60,12 +58,13 @@ __device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status) {
 // CTA reads the counter before its own first arrival, so fewer than grid
 // arrivals of this launch can precede the read.  False on timeout, which
 // also flags the launch.
-__device__ bool grid_sync_thread(unsigned long long* bar, unsigned long long target, Tab& tb, int32_t* status) {
+__device__ bool grid_sync_thread(unsigned long long* bar, unsigned long long target, Tab& tb, int32_t* status,
+                                 uint64_t wait_ns) {
   volatile int* abort_flag = tb.flags;
   int good = !*abort_flag;
   if (good) {
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
-    const uint64_t dl = global_ns() + kWaitNs;
+    const uint64_t dl = global_ns() + wait_ns;
     while (dm::ld_acquire_u64(bar) < target) {
       if (global_ns() > dl) {
         good = 0;
@@ -170,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     if (lane == 0) {
       for (int i = 0; i < kNumBars; ++i) tc::mbar_arrive(&bars[i]);
       // no copy may still be in flight when the CTA exits
-      const uint64_t dl = tc::globaltimer() + kWaitNs;
+      const uint64_t dl = tc::globaltimer() + a.wait_ns;
       for (int i = 0; i < kNumBars; ++i) tc::mbar_wait_backoff(&bars[i], 0, dl);
     }
     __syncthreads();
@@ -183,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // nothing before)
   unsigned long long bar_start = 0;
   if (threadIdx.x == 0) bar_start = rt::ld_relaxed_u64(a.bar);
-  auto bar_target = [&](unsigned n) { return (bar_start / gridDim.x + n) * gridDim.x; };
+  auto bar_target = [&](unsigned n) { return (bar_start / gridDim.x + n) * gridDim.x + a.barrier_extra; };
 
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
   if (fused) {
@@ -212,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       }
     }
     tc::named_sync(4, kCThreads);
-    const bool rin = !rstaged || await(&bars[kBarRouter], tb, a.status);
+    const bool rin = !rstaged || await(&bars[kBarRouter], tb, a.status, a.wait_ns);
     const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + g.off_act);
     for (int task = warp; task < a.T * rne; task += kCWarps) {
       const int t = task / rne, q = task - t * rne;
@@ -223,14 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
     }
     tc::named_sync(4, kCThreads);
-    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, bar_target(1), tb, a.status);
+    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, bar_target(1), tb, a.status, a.wait_ns);
     tc::named_sync(4, kCThreads);
     const bool have_logits = tb.flags[2] != 0;
     unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
     for (int t = 0; t < a.T; ++t) {
       int my_e = 0;
       float my_l = 0.0f;
-      if (have_logits) rt::topk_block<kCWarps, 4>(a.logits + (size_t)t * a.E, a.E, a.k, fin, my_e, my_l);
+      if (have_logits) rt::topk_block_fast<kCWarps, 4>(a.logits + (size_t)t * a.E, a.E, a.k, fin, my_e, my_l);
       if (warp == 0) {
         const float wgt = rt::topk_weight(lane, a.k, my_l);
         if (lane < a.k) {
@@ -291,11 +290,72 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   }
   asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // x staged, records in place
 
-  // gate/up + SwiGLU: warp w takes a contiguous block of the CTA's row pairs
-  // and works on up to kRows of them (rows of one pair) at a time, so that
-  // each load of x from shared memory serves them all.  Per row, the sums run
-  // in the same order as for a single row.
+  // gate/up + SwiGLU.
   const int n1 = share_lo(blockIdx.x + 1, (int)g.R1, g.grid) - share_lo(blockIdx.x, (int)g.R1, g.grid);
+  if constexpr (UPR > 0 && UPR <= 96) {
+    // Rows dealt round-robin over the compute warps in the CTA's row order, so
+    // that every warp has a row of each piece as the pieces land (the pieces
+    // land one after the other, in the order they were issued).  Lane j keeps
+    // x of units j, j + 32, j + 64 (of the row's token) in registers and
+    // takes those units of the gate and the up row; the lane sums run in unit
+    // order and are combined by an xor butterfly, a fixed order per row.
+    constexpr int UPL = (UPR + 31) / 32;
+    uint4 xr[UPL][4];
+    int xt = -1;
+    bool scales_in = false;
+    for (int q = warp; q < n1; q += kCWarps) {
+      int s = 0;
+      while (s + 1 < tb.nseg1 && tb.sq0[s + 1] <= q) ++s;
+      int pa = 0;
+      while (pa + 1 < tb.npieces && tb.pq0[pa + 1] <= q) ++pa;
+      const int p = tb.sp[s], t = p / a.k;
+      bool ok = tb.recs[p] != nullptr;
+      if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status, a.wait_ns);
+      if (ok) ok = await(&bars[pa], tb, a.status, a.wait_ns);
+      if (t != xt) {
+        xt = t;
+        const uint4* xt4 = act + (size_t)t * 4 * UPR;
+#pragma unroll
+        for (int i = 0; i < UPL; ++i) {
+          const int u = lane + 32 * i;
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) xr[i][wi] = u < UPR ? xt4[wi * UPR + u] : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      float gsum = 0.f, usum = 0.f;
+      if (ok) {
+        const uint8_t* grow = codes1 + tb.poff[pa] + (size_t)(q - tb.pq0[pa]) * (a.H / 2);
+        const uint8_t* urow = grow + (size_t)tb.pn[pa] * (a.H / 2);
+        const uint8_t* gsr = scales1 + tb.gwo[s] + (size_t)(q - tb.sq0[s]) * (a.H / G);
+        const uint8_t* usr = scales1 + tb.uwo[s] + (size_t)(q - tb.sq0[s]) * (a.H / G);
+#pragma unroll
+        for (int i = 0; i < UPL; ++i) {
+          const int u = lane + 32 * i;
+          if (u < UPR) {
+            gsum += dm::unit_dot_hx<FMT>(*reinterpret_cast<const uint4*>(grow + 16 * u),
+                                         dm::scale_bits<FMT>(gsr + sstep * u), xr[i]);
+            usum += dm::unit_dot_hx<FMT>(*reinterpret_cast<const uint4*>(urow + 16 * u),
+                                         dm::scale_bits<FMT>(usr + sstep * u), xr[i]);
+          }
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        gsum += __shfl_xor_sync(0xffffffffu, gsum, d);
+        usum += __shfl_xor_sync(0xffffffffu, usum, d);
+      }
+      if (lane == 0) {
+        const float ts = tb.tsc[t];
+        const float gv = gsum * ts, uv = usum * ts;
+        a.hws[(size_t)p * a.I + tb.si0[s] + (q - tb.sq0[s])] =
+            ok ? gv / (1.0f + expf(-gv)) * uv : __uint_as_float(0x7FC00000u);
+      }
+    }
+  } else {
+  // Other shapes: warp w takes a contiguous block of the CTA's row pairs and
+  // works on up to kRows of them (rows of one pair) at a time, so that each
+  // load of x from shared memory serves them all.  Per row, the sums run in
+  // the same order as for a single row.
   constexpr int kRows = 3;
   const int per_warp = (n1 + kCWarps - 1) / kCWarps;
   const int q_end = min(n1, (warp + 1) * per_warp);
@@ -312,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     const int pb = qb + nr - 1 < tb.pq0[pa] + tb.pn[pa] ? pa : pa + 1;
     const int p = tb.sp[s], t = p / a.k;
     bool ok = tb.recs[p] != nullptr;
-    if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status);
-    if (ok) ok = await(&bars[pa], tb, a.status);
-    if (ok && pb != pa) ok = await(&bars[pb], tb, a.status);
+    if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status, a.wait_ns);
+    if (ok) ok = await(&bars[pa], tb, a.status, a.wait_ns);
+    if (ok && pb != pa) ok = await(&bars[pb], tb, a.status, a.wait_ns);
     float gs[kRows], us[kRows];
     uint32_t goff[kRows], uoff[kRows];
 #pragma unroll
@@ -378,11 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     }
     qb += nr;
   }
+  }
   // grid barrier among the compute threads of every CTA (the h rows written
   // above are published by thread 0's release arrival)
   tc::named_sync(1, kCThreads);
   if (threadIdx.x == 0)
-    tb.flags[1] = grid_sync_thread(a.bar, bar_target(fused ? 2u : 1u), tb, a.status);
+    tb.flags[1] = grid_sync_thread(a.bar, bar_target(fused ? 2u : 1u), tb, a.status, a.wait_ns);
   tc::named_sync(1, kCThreads);
 
   // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats
@@ -432,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const int tasks_per_pass = 32 / L;
   const int ntask = nz * a.k;
   const int npass = (ntask + tasks_per_pass - 1) / tasks_per_pass;
-  const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], tb, a.status);
+  const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], tb, a.status, a.wait_ns);
   const int sub = lane & (L - 1);
   float* part = reinterpret_cast<float*>(smem + g.off_part);  // [row][expert]
   for (int ps = warp; ps < npass; ps += kCWarps) {
@@ -481,21 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   __syncthreads();
 }
 
-// Raises a kernel's dynamic shared-memory limit once per instantiation (the
-// attribute call is not repeated, so later launches can be captured).
-template <typename K>
-bool grant_smem(K kernel, size_t bytes, size_t* granted) {
-  if (bytes <= 48 * 1024 || bytes <= *granted) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
-    return false;
-  *granted = bytes;
-  return true;
-}
-
 template <int FMT, int UPR, int UPDR>
 int launch_shape(const DecodeOneshotArgs& a, int grid, size_t smem, cudaStream_t stream) {
-  static size_t granted = 0;
-  if (!grant_smem(oneshot_kernel<FMT, UPR, UPDR>, smem, &granted)) return MOE_ERR_CUDA;
+  static SmemGrant granted;  // per device; also checks that one CTA fits on an SM
+  if (!grant_smem(oneshot_kernel<FMT, UPR, UPDR>, smem, granted, kThreads)) return MOE_ERR_CUDA;
   return launch_pdl(oneshot_kernel<FMT, UPR, UPDR>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
@@ -511,8 +561,27 @@ int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
 }  // namespace os
 }  // namespace moe
 
-int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream) {
+namespace {
+// Test hooks of the bounded waits (moe_test_set_wait_limit): 0 = defaults.
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<unsigned> g_barrier_extra{0};
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+}  // namespace
+
+int launch_decode_oneshot(const DecodeOneshotArgs& a0, int fmt, int grid, void* stream) {
   cudaStream_t st = (cudaStream_t)stream;
+  DecodeOneshotArgs a = a0;
+  const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
+  a.wait_ns = w ? w : kDefaultWaitNs;
+  a.barrier_extra = g_barrier_extra.load(std::memory_order_relaxed);
   return fmt == MOE_FMT_NVFP4 ? moe::os::launch_fmt<MOE_FMT_NVFP4>(a, grid, st)
                               : moe::os::launch_fmt<MOE_FMT_MXFP4>(a, grid, st);
+}
+
+extern "C" int moe_test_set_wait_limit(unsigned long long wait_ns, int barrier_extra_arrivals) {
+  if (barrier_extra_arrivals < 0 || barrier_extra_arrivals > 1) return MOE_ERR_INVALID_ARG;
+  if (wait_ns != 0 && (wait_ns < 1000ull || wait_ns > 10000000000ull)) return MOE_ERR_INVALID_ARG;
+  g_wait_ns.store(wait_ns, std::memory_order_relaxed);
+  g_barrier_extra.store((unsigned)barrier_extra_arrivals, std::memory_order_relaxed);
+  return MOE_OK;
 }

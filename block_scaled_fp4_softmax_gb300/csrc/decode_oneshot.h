@@ -289,5 +289,9 @@ struct DecodeOneshotArgs {
   int32_t* idx_out;
   float* w_out;
   moe::os::Geo geo;  // the plan's geometry, computed by the host for the launch's grid
+  // limit of every bounded wait (ns), and arrivals each grid barrier expects
+  // beyond the grid (0; a test sets 1 to make the barriers run out)
+  unsigned long long wait_ns;
+  unsigned barrier_extra;
 };
 int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream);

@@ -6,28 +6,36 @@
 // through a layer at once, so each expert's weights are read once per layer
 // (not once per prompt chunk).  Here the routed (token, slot) pairs are
 // bucketed by expert on the device, and each expert's tokens form the N side
-// of a BF16 MMA whose M side is 128 weight rows dequantised from the FP4
-// record on the fly:
+// of an MMA whose M side is 128 weight rows dequantised from the FP4 record on
+// the fly:
 //
 //   phase 0  (gate/up):  Dg = Wg[128 x H] . X^T,  Du = Wu[128 x H] . X^T  (TMEM)
 //                        h  = BF16(silu(Dg) * Du)  -> workspace, rows sorted by expert
 //   phase 1  (down):     D  = Wd[128 x I] . h^T                            (TMEM)
 //                        y[t] += w * D  (FP32 atomic add)
 //
-// One persistent CTA per SM walks a static list of tiles (expert, token tile,
-// weight-row tile).  Warp roles:
+// One persistent CTA per SM walks a static list of tiles (token tile of one
+// expert, 128-row weight tile).  Per k-step of 64 elements three rings meet:
+//   raw ring  (per producer thread, 8-12 steps deep): the thread's own FP4
+//             codes and scale word, fetched with cp.async well ahead of use --
+//             the only operand that comes from HBM, so the deep ring is cheap
+//             (FP4 is a quarter of the BF16 bytes);
+//   A ring    (2 stages): the dequantised 128 x 64 weight tile(s), FP16 or
+//             BF16, 128-byte swizzled, written by the producers;
+//   B ring    (5-6 stages): the 64-element slice of up to 128 token rows (x or
+//             h), gathered with cp.async from the L2.
+// The accumulators are double-buffered in TMEM, so the epilogue of one tile
+// overlaps the mainloop of the next.  Warp roles:
 //   warp 0          TMEM allocation; lane 0 issues tcgen05.mma and commits
-//   warps 1-2       gather B rows (tokens' x or h) with cp.async into
-//                   128-byte-swizzled shared memory; each thread owns two rows
-//                   and resolves their source addresses once per tile
-//   warps 3-10      load FP4 codes + block scales, convert e2m1 x scale to BF16
-//                   (exact) and store the A tile, 128-byte swizzled
-//   warps 11-14     epilogue: tcgen05.ld from TMEM, SwiGLU or weighted combine
+//   warps 1-2       B gatherers: each thread owns two token rows of the tile
+//   warps 3-10      producers: fetch + dequantise A (e2m1 x scale, exact)
+//   warps 11-14     epilogue: tcgen05.ld, SwiGLU or the weighted combine
 // Every mbarrier wait is bounded by the global timer; a wait that runs out sets
-// MOE_DEV_TIMEOUT and the CTA drains and exits.
+// MOE_DEV_TIMEOUT, the CTA drains its copies and exits.
 #include <algorithm>
 
 #include "common.cuh"
+#include "decode_math.cuh"
 #include "tcgen05.cuh"
 
 namespace {
@@ -35,22 +43,21 @@ namespace {
 using namespace moe::tc;
 
 constexpr int BM = 128;      // weight rows per tile (MMA M)
-constexpr int BK = 64;       // K elements per stage (128 bytes of BF16)
+constexpr int BK = 64;       // K elements per step (128 bytes of FP16/BF16)
 constexpr int BN = 128;      // max tokens per tile (MMA N, padded to 16)
 constexpr int kThreads = 480;
 constexpr int kLoaderThreads = 64;     // warps 1-2: two B rows each
 constexpr int kProducerThreads = 256;  // warps 3-10
 constexpr int kEpiThreads = 128;       // warps 11-14
 constexpr int kProdWarp0 = 3, kEpiWarp0 = 11;
-constexpr int kPrefetch = 4;           // k-steps of FP4 codes a producer holds in registers
-constexpr int kLoaderDepth = 2;        // cp.async groups a loader keeps in flight
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 struct GroupedArgs {
-  const uint16_t* x;        // [T, H] BF16 (FP16 copy when use_f16: see below)
+  const uint16_t* x;        // [T, H]: FP16 (x * 2^e_t) for NVFP4 phase 0, else BF16
+  const float* xscale;      // [T] 2^-e_t (NVFP4 phase 0), else NULL
   const int32_t* pairs;     // [P] pair ids sorted by expert
-  const int32_t* offsets;   // [E+1]
-  const int32_t* ntile_off; // [E+1] exclusive scan of ceil(count/BN)
+  const int4* tiles;        // [G] token tiles: {expert, first sorted row, rows, 0}
+  const int32_t* ntiles;    // [1] G
   const float* weights;     // [T*k]
   const void* const* ptrs;  // [E] record pointers
   int E, k, H, I;
@@ -60,10 +67,10 @@ struct GroupedArgs {
 };
 
 // Phase 0 of NVFP4 runs as an FP16 x FP16 MMA: e2m1 x E4M3 scale is exact in
-// FP16 and takes one convert plus one packed multiply per pair; x is
-// converted once to FP16 (exact for BF16 values of magnitude in [2^-14,
-// 65504]; smaller ones round to FP16 subnormals, at most 2^-25 away).
-// MXFP4 scales (2^-127..2^127) do not fit FP16, so MXFP4 stays BF16.
+// FP16 and takes one convert plus one packed multiply per pair; x is scaled
+// per token by a power of two into FP16's range (exact).  MXFP4 scales
+// (2^-127..2^127) do not fit FP16, so MXFP4 stays BF16; phase 1 is BF16
+// because its B operand, the SwiGLU intermediate, is BF16.
 template <int FMT, int PHASE>
 struct OperandF16 {
   static constexpr bool value = FMT == MOE_FMT_NVFP4 && PHASE == 0;
@@ -71,39 +78,31 @@ struct OperandF16 {
 
 template <int PHASE>
 struct Cfg {
-  static constexpr int NA = PHASE == 0 ? 2 : 1;           // A matrices per tile
-  static constexpr int STAGES = PHASE == 0 ? 4 : 6;
-  static constexpr int A_BYTES = BM * BK * 2;             // 16 KB
-  static constexpr int B_BYTES = BN * BK * 2;             // 16 KB
-  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
-  static constexpr int TMEM_COLS = NA * BN;               // 256 or 128
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*bars*/ +
-                                 2 * BN * 8 /*per-column token and weight, two tiles*/;
+  static constexpr int NA = PHASE == 0 ? 2 : 1;             // A matrices per tile
+  static constexpr int UNITS = NA * BM * BK / 32 / kProducerThreads;  // 16-B code units per producer per step
+  static constexpr int A_STAGES = 2;
+  static constexpr int B_STAGES = PHASE == 0 ? 5 : 6;
+  static constexpr int RAW_DEPTH = PHASE == 0 ? 8 : 12;
+  static constexpr int A_BYTES = BM * BK * 2;               // 16 KB per matrix
+  static constexpr int B_BYTES = BN * BK * 2;               // 16 KB
+  static constexpr int RAW_STEP = kProducerThreads * (UNITS * 16 + 4);
+  static constexpr int ACC_COLS = NA * BN;                  // one accumulator buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;            // double-buffered: 512 or 256
+  static constexpr size_t OFF_A = 0;
+  static constexpr size_t OFF_B = OFF_A + (size_t)A_STAGES * NA * A_BYTES;
+  static constexpr size_t OFF_RAW = OFF_B + (size_t)B_STAGES * B_BYTES;
+  static constexpr size_t OFF_BARS = OFF_RAW + (size_t)RAW_DEPTH * RAW_STEP;
+  static constexpr size_t BAR_BYTES = 512;
+  static constexpr size_t OFF_COLS = OFF_BARS + BAR_BYTES;  // [2][BN] token, weight, x scale
+  static constexpr size_t SMEM = 1024 /*align*/ + OFF_COLS + 2 * BN * 12;
 };
+static_assert(Cfg<0>::UNITS == 2 && Cfg<1>::UNITS == 1, "producer split");
+static_assert(Cfg<0>::SMEM <= 232448 && Cfg<1>::SMEM <= 232448, "shared memory");
 
-struct TileInfo {
-  int e, row0, count, mt;  // expert, first sorted-pair row, tokens, weight-row tile
-};
-
-// tile id -> (expert, token tile, weight-row tile); experts found by binary
-// search over the exclusive scan of their token-tile counts.
-__device__ __forceinline__ TileInfo tile_info(const GroupedArgs& a, int tile, int MT) {
-  TileInfo ti;
+__device__ __forceinline__ int4 tile_of(const GroupedArgs& a, int tile, int MT, int& mt) {
   const int g = tile / MT;
-  ti.mt = tile - g * MT;
-  int lo = 0, hi = a.E;  // find e with ntile_off[e] <= g < ntile_off[e+1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(a.ntile_off + mid) <= g) lo = mid;
-    else hi = mid;
-  }
-  ti.e = lo;
-  const int nt = g - __ldg(a.ntile_off + lo);
-  const int beg = __ldg(a.offsets + lo);
-  const int cnt = __ldg(a.offsets + lo + 1) - beg;
-  ti.row0 = beg + nt * BN;
-  ti.count = min(BN, cnt - nt * BN);
-  return ti;
+  mt = tile - g * MT;
+  return __ldg(a.tiles + g);
 }
 
 __device__ __forceinline__ const uint8_t* tile_record(const GroupedArgs& a, int e) {
@@ -112,10 +111,20 @@ __device__ __forceinline__ const uint8_t* tile_record(const GroupedArgs& a, int 
   return r;
 }
 
+// cp.async of 16 or 4 bytes (L2 only for 16; the L2 fetches the surrounding
+// 256 bytes, so the following k-steps of the same row hit in L2).
+__device__ __forceinline__ void cp16_l2pf(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // 32 e2m1 codes (16 bytes) x one or two block scales -> 32 BF16 (exact), as
-// four 16-byte chunks.
+// four 16-byte chunks.  NVFP4: scale bytes s0 (elements 0-15) and s1 (16-31)
+// in the low 16 bits of sbits; MXFP4: one UE8M0 byte.
 template <int FMT>
-__device__ __forceinline__ void dequant_unit(uint4 q, uint32_t sbits, bool poison, uint4 (&out)[4]) {
+__device__ __forceinline__ void dequant_unit_bf16(uint4 q, uint32_t sbits, bool poison, uint4 (&out)[4]) {
   float s0, s1;
   if (FMT == MOE_FMT_NVFP4) {
     const float2 s = moe::e4m3x2_to_f32x2(sbits);
@@ -129,45 +138,14 @@ __device__ __forceinline__ void dequant_unit(uint4 q, uint32_t sbits, bool poiso
 #pragma unroll
   for (int wi = 0; wi < 4; ++wi) {
     const float s = wi < 2 ? s0 : s1;
-    uint32_t o[4];
+    uint32_t h[4], o[4];
+    moe::dm::cvt_e2m1x8(w[wi], h);
 #pragma unroll
     for (int bi = 0; bi < 4; ++bi) {
-      const uint32_t h2 = moe::e2m1x2_to_f16x2((w[wi] >> (8 * bi)) & 0xFFu);
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      uint32_t b;
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(f.y * s), "f"(f.x * s));
-      o[bi] = b;
+      const float2 f = __half22float2(moe::dm::as_h2(h[bi]));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[bi]) : "f"(f.y * s), "f"(f.x * s));
     }
     out[wi] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-// Asks the L2 to fetch [src, src + bytes) ahead of use (no data returned).
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// One tile's weight rows are one contiguous block per matrix (codes and
-// scales); prefetch them into L2 so the per-k-step loads hit in L2.
-template <int FMT, int PHASE>
-__device__ __forceinline__ void prefetch_tile(const GroupedArgs& a, int tile, int MT, int total_tiles) {
-  if (tile >= total_tiles) return;
-  const TileInfo ti = tile_info(a, tile, MT);
-  const uint8_t* rec = tile_record(a, ti.e);
-  if (rec == nullptr) return;
-  const moe::RecordOffsets ro = moe::record_offsets(a.H, a.I, FMT);
-  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
-  const int K = PHASE == 0 ? a.H : a.I;
-  const size_t row0 = (size_t)ti.mt * BM;
-  const uint32_t cbytes = (uint32_t)(BM * (K / 2)), sbytes = (uint32_t)(BM * (K / G));
-  if (PHASE == 0) {
-    prefetch_l2(rec + ro.gate + row0 * (K / 2), cbytes);
-    prefetch_l2(rec + ro.up + row0 * (K / 2), cbytes);
-    prefetch_l2(rec + ro.gate_s + row0 * (K / G), sbytes);
-    prefetch_l2(rec + ro.up_s + row0 * (K / G), sbytes);
-  } else {
-    prefetch_l2(rec + ro.down + row0 * (K / 2), cbytes);
-    prefetch_l2(rec + ro.down_s + row0 * (K / G), sbytes);
   }
 }
 
@@ -183,12 +161,10 @@ __device__ __forceinline__ void dequant_unit_f16(uint4 q, uint32_t sbits, bool p
 #pragma unroll
   for (int wi = 0; wi < 4; ++wi) {
     const uint32_t sc = wi < 2 ? sc0 : sc1;
-    uint32_t o[4];
+    uint32_t h[4], o[4];
+    moe::dm::cvt_e2m1x8(w[wi], h);
 #pragma unroll
-    for (int bi = 0; bi < 4; ++bi) {
-      const uint32_t h2 = moe::e2m1x2_to_f16x2((w[wi] >> (8 * bi)) & 0xFFu);
-      asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[bi]) : "r"(h2), "r"(sc));
-    }
+    for (int bi = 0; bi < 4; ++bi) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[bi]) : "r"(h[bi]), "r"(sc));
     out[wi] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -197,37 +173,48 @@ template <int FMT, int PHASE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
   constexpr bool kF16 = OperandF16<FMT, PHASE>::value;
   using C = Cfg<PHASE>;
+  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
-  uint64_t* tab_ready = drain + 1;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tab_ready + 2);
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sRaw = smem + C::OFF_RAW;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);  // [A_STAGES]
+  uint64_t* a_empty = a_full + C::A_STAGES;                             // [A_STAGES]
+  uint64_t* b_full = a_empty + C::A_STAGES;                             // [B_STAGES]
+  uint64_t* b_empty = b_full + C::B_STAGES;                             // [B_STAGES]
+  uint64_t* acc_full = b_empty + C::B_STAGES;                           // [2]
+  uint64_t* acc_empty = acc_full + 2;                                   // [2]
+  uint64_t* tab_ready = acc_empty + 2;                                  // [2]
+  uint64_t* drain = tab_ready + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* col_tok = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + 256);  // [2][BN]
-  float* col_w = reinterpret_cast<float*>(col_tok + 2 * BN);                        // [2][BN]
+  int* col_tok = reinterpret_cast<int*>(smem + C::OFF_COLS);  // [2][BN]
+  float* col_w = reinterpret_cast<float*>(col_tok + 2 * BN);  // [2][BN]
+  float* col_xs = col_w + 2 * BN;                             // [2][BN]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = PHASE == 0 ? a.H : a.I;  // contraction length
   const int KSTEPS = K / BK;
   const int MT = (PHASE == 0 ? a.I : a.H) / BM;
-  const int total_tiles = __ldg(a.ntile_off + a.E) * MT;
+  const int total_tiles = __ldg(a.ntiles) * MT;
   const moe::RecordOffsets ro = moe::record_offsets(a.H, a.I, FMT);
-  constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], kLoaderThreads + kProducerThreads);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < C::A_STAGES; ++s) {
+      mbar_init(&a_full[s], kProducerThreads);
+      mbar_init(&a_empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kEpiThreads);
+    for (int s = 0; s < C::B_STAGES; ++s) {
+      mbar_init(&b_full[s], kLoaderThreads);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiThreads);
+      mbar_init(&tab_ready[b], kEpiThreads);
+    }
     mbar_init(drain, 1);
-    mbar_init(&tab_ready[0], kEpiThreads);
-    mbar_init(&tab_ready[1], kEpiThreads);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -249,38 +236,43 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     if (lane == 0) {
       bool ok = true;
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
-        const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
-        const int n_mma = max(16, (ti.count + 15) & ~15);
+        int mt;
+        const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
+        const int n_mma = max(16, (ti.z + 15) & ~15);
         const uint32_t idesc = kF16 ? idesc_f16_f32(BM, n_mma) : idesc_bf16_f32(BM, n_mma);
-        if (*abort_flag || !mbar_wait(acc_empty, (lt & 1) ^ 1, globaltimer() + kWaitNs)) {
+        const int buf = lt & 1;
+        if (*abort_flag || !mbar_wait(&acc_empty[buf], ((lt >> 1) & 1) ^ 1, globaltimer() + kWaitNs)) {
           fail();
           ok = false;
           break;
         }
         fence_after_sync();
+        const uint32_t d_tmem = tmem + (uint32_t)(buf * C::ACC_COLS);
         for (int ks = 0; ks < KSTEPS; ++ks) {
           const int gs = lt * KSTEPS + ks;
-          const int stage = gs % C::STAGES;
-          if (*abort_flag || !mbar_wait(&full[stage], (gs / C::STAGES) & 1, globaltimer() + kWaitNs)) {
+          const int as = gs % C::A_STAGES, bs = gs % C::B_STAGES;
+          if (*abort_flag || !mbar_wait(&a_full[as], (gs / C::A_STAGES) & 1, globaltimer() + kWaitNs) ||
+              !mbar_wait(&b_full[bs], (gs / C::B_STAGES) & 1, globaltimer() + kWaitNs)) {
             fail();
             ok = false;
             break;
           }
           fence_after_sync();
-          const uint32_t sbase = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = sbase + C::NA * C::A_BYTES;
+          const uint32_t a_addr = smem_u32(sA + (size_t)as * C::NA * C::A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + (size_t)bs * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
 #pragma unroll
             for (int m = 0; m < C::NA; ++m) {
-              const uint64_t adesc = sw128_kmajor_desc(sbase + m * C::A_BYTES + kk * 32);
-              mma_bf16(tmem + m * BN, adesc, bdesc, idesc, (ks | kk) != 0);
+              const uint64_t adesc = sw128_kmajor_desc(a_addr + m * C::A_BYTES + kk * 32);
+              mma_bf16(d_tmem + m * BN, adesc, bdesc, idesc, (ks | kk) != 0);
             }
           }
-          mma_commit(&empty[stage]);
+          mma_commit(&a_empty[as]);
+          mma_commit(&b_empty[bs]);
         }
-        if (ok) mma_commit(acc_full);
+        if (ok) mma_commit(&acc_full[buf]);
       }
       // wait for every MMA issued above before the CTA may release TMEM
       mma_commit(drain);
@@ -288,40 +280,47 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     }
     __syncwarp();
   } else if (warp < kProdWarp0) {
-    // ------------------------------------------------------------- B loaders
-    const int lid = threadIdx.x - 32;  // 0..63; rows lid and lid + 64
-    int pending = 0;                    // steps issued but not yet signalled
+    // ------------------------------------------------------------- B gatherers
+    // Thread lid owns rows lid and lid + 64 of every tile's B slice; it keeps
+    // up to B_STAGES - 1 steps of cp.async in flight and signals a stage full
+    // once its own copies of that stage have landed.
+    constexpr int kDepth = C::B_STAGES - 1;
+    const int lid = threadIdx.x - 32;
+    int pending = 0;
     int cur_tile = -1;
     const uint16_t* src_row[2] = {a.x, a.x};
     uint32_t src_bytes[2] = {0, 0};
+    bool alive = true;
     for (int gs = 0; gs < my_steps; ++gs) {
       const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
-      const int stage = gs % C::STAGES;
+      const int bs = gs % C::B_STAGES;
       if (lt != cur_tile) {
         cur_tile = lt;
-        const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
-        const int n_rows = max(16, (ti.count + 15) & ~15);
+        int mt;
+        const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
+        const int n_rows = max(16, (ti.z + 15) & ~15);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int n = lid + 64 * h;
-          src_bytes[h] = n < ti.count ? 16u : 0u;
+          src_bytes[h] = n < ti.z ? 16u : 0u;  // rows past the tile's tokens are zero-filled
           src_row[h] = a.x;
-          if (n < ti.count) {
+          if (n < ti.z) {
             if (PHASE == 0) {
-              const int p = __ldg(a.pairs + ti.row0 + n);
+              const int p = __ldg(a.pairs + ti.y + n);
               src_row[h] = a.x + (size_t)(p / a.k) * a.H;
             } else {
-              src_row[h] = a.hbuf + (size_t)(ti.row0 + n) * a.I;
+              src_row[h] = a.hbuf + (size_t)(ti.y + n) * a.I;
             }
           }
           if (n >= n_rows) src_bytes[h] = 0xFFFFFFFFu;  // row not part of this tile's MMA
         }
       }
-      if (*abort_flag || !mbar_wait(&empty[stage], ((gs / C::STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
+      if (*abort_flag || !mbar_wait(&b_empty[bs], ((gs / C::B_STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
         fail();
+        alive = false;
         break;
       }
-      const uint32_t b_addr = smem_u32(smem + stage * C::STAGE_BYTES + C::NA * C::A_BYTES);
+      const uint32_t b_addr = smem_u32(sB + (size_t)bs * C::B_BYTES);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (src_bytes[h] == 0xFFFFFFFFu) continue;
@@ -329,156 +328,169 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
         const uint16_t* src = src_row[h] + (src_bytes[h] ? ks * BK : 0);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          cp_async16(b_addr + n * 128 + ((ch ^ (n & 7)) << 4), src + (src_bytes[h] ? ch * 8 : 0),
-                     src_bytes[h]);
+          cp_async16(b_addr + n * 128 + ((ch ^ (n & 7)) << 4), src + (src_bytes[h] ? ch * 8 : 0), src_bytes[h]);
       }
       cp_async_commit();
       ++pending;
-      if (pending > kLoaderDepth) {
-        cp_async_wait<kLoaderDepth>();
+      if (pending > kDepth) {
+        cp_async_wait<kDepth>();
         fence_proxy_async();
-        mbar_arrive(&full[(gs - kLoaderDepth) % C::STAGES]);
+        mbar_arrive(&b_full[(gs - kDepth) % C::B_STAGES]);
         --pending;
       }
     }
     cp_async_wait<0>();
     fence_proxy_async();
-    if (!*abort_flag) {
-      for (int gs = my_steps - pending; gs < my_steps; ++gs) mbar_arrive(&full[gs % C::STAGES]);
+    if (alive && !*abort_flag) {
+      for (int gs = my_steps - pending; gs < my_steps; ++gs) mbar_arrive(&b_full[gs % C::B_STAGES]);
     }
   } else if (warp < kEpiWarp0) {
-    // ------------------------------------------------------ A dequant producers
+    // ------------------------------------------------------ A producers
+    // Phase 0: thread (matrix m, row r) dequantises 64 elements per step (two
+    // 16-byte code units, one 4-byte scale word); phase 1: thread (row r,
+    // half) dequantises 32 elements (one unit).  Each thread fetches exactly
+    // the bytes it will convert into its private slot of the raw ring,
+    // RAW_DEPTH steps ahead, and waits for them with its own cp.async groups.
     const int pid = threadIdx.x - kProdWarp0 * 32;  // 0..255
-    const int r = pid >> 1, half = pid & 1;
-    uint4 q[kPrefetch][C::NA];
-    uint32_t sb[kPrefetch][C::NA];
-    const uint8_t* rec_of[kPrefetch];
-    // issue the loads of step gs into slot gs % kPrefetch
-    int cached_lt = -1;
-    const uint8_t* cached_rec = nullptr;
-    size_t cached_row = 0;
-    auto issue_slot = [&](int gs, const int slot) {
-      const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
-      if (lt != cached_lt) {
-        cached_lt = lt;
-        const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
-        cached_rec = tile_record(a, ti.e);
-        cached_row = (size_t)ti.mt * BM + r;
-        if (pid == 0) {  // this tile (first time) and the next one into L2
-          if (lt == 0) prefetch_tile<FMT, PHASE>(a, blockIdx.x, MT, total_tiles);
-          prefetch_tile<FMT, PHASE>(a, blockIdx.x + (lt + 1) * gridDim.x, MT, total_tiles);
+    const int m = PHASE == 0 ? pid >> 7 : 0;
+    const int r = PHASE == 0 ? (pid & 127) : (pid >> 1);
+    const int half = PHASE == 0 ? 0 : (pid & 1);
+    const int c0 = half * 32;                      // first element of the thread inside the step
+    const size_t coff = PHASE == 0 ? (m == 0 ? ro.gate : ro.up) : ro.down;
+    const size_t soff = PHASE == 0 ? (m == 0 ? ro.gate_s : ro.up_s) : ro.down_s;
+    const uint32_t raw0 = smem_u32(sRaw);
+    // tile lookups for the fetches (RAW_DEPTH steps ahead of the conversions)
+    int f_tile = -1;
+    const uint8_t* f_rec = nullptr;
+    size_t f_row = 0;
+    auto fetch = [&](int gs) {  // step gs -> raw slot gs % RAW_DEPTH, then commit
+      if (gs < my_steps) {
+        const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
+        if (lt != f_tile) {
+          f_tile = lt;
+          int mt;
+          const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
+          f_rec = tile_record(a, ti.x);
+          f_row = (size_t)mt * BM + r;
         }
-      }
-      const uint8_t* rec = cached_rec;
-      rec_of[slot] = rec;
-      if (rec == nullptr) return;
-      const size_t row = cached_row;
+        const uint32_t slot = raw0 + (uint32_t)((gs % C::RAW_DEPTH) * C::RAW_STEP);
+        if (f_rec != nullptr) {
+          const uint8_t* cp = f_rec + coff + f_row * (size_t)(K / 2) + (size_t)(ks * BK + c0) / 2;
 #pragma unroll
-      for (int m = 0; m < C::NA; ++m) {
-        size_t coff, soff;
-        if (PHASE == 0) {
-          coff = m == 0 ? ro.gate : ro.up;
-          soff = m == 0 ? ro.gate_s : ro.up_s;
-        } else {
-          coff = ro.down;
-          soff = ro.down_s;
+          for (int u = 0; u < C::UNITS; ++u) cp16_l2pf(slot + (u * kProducerThreads + pid) * 16, cp + 16 * u);
+          // the aligned 4-byte word holding the thread's scale bytes (records
+          // are a multiple of 4 bytes long, so the word stays inside it)
+          const size_t so = soff + f_row * (size_t)(K / G) + (size_t)(ks * BK + c0) / G;
+          cp4(slot + C::UNITS * kProducerThreads * 16 + pid * 4, f_rec + (so & ~(size_t)3));
         }
-        const uint8_t* cp = rec + coff + row * (K / 2) + ks * (BK / 2) + half * 16;
-        const uint8_t* sp = rec + soff + row * (K / G) + (ks * BK + half * 32) / G;
-        q[slot][m] = moe::ldg_stream_l2pf(cp);
-        sb[slot][m] = FMT == MOE_FMT_NVFP4 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(sp))
-                                           : (uint32_t)__ldg(sp);
       }
+      cp_async_commit();  // one group per step, empty or not, so the group count stays aligned
     };
-#pragma unroll
-    for (int slot = 0; slot < kPrefetch; ++slot)
-      if (slot < my_steps) issue_slot(slot, slot);
-    bool alive = true;
-    // unrolled by the prefetch depth so every register slot index is static
-    for (int gs0 = 0; gs0 < my_steps && alive; gs0 += kPrefetch) {
-#pragma unroll
-      for (int slot = 0; slot < kPrefetch; ++slot) {
-        const int gs = gs0 + slot;
-        if (gs >= my_steps || !alive) break;
-        const int stage = gs % C::STAGES;
-        if ((gs % KSTEPS) == 0 && pid == 0) {
-          const TileInfo ti = tile_info(a, blockIdx.x + (gs / KSTEPS) * gridDim.x, MT);
-          if (tile_record(a, ti.e) == nullptr)
-            moe::status_or(a.st, a.ptrs[ti.e] == nullptr ? MOE_DEV_NULL_EXPERT : MOE_DEV_MISALIGNED);
-        }
-        if (*abort_flag || !mbar_wait(&empty[stage], ((gs / C::STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
-          fail();
-          alive = false;
-          break;
-        }
-        uint8_t* sa = smem + stage * C::STAGE_BYTES;
-        const bool poison = rec_of[slot] == nullptr;
-#pragma unroll
-        for (int m = 0; m < C::NA; ++m) {
-          uint4 out[4];
-          if constexpr (kF16)
-            dequant_unit_f16(poison ? make_uint4(0, 0, 0, 0) : q[slot][m], poison ? 0u : sb[slot][m],
-                             poison, out);
-          else
-            dequant_unit<FMT>(poison ? make_uint4(0, 0, 0, 0) : q[slot][m], poison ? 0u : sb[slot][m],
-                              poison, out);
-          uint8_t* row_base = sa + m * C::A_BYTES + r * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int ch = half * 4 + c;
-            *reinterpret_cast<uint4*>(row_base + ((ch ^ (r & 7)) << 4)) = out[c];
-          }
-        }
-        fence_proxy_async();
-        mbar_arrive(&full[stage]);
-        if (gs + kPrefetch < my_steps) issue_slot(gs + kPrefetch, slot);
+    for (int s = 0; s < C::RAW_DEPTH; ++s) fetch(s);
+    int c_tile = -1;
+    bool poison = false;
+    uint32_t sshift = 0;
+    for (int gs = 0; gs < my_steps; ++gs) {
+      const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
+      if (lt != c_tile) {
+        c_tile = lt;
+        int mt;
+        const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
+        const uint8_t* rec = tile_record(a, ti.x);
+        poison = rec == nullptr;
+        if (poison && pid == 0)
+          moe::status_or(a.st, a.ptrs[ti.x] == nullptr ? MOE_DEV_NULL_EXPERT : MOE_DEV_MISALIGNED);
       }
+      {
+        const size_t so = (size_t)r * (size_t)(K / G) + (size_t)(ks * BK + c0) / G;  // alignment only
+        sshift = (uint32_t)(so & 3u) * 8u;
+      }
+      // this step's raw bytes: the oldest of the RAW_DEPTH groups in flight
+      asm volatile("cp.async.wait_group %0;" ::"n"(C::RAW_DEPTH - 1) : "memory");
+      const uint8_t* slot = sRaw + (size_t)(gs % C::RAW_DEPTH) * C::RAW_STEP;
+      uint4 q[C::UNITS];
+#pragma unroll
+      for (int u = 0; u < C::UNITS; ++u)
+        q[u] = *reinterpret_cast<const uint4*>(slot + (u * kProducerThreads + pid) * 16);
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(slot + C::UNITS * kProducerThreads * 16 + pid * 4) >> sshift;
+      uint4 out[C::UNITS][4];
+#pragma unroll
+      for (int u = 0; u < C::UNITS; ++u) {
+        const uint4 qq = poison ? make_uint4(0u, 0u, 0u, 0u) : q[u];
+        const uint32_t sb = poison ? 0u : (FMT == MOE_FMT_NVFP4 ? (sw >> (16 * u)) & 0xFFFFu : (sw >> (8 * u)) & 0xFFu);
+        if constexpr (kF16) dequant_unit_f16(qq, sb, poison, out[u]);
+        else dequant_unit_bf16<FMT>(qq, sb, poison, out[u]);
+      }
+      const int as = gs % C::A_STAGES;
+      if (*abort_flag || !mbar_wait(&a_empty[as], ((gs / C::A_STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
+        fail();
+        break;
+      }
+      uint8_t* row_base = sA + (size_t)as * C::NA * C::A_BYTES + (size_t)m * C::A_BYTES + (size_t)r * 128;
+#pragma unroll
+      for (int u = 0; u < C::UNITS; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int ch = (c0 / 8) + u * 4 + c;  // 16-byte chunk of the 128-byte row
+          *reinterpret_cast<uint4*>(row_base + ((ch ^ (r & 7)) << 4)) = out[u][c];
+        }
+      fence_proxy_async();
+      mbar_arrive(&a_full[as]);
+      // the raw slot has been read and its values stored: refill it with the
+      // step RAW_DEPTH ahead
+      fetch(gs + C::RAW_DEPTH);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ------------------------------------------------------------- epilogue
     // A warp may only touch TMEM lanes 32*(warp % 4) .. +31.
     const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;           // accumulator row = weight row in tile
+    const int row = q4 * 32 + lane;               // accumulator row = weight row in tile
     const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
     const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
     for (int lt = 0; lt < my_tiles; ++lt) {
-      const TileInfo ti = tile_info(a, blockIdx.x + lt * gridDim.x, MT);
-      // per-column token and router weight, once per tile, double buffered: a
-      // thread can be at most one tile ahead of the slowest (acc_empty counts
-      // every epilogue thread), so tile lt never overwrites a table in use.
-      int* tok = col_tok + (lt & 1) * BN;
-      float* wcol = col_w + (lt & 1) * BN;
-      if (PHASE == 1) {
-        if (et < ti.count) {
-          const int p = __ldg(a.pairs + ti.row0 + et);
-          tok[et] = p / a.k;
-          wcol[et] = __ldg(a.weights + p);
-        }
-        mbar_arrive(&tab_ready[lt & 1]);
-        if (!mbar_wait(&tab_ready[lt & 1], (lt >> 1) & 1, globaltimer() + kWaitNs)) {
-          fail();
-          break;
-        }
+      int mt;
+      const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
+      const int buf = lt & 1;
+      // per-column token, router weight and x scale, once per tile, double
+      // buffered: a thread can be at most one tile ahead of the slowest
+      // (acc_empty counts every epilogue thread), so tile lt never overwrites
+      // a table in use.
+      int* tok = col_tok + buf * BN;
+      float* wcol = col_w + buf * BN;
+      float* xs = col_xs + buf * BN;
+      if (et < ti.z) {
+        const int p = __ldg(a.pairs + ti.y + et);
+        tok[et] = p / a.k;
+        wcol[et] = __ldg(a.weights + p);
+        xs[et] = a.xscale ? __ldg(a.xscale + p / a.k) : 1.0f;
       }
-      if (*abort_flag || !mbar_wait_backoff(acc_full, lt & 1, globaltimer() + kWaitNs)) {
+      mbar_arrive(&tab_ready[buf]);
+      if (!mbar_wait(&tab_ready[buf], (lt >> 1) & 1, globaltimer() + kWaitNs)) {
+        fail();
+        break;
+      }
+      if (*abort_flag || !mbar_wait_backoff(&acc_full[buf], (lt >> 1) & 1, globaltimer() + kWaitNs)) {
         fail();
         break;
       }
       fence_after_sync();
-      const int col = ti.mt * BM + row;
-      for (int c0 = 0; c0 < ti.count; c0 += 16) {
+      const uint32_t acc = lane_addr + (uint32_t)(buf * C::ACC_COLS);
+      const int col = mt * BM + row;
+      for (int c0 = 0; c0 < ti.z; c0 += 16) {
         uint32_t v0[16];
-        tmem_ld16(lane_addr + c0, v0);
+        tmem_ld16(acc + c0, v0);
         if (PHASE == 0) {
           uint32_t v1[16];
-          tmem_ld16(lane_addr + BN + c0, v1);
+          tmem_ld16(acc + BN + c0, v1);
           tmem_ld_wait();
-          uint16_t* hrow = a.hbuf + (size_t)(ti.row0 + c0) * a.I + col;
+          uint16_t* hrow = a.hbuf + (size_t)(ti.y + c0) * a.I + col;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c0 + j < ti.count) {
-              const float g = __uint_as_float(v0[j]);
-              const float u = __uint_as_float(v1[j]);
+            if (c0 + j < ti.z) {
+              const float sc = xs[c0 + j];
+              const float g = __uint_as_float(v0[j]) * sc;
+              const float u = __uint_as_float(v1[j]) * sc;
               const float h = g / (1.0f + expf(-g)) * u;
               const __nv_bfloat16 hb = __float2bfloat16_rn(h);
               hrow[(size_t)j * a.I] = *reinterpret_cast<const uint16_t*>(&hb);
@@ -488,13 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c0 + j < ti.count)
+            if (c0 + j < ti.z)
               atomicAdd(a.y + (size_t)tok[c0 + j] * a.H + col, wcol[c0 + j] * __uint_as_float(v0[j]));
           }
         }
       }
       fence_before_sync();
-      mbar_arrive(acc_empty);
+      mbar_arrive(&acc_empty[buf]);
     }
   }
 
@@ -506,9 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
   }
 }
 
-// exclusive scan of ceil(count[e] / BN) -> ntile_off[E+1]; one CTA
-__global__ void __launch_bounds__(1024) tile_scan_kernel(const int32_t* __restrict__ counts, int E,
-                                                         int32_t* __restrict__ ntile_off) {
+// exclusive scan of ceil(count[e] / BN) -> ntile_off[E+1], then the token-tile
+// table: tile ntile_off[e] + n of expert e = {e, offsets[e] + n*BN, rows, 0};
+// *ntiles = ntile_off[E].  One CTA.
+__global__ void __launch_bounds__(1024) tile_scan_kernel(const int32_t* __restrict__ counts,
+                                                         const int32_t* __restrict__ offsets, int E,
+                                                         int32_t* __restrict__ ntile_off, int4* __restrict__ tiles,
+                                                         int32_t* __restrict__ ntiles) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -536,34 +552,51 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const int32_t* __restri
     }
     __syncthreads();
     const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + v - c;
-    if (e < E) ntile_off[e] = excl;
+    if (e < E) {
+      ntile_off[e] = excl;
+      const int cnt = counts[e], beg = offsets[e];
+      for (int n = 0; n < c; ++n) tiles[excl + n] = make_int4(e, beg + n * BN, min(BN, cnt - n * BN), 0);
+    }
     __syncthreads();
     if (threadIdx.x == 1023) carry = excl + c;
     __syncthreads();
   }
-  if (threadIdx.x == 0) ntile_off[E] = carry;
+  if (threadIdx.x == 0) {
+    ntile_off[E] = carry;
+    *ntiles = carry;
+  }
 }
 
-// x (BF16) -> FP16 for the NVFP4 gate/up MMA.  A magnitude at or above 65520
-// has no FP16 value: MOE_DEV_FP16_RANGE is set (the product rows become inf).
-__global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, long long n, uint16_t* __restrict__ x16,
-                                int32_t* __restrict__ st) {
-  bool bad = false;
-  for (long long i = (blockIdx.x * (long long)blockDim.x + threadIdx.x) * 8; i < n;
-       i += (long long)gridDim.x * blockDim.x * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
+// x (BF16) -> FP16 x * 2^e_t for the NVFP4 gate/up MMA, one warp per token:
+// e_t puts the token's largest magnitude in [2^14, 2^15), so every BF16 value
+// down to 2^-24 of that maximum is exact in FP16 (smaller ones are below the
+// last bit of any sum they enter); xscale[t] = 2^-e_t undoes it in the
+// epilogue (exact).
+__global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, int T, int H, uint16_t* __restrict__ x16,
+                                float* __restrict__ xscale) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const uint16_t* xr = x + (size_t)warp * H;
+  unsigned mx = 0u;
+  for (int i = lane * 8; i < H; i += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + i));
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = max(mx, max((wv[j] & 0x7FFFu) << 16, ((wv[j] >> 16) & 0x7FFFu) << 16));
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  const int e = moe::dm::f16_shift(__uint_as_float(mx));
+  const float sc = moe::dm::pow2f(e);
+  for (int i = lane * 8; i < H; i += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + i));
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = moe::bf16_bits_to_f32(wv[j] & 0xFFFFu), hi = moe::bf16_bits_to_f32(wv[j] >> 16);
-      bad |= !(fabsf(lo) < 65520.f) || !(fabsf(hi) < 65520.f);
-      const __half2 h = __floats2half2_rn(lo, hi);
-      o[j] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(x16 + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int j = 0; j < 4; ++j)
+      o[j] = moe::dm::pack_h2(moe::bf16_bits_to_f32(wv[j] & 0xFFFFu) * sc, moe::bf16_bits_to_f32(wv[j] >> 16) * sc);
+    *reinterpret_cast<uint4*>(x16 + (size_t)warp * H + i) = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  if (bad) moe::status_or(st, MOE_DEV_FP16_RANGE);
+  if (lane == 0) xscale[warp] = moe::dm::pow2f(-e);
 }
 
 // A pair whose expert index is outside [0, E) was dropped by the bucketing;
@@ -582,19 +615,24 @@ __global__ void poison_bad_pairs_kernel(const int32_t* __restrict__ idx, int P, 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t counts, offsets, ntile, pairs, hbuf, x16, bucket, total;
+  size_t counts, offsets, ntile, tiles, ntiles, pairs, hbuf, x16, xscale, bucket, total;
 };
 
 WsLayout ws_layout(int T, int k, int E, const moe_expert_shape& s) {
   WsLayout w;
   const size_t P = (size_t)T * k;
+  const size_t max_tiles = (P + BN - 1) / BN + (size_t)E;
   size_t o = 0;
   w.counts = o;  o = align256(o + (size_t)E * 4);
   w.offsets = o; o = align256(o + (size_t)(E + 1) * 4);
   w.ntile = o;   o = align256(o + (size_t)(E + 1) * 4);
+  w.tiles = o;   o = align256(o + max_tiles * 16);
+  w.ntiles = o;  o = align256(o + 4);
   w.pairs = o;   o = align256(o + P * 4);
   w.hbuf = o;    o = align256(o + P * (size_t)s.inter * 2);
-  w.x16 = o;     o = align256(o + (s.format == MOE_FMT_NVFP4 ? (size_t)T * s.hidden * 2 : 0));
+  const bool f16 = s.format == MOE_FMT_NVFP4;
+  w.x16 = o;     o = align256(o + (f16 ? (size_t)T * s.hidden * 2 : 0));
+  w.xscale = o;  o = align256(o + (f16 ? (size_t)T * 4 : 0));
   w.bucket = o;  o = align256(o + moe_bucket_workspace(T, k, E));
   w.total = o;
   return w;
@@ -603,20 +641,10 @@ WsLayout ws_layout(int T, int k, int E, const moe_expert_shape& s) {
 template <int FMT, int PHASE>
 int launch_phase(const GroupedArgs& a, cudaStream_t st) {
   using C = Cfg<PHASE>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(grouped_kernel<FMT, PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr = true;
-  }
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) return MOE_ERR_CUDA;
-  }
+  static moe::SmemGrant granted;
+  if (!moe::grant_smem(grouped_kernel<FMT, PHASE>, C::SMEM, granted, kThreads)) return MOE_ERR_CUDA;
+  const int sms = moe::device_info().sms;
+  if (sms <= 0) return MOE_ERR_CUDA;
   grouped_kernel<FMT, PHASE><<<sms, kThreads, C::SMEM, st>>>(a);
   return moe::launch_status();
 }
@@ -647,18 +675,21 @@ extern "C" int moe_experts_grouped(const uint16_t* x_bf16, const int32_t* idx, c
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   int32_t* ntile = reinterpret_cast<int32_t*>(ws + L.ntile);
+  int4* tiles = reinterpret_cast<int4*>(ws + L.tiles);
+  int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
   int32_t* pairs = reinterpret_cast<int32_t*>(ws + L.pairs);
   int rc = moe_bucket_by_expert(idx, T, k, E, counts, offsets, pairs, ws + L.bucket,
                                 L.total - L.bucket, dev_status, stream);
   if (rc != MOE_OK) return rc;
-  tile_scan_kernel<<<1, 1024, 0, st>>>(counts, E, ntile);
+  tile_scan_kernel<<<1, 1024, 0, st>>>(counts, offsets, E, ntile, tiles, ntiles);
   if (cudaMemsetAsync(y, 0, (size_t)T * s.hidden * sizeof(float), st) != cudaSuccess)
     return MOE_ERR_CUDA;
   GroupedArgs a;
   a.x = x_bf16;
+  a.xscale = nullptr;
   a.pairs = pairs;
-  a.offsets = offsets;
-  a.ntile_off = ntile;
+  a.tiles = tiles;
+  a.ntiles = ntiles;
   a.weights = weights;
   a.ptrs = expert_ptrs;
   a.E = E;
@@ -670,11 +701,11 @@ extern "C" int moe_experts_grouped(const uint16_t* x_bf16, const int32_t* idx, c
   a.st = dev_status;
   if (s.format == MOE_FMT_NVFP4) {
     uint16_t* x16 = reinterpret_cast<uint16_t*>(ws + L.x16);
-    const long long n = (long long)T * s.hidden;
-    x_to_f16_kernel<<<(unsigned)std::min<long long>((n / 8 + 255) / 256, 1184), 256, 0, st>>>(
-        x_bf16, n, x16, dev_status);
+    float* xsc = reinterpret_cast<float*>(ws + L.xscale);
+    x_to_f16_kernel<<<(unsigned)((T + 7) / 8), 256, 0, st>>>(x_bf16, T, s.hidden, x16, xsc);
     GroupedArgs a0 = a;
     a0.x = x16;
+    a0.xscale = xsc;
     rc = launch_phase<MOE_FMT_NVFP4, 0>(a0, st);
     if (rc == MOE_OK) rc = launch_phase<MOE_FMT_NVFP4, 1>(a, st);
   } else {

@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 // ---------------------------------------------------------------------------
 // Top-k.  One block of kTopkThreads per token, candidates keyed by (ordered
 // logit, ~expert): every warp picks the k best of its share, warp 0 merges
-// those sorted lists (moe::rt::topk_block); weights renormalised over the
+// those sorted lists (moe::rt::topk_block, behind the filter of
+// moe::rt::topk_block_fast); weights renormalised over the
 // picks.
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 512;
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const int lane = threadIdx.x & 31, t = blockIdx.x;
   int my_e = 0;
   float my_l = 0.0f;
-  moe::rt::topk_block<kTopkThreads / 32>(logits + (size_t)t * E, E, k, fin, my_e, my_l);
+  moe::rt::topk_block_fast<kTopkThreads / 32>(logits + (size_t)t * E, E, k, fin, my_e, my_l);
   if (threadIdx.x < 32) {
     const float w = moe::rt::topk_weight(lane, k, my_l);
     if (lane < k) {
@@ -213,16 +214,7 @@ __global__ void __launch_bounds__(kGridThreads) router_grid_kernel(GridArgs a) {
   }
 }
 
-int sm_count_router() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 0;
-  }
-  return sms;
-}
+int sm_count_router() { return moe::device_info().sms; }
 
 bool grid_fits(int T, int H, int E) {
   return T >= 1 && (size_t)T * H * 2 <= kGridMaxXBytes && E <= 1024 && H % 8 == 0 &&
@@ -240,13 +232,8 @@ int launch_grid_router(const GridArgs& a0, int k, int32_t* idx, float* weights, 
   a.epc = (a.E + sms - 1) / sms;
   const int grid = (a.E + a.epc - 1) / a.epc;
   const size_t smem = 1024 + (size_t)a.T * a.H * 2;
-  static size_t granted = 0;
-  if (smem > 48 * 1024 && smem > granted) {
-    if (cudaFuncSetAttribute(router_grid_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    granted = smem;
-  }
+  static moe::SmemGrant granted;
+  if (!moe::grant_smem(router_grid_kernel, smem, granted)) return MOE_ERR_CUDA;
   const int rc = moe::launch_pdl(router_grid_kernel, dim3(grid), dim3(kGridThreads), smem, st, a);
   if (rc != MOE_OK) return rc;
   return launch_topk(a.logits, a.T, a.E, k, idx, weights, st);

@@ -197,5 +197,91 @@ __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsi
   step_sync<BAR, NW * 32>();  // fin[] may be reused by the caller
 }
 
+// The same top-k as topk_block, usually in a fraction of its time: every
+// warp's largest key goes to shared memory, and tau = the k-th largest of
+// those NW maxima bounds the answer from below -- at least k keys (the k
+// largest maxima) are >= tau, so the k-th largest key of all is >= tau and
+// every pick is a key >= tau.  Those survivors (typically a few more than k
+// for continuous logits) are gathered in shared memory and warp 0 ranks them
+// exactly; when more than 32 survive (few warps hold all the large keys) or
+// NW < k, it falls back to topk_block.  Keys are unique, so both routes give
+// the same picks in the same order.  fin: NW * 32 keys of shared memory
+// (at least 128); same calling rules as topk_block.
+template <int NW, int BAR = -1>
+__device__ __forceinline__ void topk_block_fast(const float* lrow, int E, int k, unsigned long long* fin,
+                                                int& my_e, float& my_l) {
+  static_assert(NW * 32 >= 128, "scratch");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (NW < k) {
+    topk_block<NW, BAR>(lrow, E, k, fin, my_e, my_l);
+    return;
+  }
+  constexpr int kPer = (1024 + 32 * NW - 1) / (32 * NW);
+  unsigned long long cand[kPer];
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) {
+    const int e = warp * 32 + lane + 32 * NW * m;
+    cand[m] = 0ull;
+    if (e < E) cand[m] = ((unsigned long long)ordered_key(__ldcg(lrow + e)) << 32) | (unsigned long long)(~(uint32_t)e);
+    best = cand[m] > best ? cand[m] : best;
+  }
+  unsigned* cnt = reinterpret_cast<unsigned*>(fin + 96);
+  if (warp < NW) {
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+    if (lane == 0) fin[warp] = ((unsigned long long)hi << 32) | lo;
+    if (warp == 0 && lane == 0) *cnt = 0u;
+  }
+  step_sync<BAR, NW * 32>();
+  // tau: lane i < NW ranks warp maximum i among the NW maxima
+  unsigned long long tau = 0ull;
+  {
+    const unsigned long long mine = lane < NW ? fin[lane] : 0ull;
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < NW; ++j) rank += fin[j] > mine;
+    const unsigned sel = __ballot_sync(0xffffffffu, lane < NW && rank == k - 1);
+    const int src = sel ? __ffs(sel) - 1 : 0;
+    tau = __shfl_sync(0xffffffffu, mine, src);
+    if (!sel) tau = 0ull;  // maxima tied at zero (fewer than k warps hold keys): no filter
+  }
+  // survivors: real keys >= tau, gathered at fin[32 .. 64) (unordered)
+  if (warp < NW) {
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const bool keep = cand[m] != 0ull && cand[m] >= tau;
+      const unsigned b = __ballot_sync(0xffffffffu, keep);
+      unsigned base = 0u;
+      if (lane == 0 && b) base = atomicAdd(cnt, (unsigned)__popc(b));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const unsigned pos = base + __popc(b & ((1u << lane) - 1u));
+      if (keep && pos < 32u) fin[32 + pos] = cand[m];
+    }
+  }
+  step_sync<BAR, NW * 32>();
+  const unsigned total = *cnt;
+  if (total > 32u || tau == 0ull) {
+    step_sync<BAR, NW * 32>();  // every thread has read the count before topk_block reuses fin
+    topk_block<NW, BAR>(lrow, E, k, fin, my_e, my_l);
+    return;
+  }
+  if (warp == 0) {
+    const unsigned long long mine = lane < (int)total ? fin[32 + lane] : 0ull;
+    int rank = 0;
+    for (unsigned j = 0; j < total; ++j) rank += fin[32 + j] > mine;
+    if (lane < (int)total && rank < k) fin[64 + rank] = mine;
+    __syncwarp();
+    my_e = 0;
+    my_l = 0.0f;
+    if (lane < k) {
+      const unsigned long long key = fin[64 + lane];
+      my_e = (int)(~(uint32_t)key);
+      my_l = key_to_float((uint32_t)(key >> 32));
+    }
+  }
+  step_sync<BAR, NW * 32>();  // fin[] may be reused by the caller
+}
+
 }  // namespace rt
 }  // namespace moe

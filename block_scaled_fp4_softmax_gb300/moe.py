@@ -35,6 +35,7 @@ EXPORTS = (
     "moe_rmsnorm_router_topk",
     "moe_experts_decode_workspace",
     "moe_experts_decode",
+    "moe_experts_decode_host",
     "moe_decode_layer",
     "moe_experts_decode_noalloc_limit",
     "moe_experts_decode_noalloc",
@@ -44,6 +45,7 @@ EXPORTS = (
     "moe_experts_grouped",
     "fp8_rowscale_gemv",
     "moe_status_string",
+    "moe_test_set_wait_limit",
 )
 
 
@@ -75,6 +77,8 @@ _SIGS = {
     "moe_experts_decode_workspace": (_sz, [_i, _i, ExpertShape]),
     "moe_experts_decode": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _sz,
                                 _vp, _vp]),
+    "moe_experts_decode_host": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _sz,
+                                     _vp, _vp]),
     "moe_decode_layer": (_i, [_vp, _vp, _i, ctypes.c_double, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp,
                               ExpertShape, _vp, _vp, _sz, _vp, _vp]),
     "moe_experts_decode_noalloc_limit": (_sz, []),
@@ -86,6 +90,7 @@ _SIGS = {
                                  _vp, _vp]),
     "fp8_rowscale_gemv": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_i]),
+    "moe_test_set_wait_limit": (_i, [ctypes.c_ulonglong, _i]),
 }
 
 
@@ -292,6 +297,28 @@ def moe_experts_decode(x, idx, weights, ptrs, s: ExpertShape, y=None, workspace=
     return y
 
 
+def moe_experts_decode_host(x, idx, weights, ptrs, s: ExpertShape, y=None, workspace=None,
+                            dev_status=None, stream=None):
+    """Expert pass over records that may sit in host memory the device can
+    address (pinned, or Grace memory over NVLink-C2C); plain loads only."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(idx, "idx", torch.int32)
+    _cuda(weights, "weights", torch.float32)
+    _cuda(ptrs, "expert_ptrs", torch.int64)
+    T, k = idx.shape
+    H = x.shape[1]
+    if y is None:
+        y = torch.empty(T, H, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        nbytes = max(moe_experts_decode_workspace(T, k, s), 16)
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=x.device)
+    _check(load().moe_experts_decode_host(_ptr(x), _ptr(idx), _ptr(weights), T, k, _ptr(ptrs),
+                                          ptrs.numel(), s, _ptr(y), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _ptr(dev_status), _stream(stream)), "moe_experts_decode_host")
+    return y
+
+
 def moe_experts_decode_noalloc_limit() -> int:
     return int(load().moe_experts_decode_noalloc_limit())
 
@@ -374,3 +401,11 @@ def fp8_rowscale_gemv(w, row_scale, x, y=None, stream=None):
 
 def moe_status_string(status: int) -> str:
     return load().moe_status_string(int(status)).decode()
+
+
+def moe_test_set_wait_limit(wait_ns: int = 0, barrier_extra_arrivals: int = 0) -> None:
+    """Test hook: the limit of the decode kernels' bounded waits, and one extra
+    arrival each grid barrier expects (which no CTA makes, so the barriers run
+    out); (0, 0) restores the defaults."""
+    _check(load().moe_test_set_wait_limit(int(wait_ns), int(barrier_extra_arrivals)),
+           "moe_test_set_wait_limit")

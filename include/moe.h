@@ -162,11 +162,32 @@ size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s);
  *   summed in a fixed order (bit-reproducible).
  * workspace: device scratch of at least moe_experts_decode_workspace() bytes.
  * dev_status: device int32 or NULL; MOE_DEV_* bits are OR-ed into it.
- * Limits: T*k <= 4096. */
+ * Limits: T*k <= 4096, k*I <= 49152.
+ * Residency: the one-shot and ring kernels run one CTA per SM with grid-wide
+ * barriers, so all of their CTAs must be resident at once.  The library
+ * checks on the host that one CTA fits on an SM (else MOE_ERR_CUDA); kernels
+ * of other streams, processes (MPS) or green contexts that hold SMs for the
+ * whole call can still keep CTAs out, and the barrier waits then run out
+ * (2 s) with MOE_DEV_TIMEOUT and NaN outputs.  Do not run such persistent
+ * kernels concurrently with this call. */
 int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
                        int T, int k, const void* const* expert_ptrs, int E,
                        moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
                        int32_t* dev_status, void* stream);
+
+/* Decode from a host-memory expert tier (first page, "The engine", items 1-2:
+ * the experts live in host RAM and only the selected ones travel to the GPU
+ * each token).  Same arguments, output and bits as moe_experts_decode's
+ * two-kernel path, but every record byte is read with plain 16-byte loads,
+ * so expert_ptrs may point into host memory that the device can address:
+ * pinned host memory on a unified-address system, or the Grace CPU's memory
+ * that a GB300 reaches over NVLink-C2C.  Records in HBM work too (then it is
+ * simply the two-kernel path).  The records must not change while the call
+ * runs.  Same workspace rules and limits as moe_experts_decode. */
+int moe_experts_decode_host(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
+                            int T, int k, const void* const* expert_ptrs, int E,
+                            moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
+                            int32_t* dev_status, void* stream);
 
 /* One decode layer in one launch (first page, "The engine", item 4, and
  * "Where the time actually goes": the expert work of a layer waits on the
@@ -188,7 +209,8 @@ int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* 
  * start before it ends.
  * Shapes the one-shot expert pass does not cover (T*k > 64, or a per-SM
  * share larger than shared memory) return MOE_ERR_UNSUPPORTED: use the two
- * calls for those. */
+ * calls for those.  The residency requirement of moe_experts_decode (all CTAs
+ * of the grid-barrier kernel resident at once) applies. */
 int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int T, double eps, uint16_t* x_out,
                      const uint16_t* wr_bf16, const float* bias, int E, int k, int32_t* idx,
                      float* weights, float* logits, const void* const* expert_ptrs,
@@ -210,7 +232,10 @@ int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int T, double 
  *    before any stream capture.
  *  - Every call shares the one array per device: calls whose kernels overlap
  *    on the GPU (other streams, other threads) race and give wrong results.
- *    The part that must start at zero is cleared by each call on `stream`.
+ *    The part that must start at zero is cleared by each call on `stream`,
+ *    after every argument check has passed (a rejected call leaves the array
+ *    as it was and returns what moe_experts_decode would).
+ *  - The residency requirement of moe_experts_decode applies.
  *  - No cudaMalloc, cudaFree or other allocating routine is called. */
 size_t moe_experts_decode_noalloc_limit(void);
 int moe_experts_decode_noalloc(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
@@ -262,6 +287,19 @@ int fp8_rowscale_gemv(const uint8_t* w_e4m3, const float* row_scale, const uint1
 
 /* Static text for a moe_status value. */
 const char* moe_status_string(int status);
+
+/* Test hook for the bounded waits of moe_decode_layer and of
+ * moe_experts_decode's one-shot kernel, so that a test can make a wait run
+ * out without faulting or hanging the GPU.  The pages have no counterpart.
+ * wait_ns: the limit of every bounded wait in those kernels (0 restores the
+ *   default of 2 s; otherwise 1 us .. 10 s).
+ * barrier_extra_arrivals: 0, or 1 to make every grid barrier wait for one
+ *   arrival more than the grid makes -- it then runs out after wait_ns, the
+ *   launch sets MOE_DEV_TIMEOUT and writes NaN outputs.  Zero the workspace
+ *   again before the next call.
+ * The setting is process-wide and applies to launches made after the call.
+ * Returns MOE_ERR_INVALID_ARG for values outside those ranges. */
+int moe_test_set_wait_limit(unsigned long long wait_ns, int barrier_extra_arrivals);
 
 #ifdef __cplusplus
 }

@@ -372,21 +372,26 @@ def silu(g):
         return g / (1.0 + np.exp(-g))
 
 
-def moe_layer_decode(x_bits, idx, weights, records, H: int, I: int, fmt: int) -> np.ndarray:
+def moe_layer_decode(x_bits, idx, weights, records, H: int, I: int, fmt: int, experts=None) -> np.ndarray:
     """y[t] = sum_j w[t,j] * down_e (silu(gate_e x_t) * up_e x_t), e = idx[t,j].
 
     float64 throughout on the exactly dequantised weights; y returned as
-    float32.  ``records`` maps expert id -> record bytes.
+    float32.  ``records`` maps expert id -> record bytes.  ``experts``, if
+    given, restricts the sum to the pairs routed to those experts (the
+    others contribute nothing), so that callers can split the work.
     """
     x = bf16_bits_to_f32(x_bits).astype(np.float64)
     T = x.shape[0]
     idx = np.asarray(idx)
     w = np.asarray(weights, dtype=np.float64)
     y = np.zeros((T, H), dtype=np.float64)
+    keep = None if experts is None else {int(e) for e in experts}
     cache = {}
     for t in range(T):
         for j in range(idx.shape[1]):
             e = int(idx[t, j])
+            if keep is not None and e not in keep:
+                continue
             if e not in cache:
                 cache[e] = unpack_expert(records[e], H, I, fmt)
             Wg, Wu, Wd = cache[e]
@@ -422,17 +427,21 @@ def moe_layer_grouped(x_bits, idx, weights, records, H: int, I: int, fmt: int) -
 
 
 def moe_layer_grouped_by_expert(x_bits, idx, weights, records, H: int, I: int, fmt: int,
-                                tokens=None) -> np.ndarray:
+                                tokens=None, experts=None) -> np.ndarray:
     """Same result as ``moe_layer_grouped`` computed expert by expert with
     matrix products (for prompt-sized inputs).  ``tokens`` restricts the
-    returned rows to a sample of tokens (the others are left zero)."""
+    returned rows to a sample of tokens (the others are left zero);
+    ``experts`` restricts the sum to the pairs routed to those experts."""
     x = bf16_bits_to_f32(x_bits).astype(np.float64)
     T = x.shape[0]
     idx = np.asarray(idx)
     w = np.asarray(weights, dtype=np.float64)
     want = np.ones(T, dtype=bool) if tokens is None else np.isin(np.arange(T), tokens)
     y = np.zeros((T, H), dtype=np.float64)
-    for e in np.unique(idx[want]):
+    chosen = np.unique(idx[want])
+    if experts is not None:
+        chosen = np.intersect1d(chosen, np.asarray(list(experts), dtype=chosen.dtype))
+    for e in chosen:
         ts, js = np.nonzero((idx == e) & want[:, None])
         Wg, Wu, Wd = unpack_expert(records[int(e)], H, I, fmt)
         X = x[ts]

@@ -78,3 +78,32 @@ def oracle_pack_many(pool: "Pool", experts):
         for e, j in zip(want, jobs):
             pool._oracle_records[e] = j.result()
     return {int(e): pool._oracle_records[int(e)] for e in experts}
+
+
+def _split_worker(args):
+    fn_name, x, idx, w, recs, H, I, fmt, subset = args
+    fn = getattr(O, fn_name)
+    return fn(x, idx, w, recs, H, I, fmt, experts=subset)
+
+
+def oracle_layer_split(fn_name, xb, idx, w, records, H, I, fmt, parts=16):
+    """The oracle's layer function (moe_layer_decode or
+    moe_layer_grouped_by_expert) with its experts split over worker processes:
+    each worker sums the pairs of its experts, and the parts are added in
+    float64.  Each pair's arithmetic is the oracle's own; only the order in
+    which whole expert contributions are added differs (float64, far below the
+    tolerances)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    global _POOL
+    if _POOL is None:
+        _POOL = cf.ProcessPoolExecutor(max_workers=min(16, os.cpu_count() or 4),
+                                       mp_context=mp.get_context("spawn"))
+    experts = sorted({int(e) for e in np.asarray(idx).ravel()})
+    groups = [experts[i::parts] for i in range(parts) if experts[i::parts]]
+    jobs = [_POOL.submit(_split_worker, (fn_name, xb, idx, w, {e: records[e] for e in g}, H, I, fmt, g))
+            for g in groups]
+    y = np.zeros((np.asarray(xb).shape[0], H), dtype=np.float64)
+    for j in jobs:
+        y += j.result().astype(np.float64)
+    return y.astype(np.float32)

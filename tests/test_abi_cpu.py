@@ -81,3 +81,10 @@ def test_argument_validation_before_any_cuda_call(lib):
     assert lib.fp4_pack_expert(one, one, vp(20), s, one, None) == 2
     # counters header, then h [T*k][I]
     assert moe.moe_experts_decode_workspace(1, 10, s) == 16640 + 10 * 640 * 4
+
+
+def test_wait_limit_hook_rejects_bad_values(lib):
+    # host-side checks only; (0, 0) restores the defaults
+    assert lib.moe_test_set_wait_limit(10, 0) == 1            # below 1 us
+    assert lib.moe_test_set_wait_limit(200_000, 2) == 1       # only 0 or 1 extra arrival
+    assert lib.moe_test_set_wait_limit(0, 0) == 0

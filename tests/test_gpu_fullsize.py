@@ -5,9 +5,17 @@ times, on outputs the oracle computes one by one.
   CUDA-graph replay bench.py times must equal the eager per-layer calls bit
   for bit; sampled layers are checked against the oracle with the oracle's own
   inputs (layer 0 from x0, deeper layers from independently seeded inputs).
-* Qwen prompt layer: 2451 tokens, Zipf-skewed routing over 512 experts.
-* DeepSeek-shaped MXFP4 layer: 384 experts of 18,800,640 bytes, top-6.
-* Batched decode: 32 tokens over the 512-expert pool.
+* Qwen prompt layer: 2451 tokens, Zipf-skewed routing over 512 experts --
+  every token against the oracle, and every token of the most-loaded expert
+  on its own.
+* DeepSeek-shaped MXFP4 layer: 384 experts of 18,800,640 bytes, top-6; ten of
+  the forty seeded calls, with the L2 flushed before each.
+* Batched decode: 32 tokens through all 48 layers of the stack, the router's
+  RMS chaining included, teacher-forced layer by layer with the oracle's own
+  chain (marked slow as well: it runs the oracle on ~11,000 expert pairs).
+
+The oracle's layer functions run split over worker processes by expert
+(helpers.oracle_layer_split); each pair's arithmetic is the oracle's own.
 """
 import os
 import sys
@@ -17,7 +25,7 @@ import pytest
 import torch
 
 from block_scaled_fp4_softmax_gb300 import moe, synth
-from helpers import Pool, bits, oracle_pack_many
+from helpers import Pool, bits, oracle_layer_split, oracle_pack_many
 from oracle import oracle as O
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -110,23 +118,59 @@ def test_stack_layers_against_oracle(stack):
         assert O.rel_l2(gy, y_l) <= 1e-5
 
 
-def test_batched_decode_32_tokens(stack):
+class _UniqueView:
+    """Oracle packing of the stack's distinct experts, keyed by distinct id."""
+
+    def __init__(self, stack):
+        self.stack = stack
+        self.fmt = O.FMT_NVFP4
+        self._oracle_records = {}
+
+    def weights(self, u):
+        return synth.expert_weights(bench.H, bench.I, synth.expert_seed(bench.WORKLOAD_ID, 0, int(u)),
+                                    device="cuda")
+
+
+@pytest.mark.slow
+def test_batched_decode_32_tokens_48_chained_layers(stack):
+    """The batched-decode workload as bench.py runs it (router or fused RMS
+    chaining + router, then the expert pass for 32 tokens), layer by layer on
+    the oracle's own chain: the GPU gets the oracle's x_L (and, for the
+    chaining, the oracle's y_{L-1}); indices must be equal and y within the
+    decode tolerance on every one of the 48 layers."""
     st = stack
-    L = 5
-    x = synth.activations(32, bench.H, 4321)
-    xb = bits(x)
-    idx, w = O.topk_softmax(O.router_logits(xb, bits(st.wr[L])), bench.K_TOP)
-    y = moe.moe_experts_decode(x.cuda(), torch.from_numpy(idx).cuda(),
-                               torch.from_numpy(w.astype(np.float32)).cuda(), st.ptrs[L], st.s)
-    got = y.cpu().numpy()
-    sample = [0, 7, 31]
-    recs = oracle_pack_many(_StackView(st, L), idx[sample].ravel())
-    want = O.moe_layer_decode(xb[sample], idx[sample], w[sample], recs, bench.H, bench.I,
-                              O.FMT_NVFP4)
-    assert O.rel_l2(got[sample], want) <= 1e-5
+    T = 32
+    uv = _UniqueView(st)
+    x0 = synth.activations(T, bench.H, synth.seed_of(4, 100, synth.T_X), device="cuda")
+    xb = bits(x0)
+    y_prev = None
+    worst = 0.0
+    for L in range(bench.LAYERS):
+        wrb = bits(st.wr[L])
+        idx_o, w_o = O.topk_softmax(O.router_logits(xb, wrb), bench.K_TOP)
+        ch = st.choice[L]
+        recs_u = oracle_pack_many(uv, [int(ch[e]) for e in idx_o.ravel()])
+        recs = {int(e): recs_u[int(ch[e])] for e in idx_o.ravel()}
+        y_o = oracle_layer_split("moe_layer_decode", xb, idx_o, w_o, recs, bench.H, bench.I, O.FMT_NVFP4)
+        x_t = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        if y_prev is None:
+            idx_g, w_g, _ = moe.moe_router_topk(x_t, st.wr[L], None, bench.K_TOP)
+        else:
+            xg, idx_g, w_g, _ = moe.moe_rmsnorm_router_topk(torch.from_numpy(y_prev).cuda(), st.wr[L], None,
+                                                            bench.K_TOP, 1e-6)
+            assert np.array_equal(bits(xg), xb), L
+        y_g = moe.moe_experts_decode(x_t, idx_g, w_g, st.ptrs[L], st.s)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx_g.cpu().numpy(), idx_o), L
+        err = O.rel_l2(y_g.cpu().numpy(), y_o)
+        worst = max(worst, err)
+        assert err <= 1e-5, (L, err)
+        y_prev = y_o
+        xb = O.rmsnorm_bf16(y_o, 1e-6)
+    print(f"worst rel-L2 over 48 layers x 32 tokens: {worst:.2e}")
 
 
-def test_prompt_layer_full_size_sampled_tokens():
+def test_prompt_layer_full_size_all_tokens():
     pl = bench.PromptLayer(torch, moe, synth, torch.device("cuda"))
     pl.step()
     torch.cuda.synchronize()
@@ -134,10 +178,9 @@ def test_prompt_layer_full_size_sampled_tokens():
     counts = torch.bincount(pl.idx.flatten().long(), minlength=bench.E)
     assert int((counts > 0).sum()) >= 480            # Zipf bias: nearly every expert is hit
     xb = bits(pl.x)
-    tokens = np.array([0, 1, 1000, 2450])
-    logits = O.router_logits(xb[tokens], bits(pl.wr), pl.bias.cpu().numpy())
+    logits = O.router_logits(xb, bits(pl.wr), pl.bias.cpu().numpy())
     idx, w = O.topk_softmax(logits, bench.K_TOP)
-    assert np.array_equal(pl.idx.cpu().numpy()[tokens], idx)
+    assert np.array_equal(pl.idx.cpu().numpy(), idx)
 
     class _View:
         fmt = O.FMT_NVFP4
@@ -148,23 +191,42 @@ def test_prompt_layer_full_size_sampled_tokens():
                                         device="cuda")
 
     recs = oracle_pack_many(_View(), idx.ravel())
-    want = O.moe_layer_grouped(xb[tokens], idx, w, recs, bench.H, bench.I, O.FMT_NVFP4)
-    got = pl.y.cpu().numpy()[tokens]
-    assert np.all(np.isfinite(pl.y.cpu().numpy()))
+    want = oracle_layer_split("moe_layer_grouped_by_expert", xb, idx, w, recs, bench.H, bench.I, O.FMT_NVFP4)
+    got = pl.y.cpu().numpy()
+    assert np.all(np.isfinite(got))
     assert O.rel_l2(got, want) <= 2e-3
+    # every token of the most-loaded expert (its token tiles span 13 tiles of 128)
+    top = int(np.argmax(np.bincount(idx.ravel(), minlength=bench.E)))
+    toks = np.nonzero((idx == top).any(axis=1))[0]
+    assert len(toks) > 1000
+    for t in toks:
+        assert O.rel_l2(got[t], want[t]) <= 2e-3, t
 
 
-def test_deepseek_shaped_mxfp4_layer():
-    pool = Pool(384, 4096, 2880, 1, workload=3)
-    assert moe.moe_expert_record_bytes(pool.shape) == 18_800_640
-    wr = synth.router_weights(384, 4096, synth.seed_of(3, 0, synth.T_ROUTER))
-    for call in range(2):
-        x = synth.activations(1, 4096, synth.seed_of(3, 10 + call, synth.T_X))
-        xb = bits(x)
-        idx, w, _ = moe.moe_router_topk(x.cuda(), wr.cuda(), None, 6)
-        want_i, want_w = O.topk_softmax(O.router_logits(xb, bits(wr)), 6)
-        assert np.array_equal(idx.cpu().numpy(), want_i)
-        y = moe.moe_experts_decode(x.cuda(), idx, w, pool.ptrs, pool.shape)
-        recs = oracle_pack_many(pool, want_i.ravel())
-        want = O.moe_layer_decode(xb, want_i, want_w, recs, 4096, 2880, O.FMT_MXFP4)
-        assert O.rel_l2(y.cpu().numpy(), want) <= 1e-5
+def test_deepseek_shaped_mxfp4_calls():
+    """Ten of the forty seeded DeepSeek-shaped calls exactly as bench.py runs
+    them (router, then the expert pass on one 384-expert MXFP4 weight set),
+    the L2 flushed before each."""
+    dc = bench.DeepSeekCalls(torch, moe, synth, torch.device("cuda"))
+    assert dc.rb == 18_800_640
+
+    class _View:
+        fmt = O.FMT_MXFP4
+        _oracle_records = {}
+
+        def weights(self, e):
+            return synth.expert_weights(dc.HD, dc.ID, synth.expert_seed(dc.WORKLOAD, 0, int(e)), device="cuda")
+
+    view = _View()
+    for c in range(0, dc.CALLS, 4):
+        dc.flush()
+        dc.router(c)
+        dc.experts(c)
+        torch.cuda.synchronize()
+        assert int(dc.st.item()) == 0
+        xb = bits(dc.xs[c])
+        want_i, want_w = O.topk_softmax(O.router_logits(xb, bits(dc.wr[c])), dc.KD)
+        assert np.array_equal(dc.idx.cpu().numpy(), want_i), c
+        recs = oracle_pack_many(view, want_i.ravel())
+        want = oracle_layer_split("moe_layer_decode", xb, want_i, want_w, recs, dc.HD, dc.ID, O.FMT_MXFP4)
+        assert O.rel_l2(dc.y.cpu().numpy(), want) <= 1e-5, c

@@ -175,6 +175,27 @@ def test_grouped_k1_close_to_decode_and_by_expert_equal():
     assert O.rel_l2(a, b) < 1e-6
 
 
+def test_expert_restriction_sums_to_the_whole_layer():
+    # the parts restricted to disjoint expert sets add up to the full layer,
+    # and the worker-split helper the full-size GPU tests use agrees with the
+    # serial oracle
+    from helpers import oracle_layer_split
+    H, I, E, k, T = 64, 32, 8, 3, 5
+    recs = dict(enumerate(_pool(E, H, I, O.FMT_NVFP4, 600)))
+    xb = _bits(synth.activations(T, H, 61))
+    rng = np.random.default_rng(62)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = rng.dirichlet(np.ones(k), size=T)
+    for fn in ("moe_layer_decode", "moe_layer_grouped_by_expert"):
+        whole = getattr(O, fn)(xb, idx, w, recs, H, I, O.FMT_NVFP4)
+        parts = sum(getattr(O, fn)(xb, idx, w, recs, H, I, O.FMT_NVFP4, experts=g).astype(np.float64)
+                    for g in ([0, 3, 5], [1, 2], [4, 6, 7]))
+        assert O.rel_l2(parts, whole) < 1e-7
+        assert not np.any(getattr(O, fn)(xb, idx, w, recs, H, I, O.FMT_NVFP4, experts=[]))
+        split = oracle_layer_split(fn, xb, idx, w, recs, H, I, O.FMT_NVFP4, parts=3)
+        assert O.rel_l2(split, whole) < 1e-7
+
+
 def test_bucketing_brute_force():
     rng = np.random.default_rng(9)
     T, k, E = 37, 4, 11

@@ -254,8 +254,8 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier for a grid whose CTAs are all resident (cooperative
-// launch).  bar[0] counts arrivals and is reset to 0 by the last arriver,
+// Grid-wide barrier for a grid whose CTAs are all resident (one CTA per SM,
+// checked on the host before the launch).  bar[0] counts arrivals and is reset to 0 by the last arriver,
 // bar[1] is an epoch that the last arriver bumps; the others wait for the
 // epoch to move, at most until `deadline_ns`.  bar[0] must be 0 before the
 // first use and is 0 again after every completed barrier.  Returns false
@@ -294,20 +294,31 @@ namespace moe {
 // Launches `kernel` with programmatic stream serialization, so it may start
 // while the previous kernel on the stream is finishing; the kernel itself
 // calls pdl_wait() before touching anything the previous kernel produced.
+// With `cooperative`, the launch is also cooperative: the driver runs it only
+// with every CTA resident at once (else the launch fails), which a kernel
+// with a grid-wide barrier needs.
 template <typename... KArgs, typename... Args>
-inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                      cudaStream_t stream, Args... args) {
+inline int launch_pdl_ex(bool cooperative, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cooperative ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, Args... args) {
+  return launch_pdl_ex(false, kernel, grid, block, smem, stream, args...);
 }
 
 }  // namespace moe

@@ -739,8 +739,10 @@ template <int FMT, int UPR, int UPDR>
 int launch_stream_shape(const st::Args& sa, size_t smem, int sms, cudaStream_t stream) {
   static moe::SmemGrant granted;
   if (!moe::grant_smem(st::stream_kernel<FMT, UPR, UPDR>, smem, granted, st::kThreads)) return MOE_ERR_CUDA;
-  return moe::launch_pdl(st::stream_kernel<FMT, UPR, UPDR>, dim3(sms), dim3(st::kThreads), smem,
-                         stream, sa);
+  // the ring kernel's grid barrier needs every CTA resident: one CTA per SM,
+  // checked by grant_smem above (see launch_shape of the one-shot kernel on
+  // why the launch is not cooperative)
+  return moe::launch_pdl(st::stream_kernel<FMT, UPR, UPDR>, dim3(sms), dim3(st::kThreads), smem, stream, sa);
 }
 
 template <int FMT>

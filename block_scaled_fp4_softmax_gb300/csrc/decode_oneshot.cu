@@ -546,6 +546,10 @@ template <int FMT, int UPR, int UPDR>
 int launch_shape(const DecodeOneshotArgs& a, int grid, size_t smem, cudaStream_t stream) {
   static SmemGrant granted;  // per device; also checks that one CTA fits on an SM
   if (!grant_smem(oneshot_kernel<FMT, UPR, UPDR>, smem, granted, kThreads)) return MOE_ERR_CUDA;
+  // Every CTA takes part in the grid barriers, so all must be resident: one
+  // CTA per SM, checked by grant_smem above.  A cooperative launch would make
+  // the driver guarantee it, but costs about 2.5 us more host time per launch
+  // (48 eager launches per decoded token), so the waits are bounded instead.
   return launch_pdl(oneshot_kernel<FMT, UPR, UPDR>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 

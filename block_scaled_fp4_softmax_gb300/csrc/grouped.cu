@@ -16,14 +16,17 @@
 //
 // One persistent CTA per SM walks a static list of tiles (token tile of one
 // expert, 128-row weight tile).  Per k-step of 64 elements three rings meet:
-//   raw ring  (per producer thread, 8-12 steps deep): the thread's own FP4
-//             codes and scale word, fetched with cp.async well ahead of use --
-//             the only operand that comes from HBM, so the deep ring is cheap
-//             (FP4 is a quarter of the BF16 bytes);
-//   A ring    (2 stages): the dequantised 128 x 64 weight tile(s), FP16 or
+//   raw ring  (per producer warp, 8-12 steps deep): the FP4 codes and scales
+//             of the warp's rows, fetched with cp.async two k-steps at a time
+//             and well ahead of use -- the only operand that comes from HBM,
+//             so the deep ring is cheap (FP4 is a quarter of the BF16 bytes).
+//             Lanes fetch consecutive 16-byte pieces, so one instruction reads
+//             8 rows x 64 contiguous bytes: few L1->L2 requests per byte;
+//   A ring    (3-4 stages): the dequantised 128 x 64 weight tile(s), FP16 or
 //             BF16, 128-byte swizzled, written by the producers;
-//   B ring    (5-6 stages): the 64-element slice of up to 128 token rows (x or
-//             h), gathered with cp.async from the L2.
+//   B ring    (4-6 stages): the 64-element slice of up to 128 token rows (x or
+//             h), gathered with cp.async from the L2, 8 lanes per 128-byte row
+//             slice.
 // The accumulators are double-buffered in TMEM, so the epilogue of one tile
 // overlaps the mainloop of the next.  Warp roles:
 //   warp 0          TMEM allocation; lane 0 issues tcgen05.mma and commits
@@ -80,12 +83,15 @@ template <int PHASE>
 struct Cfg {
   static constexpr int NA = PHASE == 0 ? 2 : 1;             // A matrices per tile
   static constexpr int UNITS = NA * BM * BK / 32 / kProducerThreads;  // 16-B code units per producer per step
-  static constexpr int A_STAGES = 2;
-  static constexpr int B_STAGES = PHASE == 0 ? 5 : 6;
-  static constexpr int RAW_DEPTH = PHASE == 0 ? 8 : 12;
+  static constexpr int A_STAGES = PHASE == 0 ? 3 : 4;
+  static constexpr int B_STAGES = PHASE == 0 ? 4 : 6;
+  static constexpr int RW = PHASE == 0 ? 32 : 16;           // weight rows per producer warp
+  static constexpr int RAW_DEPTH = PHASE == 0 ? 3 : 6;      // super-steps (two k-steps) in flight
   static constexpr int A_BYTES = BM * BK * 2;               // 16 KB per matrix
   static constexpr int B_BYTES = BN * BK * 2;               // 16 KB
-  static constexpr int RAW_STEP = kProducerThreads * (UNITS * 16 + 4);
+  static constexpr int RAW_ROW = 64;                        // code bytes of one row per super-step
+  static constexpr int RAW_WARP = RW * (RAW_ROW + 8);       // one super-step of one warp: codes, then 8 scale bytes per row
+  static constexpr int RAW_STEP = 8 * RAW_WARP;             // one super-step of all producer warps
   static constexpr int ACC_COLS = NA * BN;                  // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;            // double-buffered: 512 or 256
   static constexpr size_t OFF_A = 0;
@@ -97,6 +103,7 @@ struct Cfg {
   static constexpr size_t SMEM = 1024 /*align*/ + OFF_COLS + 2 * BN * 12;
 };
 static_assert(Cfg<0>::UNITS == 2 && Cfg<1>::UNITS == 1, "producer split");
+static_assert(Cfg<0>::RW * 8 == 2 * BM && Cfg<1>::RW * 8 == BM, "rows of the producer warps");
 static_assert(Cfg<0>::SMEM <= 232448 && Cfg<1>::SMEM <= 232448, "shared memory");
 
 __device__ __forceinline__ int4 tile_of(const GroupedArgs& a, int tile, int MT, int& mt) {
@@ -118,6 +125,9 @@ __device__ __forceinline__ void cp16_l2pf(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // 32 e2m1 codes (16 bytes) x one or two block scales -> 32 BF16 (exact), as
@@ -281,15 +291,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     __syncwarp();
   } else if (warp < kProdWarp0) {
     // ------------------------------------------------------------- B gatherers
-    // Thread lid owns rows lid and lid + 64 of every tile's B slice; it keeps
-    // up to B_STAGES - 1 steps of cp.async in flight and signals a stage full
-    // once its own copies of that stage have landed.
+    // Thread lid copies 16-byte chunk c = lid % 8 of rows n = lid / 8 + 8 i
+    // (i < 16) of every step's B slice, so the 8 lanes of one row read its 128
+    // contiguous bytes and one instruction covers 4 rows.  A stage is signalled
+    // full once its copies have landed, which the thread checks for its oldest
+    // step in flight before it blocks on a free slot (never after), so the MMA
+    // is never kept waiting on a later issue.
     constexpr int kDepth = C::B_STAGES - 1;
+    constexpr int kRowsPerThread = BN / 8;
     const int lid = threadIdx.x - 32;
+    const int c = lid & 7, rb = lid >> 3;
     int pending = 0;
     int cur_tile = -1;
-    const uint16_t* src_row[2] = {a.x, a.x};
-    uint32_t src_bytes[2] = {0, 0};
+    const uint16_t* src_row[kRowsPerThread];
+    uint32_t row_mode = 0;  // bit i: row i is copied (else skipped); bit 16 + i: zero-filled
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) src_row[i] = a.x;
     bool alive = true;
     for (int gs = 0; gs < my_steps; ++gs) {
       const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
@@ -299,21 +316,28 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
         int mt;
         const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
         const int n_rows = max(16, (ti.z + 15) & ~15);
+        row_mode = 0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = lid + 64 * h;
-          src_bytes[h] = n < ti.z ? 16u : 0u;  // rows past the tile's tokens are zero-filled
-          src_row[h] = a.x;
+        for (int i = 0; i < kRowsPerThread; ++i) {
+          const int n = rb + 8 * i;
+          src_row[i] = a.x;
           if (n < ti.z) {
             if (PHASE == 0) {
               const int p = __ldg(a.pairs + ti.y + n);
-              src_row[h] = a.x + (size_t)(p / a.k) * a.H;
+              src_row[i] = a.x + (size_t)(p / a.k) * a.H;
             } else {
-              src_row[h] = a.hbuf + (size_t)(ti.y + n) * a.I;
+              src_row[i] = a.hbuf + (size_t)(ti.y + n) * a.I;
             }
           }
-          if (n >= n_rows) src_bytes[h] = 0xFFFFFFFFu;  // row not part of this tile's MMA
+          if (n < n_rows) row_mode |= 1u << i;              // rows past n_rows are not part of the MMA
+          if (n >= ti.z && n < n_rows) row_mode |= 1u << (16 + i);  // padding rows of the MMA: zeros
         }
+      }
+      if (pending == kDepth) {  // signal the oldest step in flight first
+        cp_async_wait<kDepth - 1>();
+        fence_proxy_async();
+        mbar_arrive(&b_full[(gs - kDepth) % C::B_STAGES]);
+        --pending;
       }
       if (*abort_flag || !mbar_wait(&b_empty[bs], ((gs / C::B_STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
         fail();
@@ -321,23 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
         break;
       }
       const uint32_t b_addr = smem_u32(sB + (size_t)bs * C::B_BYTES);
+      const uint32_t sw = (uint32_t)((c ^ rb) << 4);  // the 128-byte swizzle: n & 7 == rb
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (src_bytes[h] == 0xFFFFFFFFu) continue;
-        const int n = lid + 64 * h;
-        const uint16_t* src = src_row[h] + (src_bytes[h] ? ks * BK : 0);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          cp_async16(b_addr + n * 128 + ((ch ^ (n & 7)) << 4), src + (src_bytes[h] ? ch * 8 : 0), src_bytes[h]);
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        if (!(row_mode & (1u << i))) continue;
+        const int n = rb + 8 * i;
+        const bool zero = (row_mode >> (16 + i)) & 1u;
+        cp_async16(b_addr + n * 128 + sw, src_row[i] + (zero ? 0 : ks * BK + c * 8), zero ? 0u : 16u);
       }
       cp_async_commit();
       ++pending;
-      if (pending > kDepth) {
-        cp_async_wait<kDepth>();
-        fence_proxy_async();
-        mbar_arrive(&b_full[(gs - kDepth) % C::B_STAGES]);
-        --pending;
-      }
     }
     cp_async_wait<0>();
     fence_proxy_async();
@@ -346,99 +363,127 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_kernel(GroupedArgs a) {
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------ A producers
-    // Phase 0: thread (matrix m, row r) dequantises 64 elements per step (two
-    // 16-byte code units, one 4-byte scale word); phase 1: thread (row r,
-    // half) dequantises 32 elements (one unit).  Each thread fetches exactly
-    // the bytes it will convert into its private slot of the raw ring,
-    // RAW_DEPTH steps ahead, and waits for them with its own cp.async groups.
-    const int pid = threadIdx.x - kProdWarp0 * 32;  // 0..255
-    const int m = PHASE == 0 ? pid >> 7 : 0;
-    const int r = PHASE == 0 ? (pid & 127) : (pid >> 1);
-    const int half = PHASE == 0 ? 0 : (pid & 1);
-    const int c0 = half * 32;                      // first element of the thread inside the step
+    // Phase 0: warp pw owns the 32 rows (pw & 3) * 32 .. +31 of matrix pw >> 2
+    // (gate, up), lane = row, 64 elements per step (two 16-byte code units and
+    // four E4M3 or two UE8M0 scale bytes); phase 1: warp pw owns rows pw * 16
+    // .. +15, lane = (row, half), 32 elements per step.  The warp fetches its
+    // rows' codes and scales two k-steps (a super-step) at a time into its own
+    // slot of the raw ring, RAW_DEPTH super-steps ahead: lanes take
+    // consecutive 16-byte pieces of the rows (64 contiguous bytes per row,
+    // piece p of row rr stored at position p ^ ((rr >> 1) & 3), so that the
+    // lanes' reads and writes spread over the banks), and each row's 8 (or 4)
+    // scale bytes with one copy.  Each lane waits for its own
+    // copies (cp.async groups), then the warp synchronises so every lane sees
+    // the whole slot.
+    const int pw = warp - kProdWarp0;  // 0..7
+    const int pid = threadIdx.x - kProdWarp0 * 32;
+    const int m = PHASE == 0 ? pw >> 2 : 0;
+    const int rbase = PHASE == 0 ? (pw & 3) * 32 : pw * 16;  // first row of the warp in the tile
+    const int r_local = PHASE == 0 ? lane : lane >> 1;       // this lane's row in the warp
+    const int r = rbase + r_local;
+    const int half = PHASE == 0 ? 0 : (lane & 1);
+    const int c0 = half * 32;  // first element of the lane inside the step
     const size_t coff = PHASE == 0 ? (m == 0 ? ro.gate : ro.up) : ro.down;
     const size_t soff = PHASE == 0 ? (m == 0 ? ro.gate_s : ro.up_s) : ro.down_s;
-    const uint32_t raw0 = smem_u32(sRaw);
-    // tile lookups for the fetches (RAW_DEPTH steps ahead of the conversions)
+    const uint32_t raw_w = smem_u32(sRaw) + (uint32_t)(pw * C::RAW_WARP);
+    const uint8_t* raw_wp = sRaw + (size_t)pw * C::RAW_WARP;
+    constexpr int kSB = 128 / G;  // scale bytes of one row per super-step (8 or 4)
+    const int nss = my_steps / 2;  // super-steps (KSTEPS is even: K % 128 == 0)
     int f_tile = -1;
     const uint8_t* f_rec = nullptr;
-    size_t f_row = 0;
-    auto fetch = [&](int gs) {  // step gs -> raw slot gs % RAW_DEPTH, then commit
-      if (gs < my_steps) {
-        const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
+    size_t f_row0 = 0;
+    auto fetch = [&](int ss) {  // super-step ss -> raw slot ss % RAW_DEPTH, then commit
+      if (ss < nss) {
+        const int lt = (2 * ss) / KSTEPS, ks = 2 * ss - lt * KSTEPS;
         if (lt != f_tile) {
           f_tile = lt;
           int mt;
           const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
           f_rec = tile_record(a, ti.x);
-          f_row = (size_t)mt * BM + r;
+          f_row0 = (size_t)mt * BM + rbase;
         }
-        const uint32_t slot = raw0 + (uint32_t)((gs % C::RAW_DEPTH) * C::RAW_STEP);
         if (f_rec != nullptr) {
-          const uint8_t* cp = f_rec + coff + f_row * (size_t)(K / 2) + (size_t)(ks * BK + c0) / 2;
+          const uint32_t slot = raw_w + (uint32_t)((ss % C::RAW_DEPTH) * C::RAW_STEP);
 #pragma unroll
-          for (int u = 0; u < C::UNITS; ++u) cp16_l2pf(slot + (u * kProducerThreads + pid) * 16, cp + 16 * u);
-          // the aligned 4-byte word holding the thread's scale bytes (records
-          // are a multiple of 4 bytes long, so the word stays inside it)
-          const size_t so = soff + f_row * (size_t)(K / G) + (size_t)(ks * BK + c0) / G;
-          cp4(slot + C::UNITS * kProducerThreads * 16 + pid * 4, f_rec + (so & ~(size_t)3));
+          for (int i = 0; i < C::RW * 4 / 32; ++i) {
+            const int ch = i * 32 + lane, rr = ch >> 2, part = ch & 3;
+            cp16_l2pf(slot + rr * C::RAW_ROW + ((part ^ ((rr >> 1) & 3)) << 4),
+                      f_rec + coff + (f_row0 + rr) * (size_t)(K / 2) + (size_t)ks * (BK / 2) + part * 16);
+          }
+          if (lane < C::RW) {
+            const uint8_t* sp = f_rec + soff + (f_row0 + lane) * (size_t)(K / G) + (size_t)ks * (BK / G);
+            if (kSB == 8) cp8(slot + C::RW * C::RAW_ROW + lane * 8, sp);
+            else cp4(slot + C::RW * C::RAW_ROW + lane * 8, sp);
+          }
         }
       }
-      cp_async_commit();  // one group per step, empty or not, so the group count stays aligned
+      cp_async_commit();  // one group per super-step, empty or not, so the group count stays aligned
     };
-    for (int s = 0; s < C::RAW_DEPTH; ++s) fetch(s);
+    for (int ss = 0; ss < C::RAW_DEPTH; ++ss) fetch(ss);
     int c_tile = -1;
     bool poison = false;
-    uint32_t sshift = 0;
-    for (int gs = 0; gs < my_steps; ++gs) {
-      const int lt = gs / KSTEPS, ks = gs - lt * KSTEPS;
-      if (lt != c_tile) {
-        c_tile = lt;
-        int mt;
-        const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
-        const uint8_t* rec = tile_record(a, ti.x);
-        poison = rec == nullptr;
-        if (poison && pid == 0)
-          moe::status_or(a.st, a.ptrs[ti.x] == nullptr ? MOE_DEV_NULL_EXPERT : MOE_DEV_MISALIGNED);
-      }
-      {
-        const size_t so = (size_t)r * (size_t)(K / G) + (size_t)(ks * BK + c0) / G;  // alignment only
-        sshift = (uint32_t)(so & 3u) * 8u;
-      }
-      // this step's raw bytes: the oldest of the RAW_DEPTH groups in flight
+    bool alive = true;
+    for (int ss = 0; ss < nss && alive; ++ss) {
+      // this super-step's raw bytes: the oldest of the RAW_DEPTH groups in flight
       asm volatile("cp.async.wait_group %0;" ::"n"(C::RAW_DEPTH - 1) : "memory");
-      const uint8_t* slot = sRaw + (size_t)(gs % C::RAW_DEPTH) * C::RAW_STEP;
-      uint4 q[C::UNITS];
+      __syncwarp();
+      const uint8_t* slot = raw_wp + (size_t)(ss % C::RAW_DEPTH) * C::RAW_STEP;
+      const uint2 sw8 = *reinterpret_cast<const uint2*>(slot + C::RW * C::RAW_ROW + r_local * 8);
 #pragma unroll
-      for (int u = 0; u < C::UNITS; ++u)
-        q[u] = *reinterpret_cast<const uint4*>(slot + (u * kProducerThreads + pid) * 16);
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(slot + C::UNITS * kProducerThreads * 16 + pid * 4) >> sshift;
-      uint4 out[C::UNITS][4];
-#pragma unroll
-      for (int u = 0; u < C::UNITS; ++u) {
-        const uint4 qq = poison ? make_uint4(0u, 0u, 0u, 0u) : q[u];
-        const uint32_t sb = poison ? 0u : (FMT == MOE_FMT_NVFP4 ? (sw >> (16 * u)) & 0xFFFFu : (sw >> (8 * u)) & 0xFFu);
-        if constexpr (kF16) dequant_unit_f16(qq, sb, poison, out[u]);
-        else dequant_unit_bf16<FMT>(qq, sb, poison, out[u]);
-      }
-      const int as = gs % C::A_STAGES;
-      if (*abort_flag || !mbar_wait(&a_empty[as], ((gs / C::A_STAGES) & 1) ^ 1, globaltimer() + kWaitNs)) {
-        fail();
-        break;
-      }
-      uint8_t* row_base = sA + (size_t)as * C::NA * C::A_BYTES + (size_t)m * C::A_BYTES + (size_t)r * 128;
-#pragma unroll
-      for (int u = 0; u < C::UNITS; ++u)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int ch = (c0 / 8) + u * 4 + c;  // 16-byte chunk of the 128-byte row
-          *reinterpret_cast<uint4*>(row_base + ((ch ^ (r & 7)) << 4)) = out[u][c];
+      for (int j = 0; j < 2; ++j) {
+        const int gs = 2 * ss + j;
+        const int lt = gs / KSTEPS;
+        if (lt != c_tile) {
+          c_tile = lt;
+          int mt;
+          const int4 ti = tile_of(a, blockIdx.x + lt * gridDim.x, MT, mt);
+          const uint8_t* rec = tile_record(a, ti.x);
+          poison = rec == nullptr;
+          if (poison && pid == 0)
+            moe::status_or(a.st, a.ptrs[ti.x] == nullptr ? MOE_DEV_NULL_EXPERT : MOE_DEV_MISALIGNED);
         }
-      fence_proxy_async();
-      mbar_arrive(&a_full[as]);
-      // the raw slot has been read and its values stored: refill it with the
-      // step RAW_DEPTH ahead
-      fetch(gs + C::RAW_DEPTH);
+        uint4 q[C::UNITS];
+#pragma unroll
+        for (int u = 0; u < C::UNITS; ++u)
+          q[u] = *reinterpret_cast<const uint4*>(slot + r_local * C::RAW_ROW +
+                                                 (((2 * j + half + u) ^ ((r_local >> 1) & 3)) << 4));
+        // scale bytes of the step: NVFP4 4 per step (2 per half), MXFP4 2 per step (1 per half)
+        const uint32_t sword = j == 0 ? sw8.x : sw8.y;  // NVFP4: bytes of step j; MXFP4: both steps in sw8.x
+        uint32_t sstep;
+        if (FMT == MOE_FMT_NVFP4) sstep = sword >> (16 * half);
+        else sstep = sw8.x >> (16 * j + 8 * half);
+        uint4 out[C::UNITS][4];
+#pragma unroll
+        for (int u = 0; u < C::UNITS; ++u) {
+          const uint4 qq = poison ? make_uint4(0u, 0u, 0u, 0u) : q[u];
+          const uint32_t sb =
+              poison ? 0u : (FMT == MOE_FMT_NVFP4 ? (sstep >> (16 * u)) & 0xFFFFu : (sstep >> (8 * u)) & 0xFFu);
+          if constexpr (kF16) dequant_unit_f16(qq, sb, poison, out[u]);
+          else dequant_unit_bf16<FMT>(qq, sb, poison, out[u]);
+        }
+        const int as = gs % C::A_STAGES;
+        // the outcome is made warp-uniform: the warp synchronises again below
+        const bool ok = __all_sync(0xffffffffu, !*abort_flag &&
+                                   mbar_wait(&a_empty[as], ((gs / C::A_STAGES) & 1) ^ 1, globaltimer() + kWaitNs));
+        if (!ok) {
+          if (lane == 0) fail();
+          alive = false;
+          break;
+        }
+        uint8_t* row_base = sA + (size_t)as * C::NA * C::A_BYTES + (size_t)m * C::A_BYTES + (size_t)r * 128;
+#pragma unroll
+        for (int u = 0; u < C::UNITS; ++u)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int ch = (c0 / 8) + u * 4 + cc;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(row_base + ((ch ^ (r & 7)) << 4)) = out[u][cc];
+          }
+        fence_proxy_async();
+        mbar_arrive(&a_full[as]);
+      }
+      // every lane has read the slot: refill it with the super-step RAW_DEPTH ahead
+      __syncwarp();
+      if (alive) fetch(ss + C::RAW_DEPTH);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else {

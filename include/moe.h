@@ -165,11 +165,12 @@ size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s);
  * Limits: T*k <= 4096, k*I <= 49152.
  * Residency: the one-shot and ring kernels run one CTA per SM with grid-wide
  * barriers, so all of their CTAs must be resident at once.  The library
- * checks on the host that one CTA fits on an SM (else MOE_ERR_CUDA); kernels
- * of other streams, processes (MPS) or green contexts that hold SMs for the
- * whole call can still keep CTAs out, and the barrier waits then run out
- * (2 s) with MOE_DEV_TIMEOUT and NaN outputs.  Do not run such persistent
- * kernels concurrently with this call. */
+ * checks on the host that one CTA fits on an SM (else MOE_ERR_CUDA).  The
+ * launches are not cooperative (that would add host time to every launch),
+ * so kernels of other streams, processes (MPS) or green contexts that hold
+ * SMs for the whole call can keep CTAs out: the barrier waits then run out
+ * (2 s) with MOE_DEV_TIMEOUT and NaN outputs rather than hang.  Do not run
+ * such persistent kernels concurrently with this call. */
 int moe_experts_decode(const uint16_t* x_bf16, const int32_t* idx, const float* weights,
                        int T, int k, const void* const* expert_ptrs, int E,
                        moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,

@@ -158,19 +158,36 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       asm volatile("bar.sync 3, %0;" ::"n"(kThreads) : "memory");  // the router's records are in place
     }
     asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");  // barriers set up, records in place
-    // one copy per lane; a copy of a missing record still arrives (0 bytes)
+    // One copy per lane; a copy of a missing record still arrives (0 bytes).
+    // The gate/up pieces and scales go first.  The down rows are needed only
+    // after the second grid barrier, so they are issued once the gate/up bytes
+    // have landed: issued together, they would share the HBM stream with the
+    // gate/up bytes and delay the gate/up pass by about a third.
     const uint32_t base = tc::smem_u32(smem);
-    for (int c = lane; c < tb.ncopies; c += 32) {
-      const uint8_t* rec = tb.recs[tb.cpair[c]];
-      uint64_t* bar = &bars[tb.cbar[c]];
-      tc::mbar_arrive_expect_tx(bar, rec ? tb.cbytes[c] : 0u);
-      if (rec) tc::bulk_g2s(base + tb.cdst[c], rec + tb.csrc[c], tb.cbytes[c], bar);
-    }
+    auto issue_if = [&](auto take) {
+      for (int c = lane; c < tb.ncopies; c += 32) {
+        if (!take((int)tb.cbar[c])) continue;
+        const uint8_t* rec = tb.recs[tb.cpair[c]];
+        uint64_t* bar = &bars[tb.cbar[c]];
+        tc::mbar_arrive_expect_tx(bar, rec ? tb.cbytes[c] : 0u);
+        if (rec) tc::bulk_g2s(base + tb.cdst[c], rec + tb.csrc[c], tb.cbytes[c], bar);
+      }
+    };
+    issue_if([](int b) { return b != kBarDown; });
     if (lane == 0) {
-      for (int i = 0; i < kNumBars; ++i) tc::mbar_arrive(&bars[i]);
-      // no copy may still be in flight when the CTA exits
+      for (int i = 0; i < kNumBars; ++i)
+        if (i != kBarDown) tc::mbar_arrive(&bars[i]);
+      // bounded: the down copies are issued whether or not these land in time
       const uint64_t dl = tc::globaltimer() + a.wait_ns;
-      for (int i = 0; i < kNumBars; ++i) tc::mbar_wait_backoff(&bars[i], 0, dl);
+      for (int i = 0; i < kNumBars; ++i)
+        if (i != kBarDown) tc::mbar_wait_backoff(&bars[i], 0, dl);
+    }
+    __syncwarp();
+    issue_if([](int b) { return b == kBarDown; });
+    if (lane == 0) {
+      tc::mbar_arrive(&bars[kBarDown]);
+      // no copy may still be in flight when the CTA exits
+      tc::mbar_wait_backoff(&bars[kBarDown], 0, tc::globaltimer() + a.wait_ns);
     }
     __syncthreads();
     return;

@@ -1060,13 +1060,30 @@ def cpu_baseline_prompt(budget_s: float):
             "seconds": round(busy, 2)}
 
 
+def _oracle_sample_one_thread(budget_s: float):
+    """The same bounded sample with the oracle's BLAS limited to one thread
+    (a fresh interpreter, so the limit is in place before numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_sample(%r)))" % (ROOT, float(budget_s)))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    nbytes, secs, layers = json.loads(r.stdout.strip().splitlines()[-1])
+    return nbytes, secs, layers
+
+
 def cpu_baseline(budget_s: float):
     nbytes, secs, layers = _oracle_sample(budget_s)
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": _cores(),
-            "kind": "oracle",
-            "sample": f"{layers} layers of the decode stack for 1 token (router + 10 experts + "
-                      f"RMS chaining per layer), float64 numpy; record packing untimed",
-            "seconds": round(secs, 2)}
+    out = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": _cores(),
+           "kind": "oracle",
+           "sample": f"{layers} layers of the decode stack for 1 token (router + 10 experts + "
+                     f"RMS chaining per layer), float64 numpy; record packing untimed",
+           "seconds": round(secs, 2)}
+    try:
+        n1, s1, l1 = _oracle_sample_one_thread(budget_s / 2)
+        out["one_thread"] = {"value": round(n1 / s1 / 1e9, 4), "cores": 1, "layers": l1, "seconds": round(s1, 2)}
+    except Exception as exc:  # report, do not hide
+        out["one_thread"] = {"error": repr(exc)[:200]}
+    return out
 
 
 def run_reference(args):

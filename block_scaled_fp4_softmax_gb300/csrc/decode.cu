@@ -923,6 +923,51 @@ extern "C" int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int
   return launch_decode_oneshot(oa, s.format, sm_count(), stream);
 }
 
+// A whole decode stack in one launch: layer 0 routes x0, every later layer
+// RMS-chains the previous layer's y; the layers are separated by grid
+// barriers inside one persistent kernel instead of launch boundaries.
+extern "C" int moe_decode_stack(const uint16_t* x0, int T, double eps, int layers, const uint16_t* wr_bf16,
+                                const float* bias, int E, int k, const void* const* expert_ptrs,
+                                moe_expert_shape s, int32_t* idx, float* weights, float* logits, uint16_t* x_out,
+                                float* y, void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (!x0 || !wr_bf16 || !idx || !weights || !logits || !expert_ptrs || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || layers <= 0 || layers > 4096 || E <= 0 || k <= 0 || k > E || k > 32 || !(eps >= 0.0))
+    return MOE_ERR_INVALID_ARG;
+  if (!moe::shape_ok(s) || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_experts_decode_workspace(T, k, s)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!moe::aligned16(x0) || (x_out && !moe::aligned16(x_out)) || !moe::aligned16(wr_bf16) ||
+      !moe::aligned16(workspace))
+    return MOE_ERR_ALIGNMENT;
+  if (sm_count() <= 0) return MOE_ERR_CUDA;
+  if (!decode_oneshot_fits(T, k, s.hidden, s.inter, s.format, sm_count(), (size_t)stream_smem_limit(), true, E))
+    return MOE_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeOneshotArgs oa = {};
+  oa.x = x0;
+  oa.T = T;
+  oa.k = k;
+  oa.ptrs = expert_ptrs;
+  oa.E = E;
+  oa.H = s.hidden;
+  oa.I = s.inter;
+  oa.bar = reinterpret_cast<unsigned long long*>(ws);
+  oa.hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
+  oa.y = y;
+  oa.status = dev_status;
+  oa.y_prev = nullptr;
+  oa.eps = (float)eps;
+  oa.x_out = x_out;
+  oa.wr = wr_bf16;
+  oa.bias = bias;
+  oa.logits = logits;
+  oa.idx_out = idx;
+  oa.w_out = weights;
+  oa.layers = layers;
+  return launch_decode_oneshot(oa, s.format, sm_count(), stream);
+}
+
 // ---------------------------------------------------------------------------
 // Decode without any caller-side or library-side allocation.
 //

@@ -37,14 +37,27 @@
 namespace moe {
 namespace os {
 
-// Waits (bounded by wait_ns) for one barrier's parity-0 phase; on timeout
-// flags the launch and returns false.
-__device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status, uint64_t wait_ns) {
+// Where a bounded wait gave up: the first one in the launch's workspace
+// (byte 128 of the header, a 64-bit word that stays zero while every wait
+// succeeds) gets site << 56 | (layer + 1) << 32 | block.
+enum WaitSite : unsigned {
+  kSiteRouter = 1, kSiteScales, kSitePiece, kSiteDown, kSiteGrid1, kSiteGrid2, kSiteLayer, kSiteLoader
+};
+__device__ __forceinline__ void note_timeout(unsigned long long* bar, unsigned site, int layer) {
+  unsigned long long* diag = bar + 16;
+  atomicCAS(diag, 0ull, (unsigned long long)site << 56 | (unsigned long long)(layer + 1) << 32 | blockIdx.x);
+}
+
+// Waits (bounded by wait_ns) for the phase of one barrier with the given
+// parity; on timeout flags the launch, records the site and returns false.
+__device__ __forceinline__ bool await(uint64_t* bar, uint32_t parity, Tab& tb, const DecodeOneshotArgs& a,
+                                      unsigned site, int layer) {
   volatile int* abort_flag = tb.flags;
   if (*abort_flag) return false;
-  if (tc::mbar_wait(bar, 0, tc::globaltimer() + wait_ns)) return true;
+  if (tc::mbar_wait(bar, parity, tc::globaltimer() + a.wait_ns)) return true;
   *abort_flag = 1;
-  status_or(status, MOE_DEV_TIMEOUT);
+  status_or(a.status, MOE_DEV_TIMEOUT);
+  note_timeout(a.bar, site, layer);
   return false;
 }
 
@@ -56,36 +69,99 @@ __device__ __forceinline__ bool await(uint64_t* bar, Tab& tb, int32_t* status, u
 // counter at the start of the launch, rounded down to a multiple of the
 // grid: every earlier launch has passed all its barriers by then, and each
 // CTA reads the counter before its own first arrival, so fewer than grid
-// arrivals of this launch can precede the read.  False on timeout, which
-// also flags the launch.
-__device__ bool grid_sync_thread(unsigned long long* bar, unsigned long long target, Tab& tb, int32_t* status,
-                                 uint64_t wait_ns) {
+// arrivals of this launch can precede the read.  `between` runs after the
+// arrival and before the poll (work that overlaps the wait without holding
+// up the release).  False on timeout, which also flags the launch.
+template <class F>
+__device__ __forceinline__ bool grid_sync_thread(unsigned long long target, Tab& tb, const DecodeOneshotArgs& a,
+                                                 unsigned site, int layer, F&& between) {
   volatile int* abort_flag = tb.flags;
   int good = !*abort_flag;
   if (good) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
-    const uint64_t dl = global_ns() + wait_ns;
-    while (dm::ld_acquire_u64(bar) < target) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(a.bar) : "memory");
+    between();
+    const uint64_t dl = global_ns() + a.wait_ns;
+    while (dm::ld_acquire_u64(a.bar) < target) {
       if (global_ns() > dl) {
         good = 0;
+        note_timeout(a.bar, site, layer);
         break;
       }
     }
   }
   if (!good) {
     *abort_flag = 1;
-    status_or(status, MOE_DEV_TIMEOUT);
+    status_or(a.status, MOE_DEV_TIMEOUT);
   }
   return good;
 }
+__device__ __forceinline__ bool grid_sync_thread(unsigned long long target, Tab& tb, const DecodeOneshotArgs& a,
+                                                 unsigned site, int layer) {
+  return grid_sync_thread(target, tb, a, site, layer, [] {});
+}
 
-template <int FMT, int UPR, int UPDR>
+// The CTA's share of the router rows of a fused launch: experts
+// [re0, re0 + rne) of E, epc per CTA.
+struct RouterShare {
+  int re0, rne;
+  uint32_t wr_bytes;
+};
+__device__ __forceinline__ RouterShare router_share(const DecodeOneshotArgs& a, bool fused) {
+  const int epc = (a.E + (int)gridDim.x - 1) / (int)gridDim.x;
+  RouterShare r;
+  r.re0 = blockIdx.x * epc;
+  r.rne = fused ? max(0, min(epc, a.E - r.re0)) : 0;
+  r.wr_bytes = (uint32_t)r.rne * (uint32_t)a.H * 2u;
+  return r;
+}
+// The pointer table goes to shared memory with the router rows when the
+// rows are staged and the table's bulk copy is 16-byte aligned.
+__device__ __forceinline__ bool ptrs_staged(const DecodeOneshotArgs& a) {
+  return a.geo.rstage != 0 && (reinterpret_cast<uintptr_t>(a.ptrs) & 15u) == 0 && (a.E & 1) == 0;
+}
+
+// Thread 0: bulk copies of layer l's router rows of this CTA and of the
+// pointer table into the x/h region, completing one phase of `bar` (set up
+// here for layer 0).
+__device__ __forceinline__ void stage_router(const DecodeOneshotArgs& a, uint8_t* smem, uint64_t* bar, int l) {
+  const RouterShare r = router_share(a, true);
+  if (l == 0) {
+    tc::mbar_init(bar, 1);
+    tc::mbar_fence_init();
+  }
+  const uint32_t ptr_bytes = ptrs_staged(a) ? (uint32_t)a.E * 8u : 0u;
+  tc::mbar_arrive_expect_tx(bar, r.wr_bytes + ptr_bytes);
+  if (r.wr_bytes)
+    tc::bulk_g2s(tc::smem_u32(smem + a.geo.off_act), a.wr + ((size_t)l * a.E + r.re0) * a.H, r.wr_bytes, bar);
+  if (ptr_bytes)
+    tc::bulk_g2s(tc::smem_u32(smem + a.geo.off_act + r.wr_bytes), a.ptrs + (size_t)l * a.E, ptr_bytes, bar);
+}
+
+// STACK: the launch runs a.layers layers (a whole-stack launch); otherwise
+// exactly one, and the layer loop compiles away.
+template <int FMT, int UPR, int UPDR, bool STACK>
 __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   pdl_launch_dependents();
+  // A launch runs a.layers >= 1 layers (more than one only for a whole-layer
+  // launch, moe_decode_stack): layer 0 from a.x or a.y_prev, every later layer
+  // RMS-chained from the previous layer's y.  Layer L uses grid barriers
+  // 3L + 1 and 3L + 2, and barrier 3L + 3 publishes its y to the next layer.
+  // The mbarriers are set up once; each completes one phase per layer, so
+  // layer L waits for the phase of parity L & 1.
+  const int nl = STACK ? a.layers : 1;
+  for (int L = 0; L < nl; ++L) {
+  const uint32_t ph = (uint32_t)L & 1u;
+  const uint16_t* L_wr = a.wr ? a.wr + (size_t)L * a.E * a.H : nullptr;
+  const void* const* L_ptrs = a.ptrs + (size_t)L * a.E;
+  const float* L_bias = a.bias ? a.bias + (size_t)L * a.E : nullptr;
+  const uint16_t* L_x = L == 0 ? a.x : nullptr;
+  const float* L_yprev = L == 0 ? a.y_prev : a.y;
+  int32_t* L_idx_out = a.idx_out ? a.idx_out + (size_t)L * a.T * a.k : nullptr;
+  float* L_w_out = a.w_out ? a.w_out + (size_t)L * a.T * a.k : nullptr;
   constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
-  const bool fused = a.wr != nullptr;
+  const bool fused = L_wr != nullptr;
   const Geo& g = a.geo;
   const RecordOffsets o = record_offsets(a.H, a.I, FMT);
   const int upr = UPR > 0 ? UPR : a.H >> 5;
@@ -104,41 +180,39 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // router rows of this CTA's experts (fused launch) and the pointer table:
   // neither depends on the previous kernel, so they are fetched before the
   // wait for it -- into shared memory (the x/h region, which they leave
-  // before x arrives there) when the plan has room, else into L2
-  const int epc = (a.E + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int re0 = blockIdx.x * epc, rne = fused ? max(0, min(epc, a.E - re0)) : 0;
-  const uint32_t wr_bytes = (uint32_t)rne * (uint32_t)a.H * 2u;
+  // before x arrives there) when the plan has room, else into L2.  Layer
+  // L + 1's are fetched during the barrier at the end of layer L.
+  const RouterShare rs = router_share(a, fused);
+  const int re0 = rs.re0, rne = rs.rne;
+  const uint32_t wr_bytes = rs.wr_bytes;
   const bool rstaged = g.rstage != 0;
-  const bool pstaged = rstaged && (reinterpret_cast<uintptr_t>(a.ptrs) & 15u) == 0 && (a.E & 1) == 0;
-  if (threadIdx.x == 0) {
-    tb.flags[0] = 0;
-    tb.flags[1] = 0;
-    if (rstaged) {
-      tc::mbar_init(&bars[kBarRouter], 1);
-      tc::mbar_fence_init();
-      const uint32_t ptr_bytes = pstaged ? (uint32_t)a.E * 8u : 0u;
-      tc::mbar_arrive_expect_tx(&bars[kBarRouter], wr_bytes + ptr_bytes);
-      if (wr_bytes) tc::bulk_g2s(tc::smem_u32(smem + g.off_act), a.wr + (size_t)re0 * a.H, wr_bytes, &bars[kBarRouter]);
-      if (ptr_bytes) tc::bulk_g2s(tc::smem_u32(smem + g.off_act + wr_bytes), a.ptrs, ptr_bytes, &bars[kBarRouter]);
-    }
-  }
-  if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
+  const bool pstaged = ptrs_staged(a);
   if (!pstaged)
     for (int i = threadIdx.x; i < (a.E * 8 + 127) / 128; i += kThreads)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(a.ptrs) + (size_t)i * 128));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(L_ptrs) + (size_t)i * 128));
   if (!rstaged) {
-    const char* wb = fused ? reinterpret_cast<const char*>(a.wr + (size_t)re0 * a.H) : nullptr;
+    const char* wb = fused ? reinterpret_cast<const char*>(L_wr + (size_t)re0 * a.H) : nullptr;
     for (size_t off = (size_t)threadIdx.x * 128; off < wr_bytes; off += (size_t)kThreads * 128)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
   }
-  __syncthreads();
+  if (L == 0) {
+    // later layers are reset at the end of the previous one
+    if (threadIdx.x == 0) {
+      tb.flags[0] = 0;  // a wait that ran out stays flagged for the launch's later layers
+      tb.flags[1] = 0;
+      if (rstaged) stage_router(a, smem, &bars[kBarRouter], 0);
+    }
+    if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
+    __syncthreads();
+  }
 
   if (warp == kCWarps) {
     // ------------------------------------------------------------ loader
     // The plan of the CTA's copies has no data dependence: lane 0 builds it
     // (and the barriers' arrival counts: one per copy, plus one by lane 0 on
     // every barrier) while, in a fused launch, warps 0-14 run the router.
-    if (lane == 0) {
+    // It is the same for every layer.
+    if (lane == 0 && L == 0) {
       uint32_t n_scale, n_down;
       build_tables(g, blockIdx.x, o, tb, n_scale, n_down);
       for (int i = 0; i < kMaxPieces; ++i) tc::mbar_init(&bars[i], i < tb.npieces ? 3u : 1u);
@@ -147,10 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       tc::mbar_fence_init();
     }
     __syncwarp();
-    pdl_wait();
+    if (L == 0) pdl_wait();
     if (!fused) {
       for (int p = lane; p < P; p += 32) {
-        tb.recs[p] = dm::checked_record(a.idx[p], a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr);
+        tb.recs[p] = dm::checked_record(a.idx[p], a.E, L_ptrs, blockIdx.x == 0 ? a.status : nullptr);
         tb.wts[p] = a.w[p];
       }
       __syncwarp();
@@ -173,33 +247,47 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
         if (rec) tc::bulk_g2s(base + tb.cdst[c], rec + tb.csrc[c], tb.cbytes[c], bar);
       }
     };
-    issue_if([](int b) { return b != kBarDown; });
-    if (lane == 0) {
+    // Once the launch is flagged (a wait gave up), no more copies are issued:
+    // nothing waits for them any more.  Lane 0 decides for the warp.
+    const bool live = __shfl_sync(0xffffffffu, (int)(*abort_flag == 0), 0) != 0;
+    if (live) issue_if([](int b) { return b != kBarDown; });
+    int landed = live;
+    if (lane == 0 && live) {
       for (int i = 0; i < kNumBars; ++i)
         if (i != kBarDown) tc::mbar_arrive(&bars[i]);
-      // bounded: the down copies are issued whether or not these land in time
       const uint64_t dl = tc::globaltimer() + a.wait_ns;
       for (int i = 0; i < kNumBars; ++i)
-        if (i != kBarDown) tc::mbar_wait_backoff(&bars[i], 0, dl);
+        if (i != kBarDown && !tc::mbar_wait_backoff(&bars[i], ph, dl)) landed = 0;
+      if (!landed) {
+        *abort_flag = 1;
+        status_or(a.status, MOE_DEV_TIMEOUT);
+        note_timeout(a.bar, kSiteLoader, L);
+      }
     }
-    __syncwarp();
-    issue_if([](int b) { return b == kBarDown; });
-    if (lane == 0) {
-      tc::mbar_arrive(&bars[kBarDown]);
-      // no copy may still be in flight when the CTA exits
-      tc::mbar_wait_backoff(&bars[kBarDown], 0, tc::globaltimer() + a.wait_ns);
+    if (__shfl_sync(0xffffffffu, landed, 0)) {
+      issue_if([](int b) { return b == kBarDown; });
+      if (lane == 0) {
+        tc::mbar_arrive(&bars[kBarDown]);
+        // no copy may still be in flight when the layer (or the CTA) ends
+        if (!tc::mbar_wait_backoff(&bars[kBarDown], ph, tc::globaltimer() + a.wait_ns)) {
+          *abort_flag = 1;
+          status_or(a.status, MOE_DEV_TIMEOUT);
+          note_timeout(a.bar, kSiteLoader, L);
+        }
+      }
     }
-    __syncthreads();
-    return;
-  }
+  } else {
 
-  pdl_wait();
-  // grid-barrier counter at the start of this launch (thread 0 arrives for
-  // the CTA; a relaxed load, first used at the first barrier, so it stalls
-  // nothing before)
-  unsigned long long bar_start = 0;
-  if (threadIdx.x == 0) bar_start = rt::ld_relaxed_u64(a.bar);
-  auto bar_target = [&](unsigned n) { return (bar_start / gridDim.x + n) * gridDim.x + a.barrier_extra; };
+  if (L == 0) {
+    pdl_wait();
+    // grid-barrier counter at the start of this launch (thread 0 arrives for
+    // the CTA; a relaxed load, first used at the first barrier, so it stalls
+    // nothing before)
+    if (threadIdx.x == 0) tb.bar_base = rt::ld_relaxed_u64(a.bar) / gridDim.x;
+  }
+  auto bar_target = [&](unsigned n) {
+    return (tb.bar_base + 3u * (unsigned)L + n) * gridDim.x + a.barrier_extra;
+  };
 
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
   if (fused) {
@@ -211,35 +299,37 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     // the records through named barrier 3.
     float* rpart = reinterpret_cast<float*>(smem + g.off_xb);
     for (int t = 0; t < a.T; ++t) {
-      if (a.y_prev) {
-        const float* yr = a.y_prev + (size_t)t * a.H;
-        const float r = rt::rms_inv_fixed_order<4, kCThreads>(yr, a.H, a.eps, rpart);
+      if (L_yprev) {
+        const float* yr = L_yprev + (size_t)t * a.H;
+        // a whole-stack launch reads the y it wrote in the previous layer:
+        // through L2 only, as L1 is not coherent across SMs
+        const float r = rt::rms_inv_fixed_order<4, kCThreads, STACK>(yr, a.H, a.eps, rpart);
         for (int i = threadIdx.x; i < a.H; i += kCThreads) {
-          const uint16_t x16 = rt::f32_to_bf16_bits(__fmul_rn(yr[i], r));
+          const uint16_t x16 = rt::f32_to_bf16_bits(__fmul_rn(STACK ? __ldcg(yr + i) : yr[i], r));
           xb[(size_t)t * a.H + i] = x16;
           if (blockIdx.x == 0 && a.x_out) a.x_out[(size_t)t * a.H + i] = x16;
         }
       } else {
         for (int i = threadIdx.x * 8; i < a.H; i += kCThreads * 8) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H + i));
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(L_x + (size_t)t * a.H + i));
           *reinterpret_cast<uint4*>(xb + (size_t)t * a.H + i) = v;
           if (blockIdx.x == 0 && a.x_out) *reinterpret_cast<uint4*>(a.x_out + (size_t)t * a.H + i) = v;
         }
       }
     }
     tc::named_sync(4, kCThreads);
-    const bool rin = !rstaged || await(&bars[kBarRouter], tb, a.status, a.wait_ns);
+    const bool rin = !rstaged || await(&bars[kBarRouter], ph, tb, a, kSiteRouter, L);
     const uint16_t* wsm = reinterpret_cast<const uint16_t*>(smem + g.off_act);
     for (int task = warp; task < a.T * rne; task += kCWarps) {
       const int t = task / rne, q = task - t * rne;
       float v;
       if (rstaged) v = rin ? rt::logit_dot<true>(xb + (size_t)t * a.H, wsm + (size_t)q * a.H, a.H, lane)
                            : __uint_as_float(0x7FC00000u);
-      else v = rt::logit_dot(xb + (size_t)t * a.H, a.wr + (size_t)(re0 + q) * a.H, a.H, lane);
-      if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = a.bias ? __fadd_rn(v, a.bias[re0 + q]) : v;
+      else v = rt::logit_dot(xb + (size_t)t * a.H, L_wr + (size_t)(re0 + q) * a.H, a.H, lane);
+      if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = L_bias ? __fadd_rn(v, L_bias[re0 + q]) : v;
     }
     tc::named_sync(4, kCThreads);
-    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(a.bar, bar_target(1), tb, a.status, a.wait_ns);
+    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(bar_target(1), tb, a, kSiteGrid1, L);
     tc::named_sync(4, kCThreads);
     const bool have_logits = tb.flags[2] != 0;
     unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
@@ -252,13 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
         if (lane < a.k) {
           const int p = t * a.k + lane;
           const void* const* pt =
-              pstaged ? reinterpret_cast<const void* const*>(smem + g.off_act + wr_bytes) : a.ptrs;
+              pstaged ? reinterpret_cast<const void* const*>(smem + g.off_act + wr_bytes) : L_ptrs;
           tb.recs[p] = have_logits && rin ? dm::checked_record(my_e, a.E, pt, blockIdx.x == 0 ? a.status : nullptr)
                                           : nullptr;
           tb.wts[p] = wgt;
           if (blockIdx.x == 0) {
-            a.idx_out[p] = my_e;
-            a.w_out[p] = wgt;
+            L_idx_out[p] = my_e;
+            L_w_out[p] = wgt;
           }
         }
       }
@@ -273,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // (exact: BF16 has 8 significant bits and the scaled values lie in FP16's
   // normal range)
   const int nx8 = a.T * a.H / 8;
-  const uint4* xg = reinterpret_cast<const uint4*>(fused ? xb : a.x);
+  const uint4* xg = reinterpret_cast<const uint4*>(fused ? xb : L_x);
   uint4 xr = make_uint4(0u, 0u, 0u, 0u);
   for (int b = warp * 32; b < nx8; b += kCThreads) {
     const int q = b + lane;
@@ -327,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       while (pa + 1 < tb.npieces && tb.pq0[pa + 1] <= q) ++pa;
       const int p = tb.sp[s], t = p / a.k;
       bool ok = tb.recs[p] != nullptr;
-      if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status, a.wait_ns);
-      if (ok) ok = await(&bars[pa], tb, a.status, a.wait_ns);
+      if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], ph, tb, a, kSiteScales, L);
+      if (ok) ok = await(&bars[pa], ph, tb, a, kSitePiece, L);
       if (t != xt) {
         xt = t;
         const uint4* xt4 = act + (size_t)t * 4 * UPR;
@@ -389,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     const int pb = qb + nr - 1 < tb.pq0[pa] + tb.pn[pa] ? pa : pa + 1;
     const int p = tb.sp[s], t = p / a.k;
     bool ok = tb.recs[p] != nullptr;
-    if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], tb, a.status, a.wait_ns);
-    if (ok) ok = await(&bars[pa], tb, a.status, a.wait_ns);
-    if (ok && pb != pa) ok = await(&bars[pb], tb, a.status, a.wait_ns);
+    if (ok && !scales_in) ok = scales_in = await(&bars[kBarScales], ph, tb, a, kSiteScales, L);
+    if (ok) ok = await(&bars[pa], ph, tb, a, kSitePiece, L);
+    if (ok && pb != pa) ok = await(&bars[pb], ph, tb, a, kSitePiece, L);
     float gs[kRows], us[kRows];
     uint32_t goff[kRows], uoff[kRows];
 #pragma unroll
@@ -460,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   // above are published by thread 0's release arrival)
   tc::named_sync(1, kCThreads);
   if (threadIdx.x == 0)
-    tb.flags[1] = grid_sync_thread(a.bar, bar_target(fused ? 2u : 1u), tb, a.status, a.wait_ns);
+    tb.flags[1] = grid_sync_thread(bar_target(fused ? 2u : 1u), tb, a, kSiteGrid2, L);
   tc::named_sync(1, kCThreads);
 
   // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats
@@ -500,21 +590,21 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   }
   tc::named_sync(1, kCThreads);
 
-  // down: task (row z, expert j) -> a group of L lanes (L a power of two),
-  // lane sub of the group taking units sub, sub + L, ...; the group's sum is
+  // down: task (row z, expert j) -> a group of NG lanes (NG a power of two),
+  // lane sub of the group taking units sub, sub + NG, ...; the group's sum is
   // reduced over its lanes in a fixed order and, times the router weight,
-  // kept per (row, expert).  32 / L tasks per warp pass, passes round-robin.
+  // kept per (row, expert).  32 / NG tasks per warp pass, passes round-robin.
   constexpr int kUnitsPerLane = 5;
-  int L = 1;
-  while (L < 32 && L * kUnitsPerLane < updr) L <<= 1;
-  const int tasks_per_pass = 32 / L;
+  int NG = 1;
+  while (NG < 32 && NG * kUnitsPerLane < updr) NG <<= 1;
+  const int tasks_per_pass = 32 / NG;
   const int ntask = nz * a.k;
   const int npass = (ntask + tasks_per_pass - 1) / tasks_per_pass;
-  const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], tb, a.status, a.wait_ns);
-  const int sub = lane & (L - 1);
+  const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], ph, tb, a, kSiteDown, L);
+  const int sub = lane & (NG - 1);
   float* part = reinterpret_cast<float*>(smem + g.off_part);  // [row][expert]
   for (int ps = warp; ps < npass; ps += kCWarps) {
-    const int task = ps * tasks_per_pass + lane / L;
+    const int task = ps * tasks_per_pass + lane / NG;
     float v = 0.f;
     int z = 0, j = 0, s = 0, p = 0;
     if (task < ntask) {
@@ -539,13 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
                                          dm::scale_bits<FMT>(srow + sstep * u), hq + 8 * u, 8 * UPDR);
           }
         } else {
-          for (int u = sub; u < updr; u += L)
+          for (int u = sub; u < updr; u += NG)
             v += dm::unit_dot_f32<FMT>(*reinterpret_cast<const uint4*>(crow + 16 * u),
                                        dm::scale_bits<FMT>(srow + sstep * u), hq + 8 * u, 8 * updr);
         }
       }
     }
-    for (int d = L >> 1; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    for (int d = NG >> 1; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
     if (task < ntask && sub == 0) part[task] = tb.wts[p] * v;
   }
   tc::named_sync(1, kCThreads);
@@ -556,18 +646,45 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     for (int jj = 0; jj < a.k; ++jj) v += part[(size_t)z * a.k + jj];
     a.y[d0 + z] = failed ? __uint_as_float(0x7FC00000u) : v;
   }
-  __syncthreads();
+  }  // compute warps
+  if (L + 1 < nl) {
+    // The next layer's router rows go into the x/h region, by bulk copies
+    // (the async proxy) after this layer's ordinary stores there: every
+    // thread orders its own stores before them, then the CTA-wide barrier.
+    tc::fence_proxy_async();
+    __syncthreads();  // end of layer L: y written, every shared buffer free again
+    if (threadIdx.x == 0) {
+      tb.flags[1] = 0;
+      // barrier 3L + 3 publishes y; the next layer's router rows are fetched
+      // while it completes, once the router barrier's phase of this layer
+      // has completed (a flagged launch stages nothing more)
+      tb.flags[2] = grid_sync_thread((tb.bar_base + 3u * (unsigned)L + 3u) * gridDim.x + a.barrier_extra, tb, a,
+                                     kSiteLayer, L, [&] {
+        if (!rstaged || *abort_flag) return;
+        if (tc::mbar_wait_backoff(&bars[kBarRouter], ph, tc::globaltimer() + a.wait_ns)) {
+          stage_router(a, smem, &bars[kBarRouter], L + 1);
+        } else {
+          *abort_flag = 1;
+          status_or(a.status, MOE_DEV_TIMEOUT);
+          note_timeout(a.bar, kSiteRouter, L);
+        }
+      });
+    }
+    if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
+    __syncthreads();
+  }
+  }  // layers
 }
 
-template <int FMT, int UPR, int UPDR>
+template <int FMT, int UPR, int UPDR, bool STACK>
 int launch_shape(const DecodeOneshotArgs& a, int grid, size_t smem, cudaStream_t stream) {
   static SmemGrant granted;  // per device; also checks that one CTA fits on an SM
-  if (!grant_smem(oneshot_kernel<FMT, UPR, UPDR>, smem, granted, kThreads)) return MOE_ERR_CUDA;
+  if (!grant_smem(oneshot_kernel<FMT, UPR, UPDR, STACK>, smem, granted, kThreads)) return MOE_ERR_CUDA;
   // Every CTA takes part in the grid barriers, so all must be resident: one
   // CTA per SM, checked by grant_smem above.  A cooperative launch would make
   // the driver guarantee it, but costs about 2.5 us more host time per launch
   // (48 eager launches per decoded token), so the waits are bounded instead.
-  return launch_pdl(oneshot_kernel<FMT, UPR, UPDR>, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_pdl(oneshot_kernel<FMT, UPR, UPDR, STACK>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int FMT>
@@ -575,8 +692,12 @@ int launch_fmt(const DecodeOneshotArgs& a, int grid, cudaStream_t stream) {
   DecodeOneshotArgs b = a;
   b.geo = make_geo(a.T, a.k, a.H, a.I, FMT == MOE_FMT_NVFP4 ? 16 : 32, grid, a.wr != nullptr, a.E);
   // the row strides are compile-time constants for the decode model shape
-  if (a.H == 2560 && a.I == 640) return launch_shape<FMT, 80, 20>(b, grid, b.geo.total, stream);
-  return launch_shape<FMT, 0, 0>(b, grid, b.geo.total, stream);
+  const bool stack = a.layers > 1;
+  if (a.H == 2560 && a.I == 640)
+    return stack ? launch_shape<FMT, 80, 20, true>(b, grid, b.geo.total, stream)
+                 : launch_shape<FMT, 80, 20, false>(b, grid, b.geo.total, stream);
+  return stack ? launch_shape<FMT, 0, 0, true>(b, grid, b.geo.total, stream)
+               : launch_shape<FMT, 0, 0, false>(b, grid, b.geo.total, stream);
 }
 
 }  // namespace os

@@ -121,6 +121,7 @@ struct Tab {
   float tsc[kMaxPairs];      // per token: 2^-e of the FP16 scale of x
   unsigned amax[kMaxPairs];  // max |x| of each token, as float bits
   int flags[4];              // [0] abort, [1] grid barrier passed, [2] router barrier passed
+  unsigned long long bar_base;  // grid-barrier counter at launch start / grid (thread 0)
   int npieces, nseg1, nseg2, ncopies;
   int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];
   uint32_t poff[kMaxPieces];  // piece: gate rows at codes1 + poff, up rows right after
@@ -293,5 +294,9 @@ struct DecodeOneshotArgs {
   // beyond the grid (0; a test sets 1 to make the barriers run out)
   unsigned long long wait_ns;
   unsigned barrier_extra;
+  // layers of a whole-layer launch (moe_decode_stack: wr, ptrs, bias, idx_out
+  // and w_out hold one block per layer; layer 0 from x, the others chained
+  // from y); 0 or 1 for one layer
+  int layers;
 };
 int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream);

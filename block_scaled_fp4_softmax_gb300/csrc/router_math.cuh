@@ -32,8 +32,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
 // 256 partial sums, mean = sum / H, r = 1 / sqrt(mean + eps) with IEEE sqrt
 // and divide.  Every thread of the block (BAR < 0), or the first N >= 256
 // threads (named barrier BAR), calls it; threads from 256 on only take part
-// in the barriers.  part: 256 floats of shared memory.
-template <int BAR = -1, int N = 0>
+// in the barriers.  part: 256 floats of shared memory.  L2_ONLY: y is read
+// through L2 only (a persistent kernel reads a new y at the same address
+// every layer; L1 is not coherent across SMs).
+template <int BAR = -1, int N = 0, bool L2_ONLY = false>
 __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ yr, int H, float eps,
                                                      float* part) {
   if (threadIdx.x < 256) {
@@ -42,7 +44,8 @@ __device__ __forceinline__ float rms_inv_fixed_order(const float* __restrict__ y
     for (int i0 = threadIdx.x; i0 < H; i0 += 256 * kBatch) {
       float v[kBatch];
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) v[b] = i0 + 256 * b < H ? yr[i0 + 256 * b] : 0.0f;
+      for (int b = 0; b < kBatch; ++b)
+        v[b] = i0 + 256 * b >= H ? 0.0f : L2_ONLY ? __ldcg(yr + i0 + 256 * b) : yr[i0 + 256 * b];
 #pragma unroll
       for (int b = 0; b < kBatch; ++b)
         if (i0 + 256 * b < H) acc = __fadd_rn(acc, __fmul_rn(v[b], v[b]));

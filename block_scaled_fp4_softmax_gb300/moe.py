@@ -37,6 +37,7 @@ EXPORTS = (
     "moe_experts_decode",
     "moe_experts_decode_host",
     "moe_decode_layer",
+    "moe_decode_stack",
     "moe_experts_decode_noalloc_limit",
     "moe_experts_decode_noalloc",
     "moe_bucket_workspace",
@@ -81,6 +82,8 @@ _SIGS = {
                                      _vp, _vp]),
     "moe_decode_layer": (_i, [_vp, _vp, _i, ctypes.c_double, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp,
                               ExpertShape, _vp, _vp, _sz, _vp, _vp]),
+    "moe_decode_stack": (_i, [_vp, _i, ctypes.c_double, _i, _vp, _vp, _i, _i, _vp, ExpertShape, _vp, _vp, _vp,
+                              _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_experts_decode_noalloc_limit": (_sz, []),
     "moe_experts_decode_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _vp, _i, ExpertShape, _vp, _vp, _vp]),
     "moe_bucket_workspace": (_sz, [_i, _i, _i]),
@@ -274,6 +277,38 @@ def moe_decode_layer(wr, bias, k: int, ptrs, s: ExpertShape, x=None, y_prev=None
                                    E, k, _ptr(idx), _ptr(weights), _ptr(logits), _ptr(ptrs), s, _ptr(y),
                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_status), _stream(stream)), "moe_decode_layer")
+    return x_out, idx, weights, logits, y
+
+
+def moe_decode_stack(x0, wr, bias, k: int, ptrs, s: ExpertShape, eps: float = 1e-6, idx=None, weights=None,
+                     logits=None, x_out=None, y=None, workspace=None, dev_status=None, stream=None):
+    """All layers of a decode stack in one launch.  wr [L, E, H] BF16, ptrs
+    [L, E] int64 record addresses, bias [L, E] or None.  Returns
+    (x_out, idx [L, T, k], weights [L, T, k], logits [T, E], y [T, H])."""
+    _cuda(x0, "x0", torch.bfloat16)
+    _cuda(wr, "wr", torch.bfloat16)
+    _cuda(ptrs, "expert_ptrs", torch.int64)
+    if bias is not None:
+        _cuda(bias, "bias", torch.float32)
+    T, H = x0.shape
+    layers, E = wr.shape[0], wr.shape[1]
+    dev = x0.device
+    if idx is None:
+        idx = torch.empty(layers, T, k, dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty(layers, T, k, dtype=torch.float32, device=dev)
+    if logits is None:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    if x_out is None:
+        x_out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if y is None:
+        y = torch.empty(T, H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(max(moe_experts_decode_workspace(T, k, s), 16), dtype=torch.uint8, device=dev)
+    _check(load().moe_decode_stack(_ptr(x0), T, float(eps), layers, _ptr(wr), _ptr(bias), E, k, _ptr(ptrs), s,
+                                   _ptr(idx), _ptr(weights), _ptr(logits), _ptr(x_out), _ptr(y), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                   _stream(stream)), "moe_decode_stack")
     return x_out, idx, weights, logits, y
 
 

@@ -144,7 +144,12 @@ int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps, uint1
  * leaves the counters in a state the next call accepts, so one zeroed
  * workspace serves any number of calls, of any shape, on one stream; calls
  * that overlap in time need separate workspaces.  After a call that reported
- * MOE_DEV_TIMEOUT, zero it again. */
+ * MOE_DEV_TIMEOUT, zero it again.  For diagnosis, the 64-bit word at byte
+ * 128 of the workspace then holds the first wait that gave up since the
+ * zero-fill: site << 56 | (layer + 1) << 32 | CTA index, with site 1 the
+ * router rows' copy, 2 the gate/up scales, 3 a gate/up piece, 4 the down
+ * rows, 5 and 6 the two grid barriers of a layer, 7 the barrier between
+ * layers (moe_decode_stack), 8 the copy warp's own wait. */
 size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s);
 
 /* Decode path: the experts of T tokens (T*k small, GEMV shaped), HBM bound
@@ -217,6 +222,27 @@ int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int T, double 
                      float* weights, float* logits, const void* const* expert_ptrs,
                      moe_expert_shape s, float* y, void* workspace, size_t ws_bytes,
                      int32_t* dev_status, void* stream);
+
+/* A whole decode stack in one launch (first page, "Why this model": 48
+ * layers in a row, each routing the previous layer's output; "Where the time
+ * actually goes": the per-layer issue overhead).  Computes exactly what
+ * `layers` calls of moe_decode_layer compute -- layer 0 with x_bf16 = x0, each
+ * later layer with y_prev = y (RMS-chained with eps) -- with the same bits,
+ * in one persistent kernel whose layers are separated by grid barriers
+ * instead of launch boundaries:
+ *  - wr_bf16 [layers x E x H] BF16, bias [layers x E] FP32 or NULL,
+ *    expert_ptrs [layers x E] (device): one block per layer, back to back;
+ *  - idx, weights [layers x T x k]: each layer's routing;
+ *  - logits [T x E]: scratch, the last layer's logits at the end;
+ *  - x_out [T x H] (may be NULL): the last layer's input;
+ *  - y [T x H]: the last layer's output (each layer's output in turn).
+ * Same limits, workspace rules and residency requirement as
+ * moe_decode_layer; shapes outside the one-shot plan return
+ * MOE_ERR_UNSUPPORTED.  1 <= layers <= 4096. */
+int moe_decode_stack(const uint16_t* x0, int T, double eps, int layers, const uint16_t* wr_bf16,
+                     const float* bias, int E, int k, const void* const* expert_ptrs, moe_expert_shape s,
+                     int32_t* idx, float* weights, float* logits, uint16_t* x_out, float* y,
+                     void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Decode without allocation.  The pages have no counterpart: this entry
  * point exists for callers that cannot allocate device memory on the decode

@@ -88,6 +88,24 @@ def test_stack_graph_replay_equals_eager_calls(stack):
     assert torch.isfinite(y_graph).all()
 
 
+def test_persistent_stack_equals_graph_replay(stack):
+    """moe_decode_stack runs all 48 layers of the bench's stack in one launch;
+    it must give the bits of the per-layer launches bench.py times."""
+    st = stack
+    st.x.copy_(st.x0[2:3])
+    st.run_layers()
+    torch.cuda.synchronize()
+    y_ref, idx_last = st.y.clone(), st.idx.clone()
+    ptrs = torch.stack(st.ptrs)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x_out, idx, w, lg, y = moe.moe_decode_stack(st.x0[2:3].contiguous(), st.wr, None, bench.K_TOP, ptrs, st.s,
+                                                dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(idx[-1], idx_last)
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+
+
 def test_stack_layers_against_oracle(stack):
     st = stack
     # layer 0 from the stack's own first token, then the oracle's chained x1

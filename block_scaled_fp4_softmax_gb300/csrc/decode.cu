@@ -759,14 +759,18 @@ int launch_stream(const st::Args& sa, cudaStream_t stream) {
 
 }  // namespace
 
-// Workspace: a header (the one-shot kernel's 64-bit grid-barrier counter at
-// 0, the ring kernel's two barrier words at 128, the rest reserved), then h
-// [T*k][I] FP32.  The header sits at a fixed place so that calls of any shape
-// can share one workspace.
+// Workspace: a header (the one-shot kernel's 64-bit barrier counter at 0,
+// the ring kernel's two barrier words at 128, the one-shot kernel's record
+// of a wait that gave up at 192, the rest reserved), then the one-shot
+// kernel's tagged logits and FP32 h (moe::os::oneshot_ws_bytes); the other
+// paths keep their FP32 h [T*k][I] right after the header.  The header sits
+// at a fixed place so that calls of any shape can share one workspace.
 constexpr size_t kRingBarrierOffset = 128;
 extern "C" size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s) {
   if (T <= 0 || k <= 0 || !moe::shape_ok(s)) return 0;
-  return moe::os::kHeaderBytes + (size_t)T * k * s.inter * sizeof(float);
+  const size_t fp32_h = moe::os::kHeaderBytes + (size_t)T * k * s.inter * sizeof(float);
+  const size_t tagged = moe::os::oneshot_ws_bytes(T, k, s.inter);
+  return tagged > fp32_h ? tagged : fp32_h;
 }
 
 // The argument checks of moe_experts_decode that do not involve the
@@ -817,8 +821,7 @@ static int decode_launch(const uint16_t* x_bf16, const int32_t* idx, const float
     oa.E = E;
     oa.H = s.hidden;
     oa.I = s.inter;
-    oa.bar = reinterpret_cast<unsigned long long*>(ws);
-    oa.hws = hws;
+    oneshot_set_workspace(oa, ws);
     oa.y = y;
     oa.status = dev_status;
     return launch_decode_oneshot(oa, s.format, sm_count(), stream);
@@ -908,8 +911,7 @@ extern "C" int moe_decode_layer(const uint16_t* x_bf16, const float* y_prev, int
   oa.E = E;
   oa.H = s.hidden;
   oa.I = s.inter;
-  oa.bar = reinterpret_cast<unsigned long long*>(ws);
-  oa.hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
+  oneshot_set_workspace(oa, ws);
   oa.y = y;
   oa.status = dev_status;
   oa.y_prev = y_prev;
@@ -952,8 +954,7 @@ extern "C" int moe_decode_stack(const uint16_t* x0, int T, double eps, int layer
   oa.E = E;
   oa.H = s.hidden;
   oa.I = s.inter;
-  oa.bar = reinterpret_cast<unsigned long long*>(ws);
-  oa.hws = reinterpret_cast<float*>(ws + moe::os::kHeaderBytes);
+  oneshot_set_workspace(oa, ws);
   oa.y = y;
   oa.status = dev_status;
   oa.y_prev = nullptr;
@@ -1026,9 +1027,9 @@ extern "C" int moe_experts_decode_noalloc(const uint16_t* x_bf16, const int32_t*
   void* scratch = nullptr;
   rc = static_scratch(&scratch);
   if (rc != MOE_OK) return rc;
-  // The array keeps whatever the previous call left; its header of barrier
-  // counters must start at zero.
-  if (cudaMemsetAsync(scratch, 0, moe::os::kHeaderBytes, (cudaStream_t)stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  // The array keeps whatever the previous call left.  The part this call
+  // uses starts at zero, as a fresh workspace would: the counters, and the
+  // tagged exchange words, whose tags restart with the counter.
+  if (cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
   return decode_launch(x_bf16, idx, weights, T, k, expert_ptrs, E, s, y, scratch, dev_status, stream);
 }

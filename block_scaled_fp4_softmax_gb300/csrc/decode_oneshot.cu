@@ -38,13 +38,14 @@ namespace moe {
 namespace os {
 
 // Where a bounded wait gave up: the first one in the launch's workspace
-// (byte 128 of the header, a 64-bit word that stays zero while every wait
-// succeeds) gets site << 56 | (layer + 1) << 32 | block.
+// (byte 192 of the header, a 64-bit word that stays zero while every wait
+// succeeds; the ring kernel's barrier words sit at 128) gets
+// site << 56 | (layer + 1) << 32 | block.
 enum WaitSite : unsigned {
   kSiteRouter = 1, kSiteScales, kSitePiece, kSiteDown, kSiteGrid1, kSiteGrid2, kSiteLayer, kSiteLoader
 };
 __device__ __forceinline__ void note_timeout(unsigned long long* bar, unsigned site, int layer) {
-  unsigned long long* diag = bar + 16;
+  unsigned long long* diag = bar + 24;
   atomicCAS(diag, 0ull, (unsigned long long)site << 56 | (unsigned long long)(layer + 1) << 32 | blockIdx.x);
 }
 
@@ -61,6 +62,42 @@ __device__ __forceinline__ bool await(uint64_t* bar, uint32_t parity, Tab& tb, c
   return false;
 }
 
+// Exchange words between CTAs: a value's 32 bits and a 32-bit tag in one
+// 8-byte word, stored and loaded whole (single-copy atomic), so a reader
+// that sees this layer's tag sees the value written with it; the data is its
+// own flag and no grid barrier separates writer and reader.  Tags are
+// quiet-NaN patterns 0x7FC00001 .. 0x7FFFFFFE, one per layer of the
+// workspace's counter (cycling after about 4 million layers); no FP32
+// arithmetic of this library yields them (its NaNs are 0x7FFFFFFF and
+// 0x7FC00000), so FP32 data that other paths leave in the workspace never
+// passes for a tag.
+__device__ __forceinline__ uint32_t layer_tag(unsigned long long n) {
+  return 0x7FC00000u | (1u + (uint32_t)(n % 0x3FFFFEull));
+}
+__device__ __forceinline__ void put_tagged(unsigned long long* p, float v, uint32_t tag) {
+  const unsigned long long w = (unsigned long long)tag << 32 | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+// The value of a word already loaded, or, when it does not carry `tag` yet,
+// of the word polled until it does (bounded: on timeout the launch is
+// flagged, the site recorded, and NaN returned).
+__device__ __forceinline__ float tagged_value(unsigned long long w, const unsigned long long* p, uint32_t tag,
+                                              Tab& tb, const DecodeOneshotArgs& a, unsigned site, int layer) {
+  if ((uint32_t)(w >> 32) == tag) return __uint_as_float((uint32_t)w);
+  volatile int* abort_flag = tb.flags;
+  const uint64_t dl = global_ns() + a.wait_ns;
+  while (!*abort_flag) {
+    w = rt::ld_relaxed_u64(p);
+    if ((uint32_t)(w >> 32) == tag) return __uint_as_float((uint32_t)w);
+    if (global_ns() > dl) {
+      *abort_flag = 1;
+      status_or(a.status, MOE_DEV_TIMEOUT);
+      note_timeout(a.bar, site, layer);
+    }
+  }
+  return __uint_as_float(0x7FC00000u);
+}
+
 // Grid barrier, called by one thread per CTA after a CTA-wide barrier: one
 // arrival on a counter that only grows (a release reduction, so the writes
 // of every thread of the CTA that precede the CTA-wide barrier are visible
@@ -72,13 +109,15 @@ __device__ __forceinline__ bool await(uint64_t* bar, uint32_t parity, Tab& tb, c
 // arrivals of this launch can precede the read.  `between` runs after the
 // arrival and before the poll (work that overlaps the wait without holding
 // up the release).  False on timeout, which also flags the launch.
-template <class F>
+template <bool RELEASE = true, class F>
 __device__ __forceinline__ bool grid_sync_thread(unsigned long long target, Tab& tb, const DecodeOneshotArgs& a,
                                                  unsigned site, int layer, F&& between) {
   volatile int* abort_flag = tb.flags;
   int good = !*abort_flag;
   if (good) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(a.bar) : "memory");
+    if (RELEASE) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(a.bar) : "memory");
+    else asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(a.bar) : "memory");
+    ++tb.arrived;
     between();
     const uint64_t dl = global_ns() + a.wait_ns;
     while (dm::ld_acquire_u64(a.bar) < target) {
@@ -95,9 +134,10 @@ __device__ __forceinline__ bool grid_sync_thread(unsigned long long target, Tab&
   }
   return good;
 }
+template <bool RELEASE = true>
 __device__ __forceinline__ bool grid_sync_thread(unsigned long long target, Tab& tb, const DecodeOneshotArgs& a,
                                                  unsigned site, int layer) {
-  return grid_sync_thread(target, tb, a, site, layer, [] {});
+  return grid_sync_thread<RELEASE>(target, tb, a, site, layer, [] {});
 }
 
 // The CTA's share of the router rows of a fused launch: experts
@@ -145,8 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   pdl_launch_dependents();
   // A launch runs a.layers >= 1 layers (more than one only for a whole-layer
   // launch, moe_decode_stack): layer 0 from a.x or a.y_prev, every later layer
-  // RMS-chained from the previous layer's y.  Layer L uses grid barriers
-  // 3L + 1 and 3L + 2, and barrier 3L + 3 publishes its y to the next layer.
+  // RMS-chained from the previous layer's y.  Each layer has nb grid barriers
+  // on the workspace counter: the logits (fused launch), h, and, between the
+  // layers of a whole-stack launch, y.  The counter at launch start, over the
+  // grid, is the base: layer L's barrier n waits for (base + nb L + n) grid.
+  // The logits travel as words tagged with tag(base + nb L + 1) and are
+  // checked after their barrier, which therefore needs no release (h and y
+  // are FP32, published by release arrivals: tagged h doubles the bytes each
+  // CTA reads and measured slower).
   // The mbarriers are set up once; each completes one phase per layer, so
   // layer L waits for the phase of parity L & 1.
   const int nl = STACK ? a.layers : 1;
@@ -162,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
   const bool fused = L_wr != nullptr;
+  const unsigned nb = (fused ? 2u : 1u) + (STACK ? 1u : 0u);
   const Geo& g = a.geo;
   const RecordOffsets o = record_offsets(a.H, a.I, FMT);
   const int upr = UPR > 0 ? UPR : a.H >> 5;
@@ -176,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const uint8_t* scales2 = smem + g.off_scales2;
   uint4* act = reinterpret_cast<uint4*>(smem + g.off_act);
   volatile int* abort_flag = tb.flags;
+  // layer L's barrier n (thread 0, which holds the base)
+  auto bar_target = [&](unsigned n) { return (tb.bar_base + nb * L + n) * gridDim.x + a.barrier_extra; };
 
   // router rows of this CTA's experts (fused launch) and the pointer table:
   // neither depends on the previous kernel, so they are fetched before the
@@ -199,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     // later layers are reset at the end of the previous one
     if (threadIdx.x == 0) {
       tb.flags[0] = 0;  // a wait that ran out stays flagged for the launch's later layers
-      tb.flags[1] = 0;
       if (rstaged) stage_router(a, smem, &bars[kBarRouter], 0);
     }
     if (threadIdx.x < kMaxPairs) tb.amax[threadIdx.x] = 0u;
@@ -280,14 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
 
   if (L == 0) {
     pdl_wait();
-    // grid-barrier counter at the start of this launch (thread 0 arrives for
-    // the CTA; a relaxed load, first used at the first barrier, so it stalls
-    // nothing before)
-    if (threadIdx.x == 0) tb.bar_base = rt::ld_relaxed_u64(a.bar) / gridDim.x;
+    // the counter at the start of this launch, over the grid: every earlier
+    // launch has added its grid x layers by now, and fewer than a grid of
+    // this launch's additions can precede the read (each CTA adds only after
+    // its own read), so every CTA gets the same number.  Thread 0 reads it;
+    // the router's (or the x staging's) first barrier publishes it.
+    if (threadIdx.x == 0) {
+      tb.bar_base = rt::ld_relaxed_u64(a.bar) / gridDim.x;
+      tb.arrived = 0;
+    }
   }
-  auto bar_target = [&](unsigned n) {
-    return (tb.bar_base + 3u * (unsigned)L + n) * gridDim.x + a.barrier_extra;
-  };
 
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + g.off_xb + 1024 + 4096);  // x (BF16), fused launch
   if (fused) {
@@ -326,17 +376,45 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
       if (rstaged) v = rin ? rt::logit_dot<true>(xb + (size_t)t * a.H, wsm + (size_t)q * a.H, a.H, lane)
                            : __uint_as_float(0x7FC00000u);
       else v = rt::logit_dot(xb + (size_t)t * a.H, L_wr + (size_t)(re0 + q) * a.H, a.H, lane);
-      if (lane == 0) a.logits[(size_t)t * a.E + re0 + q] = L_bias ? __fadd_rn(v, L_bias[re0 + q]) : v;
+      if (lane == 0) {
+        const float lv = L_bias ? __fadd_rn(v, L_bias[re0 + q]) : v;
+        a.logits[(size_t)t * a.E + re0 + q] = lv;
+        put_tagged(a.xlog + (size_t)t * kLogitStride + re0 + q, lv, layer_tag(tb.bar_base + nb * L + 1));
+      }
     }
+    // the logits' barrier: a relaxed arrival (no wait for the stores above),
+    // the words themselves are checked below
     tc::named_sync(4, kCThreads);
-    if (threadIdx.x == 0) tb.flags[2] = grid_sync_thread(bar_target(1), tb, a, kSiteGrid1, L);
+    if (threadIdx.x == 0) grid_sync_thread<false>(bar_target(1), tb, a, kSiteGrid1, L);
     tc::named_sync(4, kCThreads);
-    const bool have_logits = tb.flags[2] != 0;
     unsigned long long* fin = reinterpret_cast<unsigned long long*>(smem + g.off_xb + 1024);
+    // every CTA's logits of token t, each word checked for this layer's tag
+    // (one still in flight is polled), into the gate/up region, which is free
+    // until the copies are issued after the router
+    float* lsm = reinterpret_cast<float*>(smem + g.off_codes1);
+    const uint32_t want = layer_tag(tb.bar_base + nb * L + 1);
     for (int t = 0; t < a.T; ++t) {
+      {
+        const unsigned long long* src = a.xlog + (size_t)t * kLogitStride;
+        constexpr int kPer = (kLogitStride + kCThreads - 1) / kCThreads;
+        unsigned long long wv[kPer];
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int e = threadIdx.x + kCThreads * m;
+          wv[m] = e < a.E ? rt::ld_relaxed_u64(src + e) : 0ull;
+        }
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int e = threadIdx.x + kCThreads * m;
+          if (e < a.E) lsm[e] = tagged_value(wv[m], src + e, want, tb, a, kSiteGrid1, L);
+        }
+      }
+      tc::named_sync(4, kCThreads);
+      // set only before the barrier above, so every thread reads the same
+      const bool have_logits = *abort_flag == 0;
       int my_e = 0;
       float my_l = 0.0f;
-      if (have_logits) rt::topk_block_fast<kCWarps, 4>(a.logits + (size_t)t * a.E, a.E, a.k, fin, my_e, my_l);
+      if (have_logits) rt::topk_block_fast<kCWarps, 4, true>(lsm, a.E, a.k, fin, my_e, my_l);
       if (warp == 0) {
         const float wgt = rt::topk_weight(lane, a.k, my_l);
         if (lane < a.k) {
@@ -353,6 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
         }
       }
     }
+    // the logits' generic stores in the gate/up region come before the
+    // loader's bulk copies there
+    tc::fence_proxy_async();
     tc::named_sync(4, kCThreads);  // the staged pointers in the x/h region are no longer read
     asm volatile("bar.arrive 3, %0;" ::"n"(kThreads) : "memory");  // records in place for the loader
   }
@@ -397,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   }
   asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");  // x staged, records in place
 
-  // gate/up + SwiGLU.
+  // gate/up + SwiGLU
   const int n1 = share_lo(blockIdx.x + 1, (int)g.R1, g.grid) - share_lo(blockIdx.x, (int)g.R1, g.grid);
   if constexpr (UPR > 0 && UPR <= 96) {
     // Rows dealt round-robin over the compute warps in the CTA's row order, so
@@ -546,11 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     qb += nr;
   }
   }
-  // grid barrier among the compute threads of every CTA (the h rows written
-  // above are published by thread 0's release arrival)
+  // h's barrier (a release arrival publishes the h rows written above); every
+  // warp is also done with x in the x/h region before h is staged there
   tc::named_sync(1, kCThreads);
-  if (threadIdx.x == 0)
-    tb.flags[1] = grid_sync_thread(bar_target(fused ? 2u : 1u), tb, a, kSiteGrid2, L);
+  if (threadIdx.x == 0) grid_sync_thread(bar_target(fused ? 2u : 1u), tb, a, kSiteGrid2, L);
   tc::named_sync(1, kCThreads);
 
   // h of the pairs of the CTA's tokens, FP32, staged as 4 quads of 8 floats
@@ -561,8 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const int t_lo = nz > 0 ? tb.dt[0] : 0;
   const int nlp = nz > 0 ? (tb.dt[tb.nseg2 - 1] - t_lo + 1) * a.k : 0;
   float* hs = reinterpret_cast<float*>(act);
-  const bool have_h = tb.flags[1] != 0;
-  if (have_h) {
+  if (*abort_flag == 0) {
     const int n8 = nlp * (a.I / 8);
     const float4* src = reinterpret_cast<const float4*>(a.hws + (size_t)t_lo * a.k * a.I);
     constexpr int kB = 4;
@@ -600,6 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
   const int tasks_per_pass = 32 / NG;
   const int ntask = nz * a.k;
   const int npass = (ntask + tasks_per_pass - 1) / tasks_per_pass;
+  // set only before the barrier above, so every thread reads the same
+  const bool have_h = *abort_flag == 0;
   const bool down_in = have_h && nz > 0 && await(&bars[kBarDown], ph, tb, a, kSiteDown, L);
   const int sub = lane & (NG - 1);
   float* part = reinterpret_cast<float*>(smem + g.off_part);  // [row][expert]
@@ -654,12 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     tc::fence_proxy_async();
     __syncthreads();  // end of layer L: y written, every shared buffer free again
     if (threadIdx.x == 0) {
-      tb.flags[1] = 0;
-      // barrier 3L + 3 publishes y; the next layer's router rows are fetched
-      // while it completes, once the router barrier's phase of this layer
-      // has completed (a flagged launch stages nothing more)
-      tb.flags[2] = grid_sync_thread((tb.bar_base + 3u * (unsigned)L + 3u) * gridDim.x + a.barrier_extra, tb, a,
-                                     kSiteLayer, L, [&] {
+      // this layer's arrival publishes y; the next layer's router rows are
+      // fetched while the barrier completes, once the router barrier's phase
+      // of this layer has completed (a flagged launch stages nothing more)
+      grid_sync_thread(bar_target(nb), tb, a, kSiteLayer, L, [&] {
         if (!rstaged || *abort_flag) return;
         if (tc::mbar_wait_backoff(&bars[kBarRouter], ph, tc::globaltimer() + a.wait_ns)) {
           stage_router(a, smem, &bars[kBarRouter], L + 1);
@@ -674,6 +753,15 @@ __global__ void __launch_bounds__(kThreads, 1) oneshot_kernel(DecodeOneshotArgs 
     __syncthreads();
   }
   }  // layers
+  // every barrier's arrival, also those a flagged launch skipped (and the
+  // barrier after the last layer, which a whole-stack launch does not wait
+  // for), so that the counter stays a multiple of the grid between launches
+  if (threadIdx.x == 0) {
+    const Tab& tb = *reinterpret_cast<const Tab*>(smem + a.geo.off_tab);
+    const unsigned nb = (a.wr ? 2u : 1u) + (STACK ? 1u : 0u);
+    const unsigned long long rest = (unsigned long long)nb * (unsigned long long)nl - (unsigned long long)tb.arrived;
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(a.bar), "l"(rest) : "memory");
+  }
 }
 
 template <int FMT, int UPR, int UPDR, bool STACK>

@@ -35,6 +35,14 @@ constexpr uint32_t kMaxCopy = 32768;
 constexpr size_t kBarrierBytes = 256;  // grid-barrier counter
 constexpr size_t kCounterBytes = 16384;  // reserved (kept so the workspace layout stays fixed)
 constexpr size_t kHeaderBytes = kBarrierBytes + kCounterBytes;
+constexpr int kLogitStride = 1024;  // tagged logits per token in the workspace (E <= 1024)
+
+// The one-shot kernel's workspace after the header: tagged logits, then h
+// [T*k][I] FP32.  The other decode paths keep their FP32 h right after the
+// header.
+__host__ __device__ inline size_t oneshot_ws_bytes(int T, int k, int I) {
+  return kHeaderBytes + (size_t)T * kLogitStride * 8 + (size_t)T * k * I * 4;
+}
 
 __host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -81,7 +89,9 @@ __host__ __device__ inline Geo make_geo(int T, int k, int H, int I, int G, int g
   g.off_tab = o = round_up(o, 16);                // tables, weights, scales, flags
   o += 8192;
   g.off_codes1 = o = round_up(o, 128);
-  o += (size_t)g.rows1 * H;                       // gate + up codes
+  // gate + up codes; a fused launch first stages one token's E logits here
+  const size_t lg = fused ? (size_t)E * 4 : 0;
+  o += (size_t)g.rows1 * H > lg ? (size_t)g.rows1 * H : lg;
   g.off_scales1 = o = round_up(o, 128);
   o += 2 * ((size_t)g.rows1 * (H / G) + 32 * (size_t)g.segs1);
   g.off_codes2 = o = round_up(o, 128);
@@ -120,8 +130,9 @@ struct Tab {
   float wts[kMaxPairs];
   float tsc[kMaxPairs];      // per token: 2^-e of the FP16 scale of x
   unsigned amax[kMaxPairs];  // max |x| of each token, as float bits
-  int flags[4];              // [0] abort, [1] grid barrier passed, [2] router barrier passed
-  unsigned long long bar_base;  // grid-barrier counter at launch start / grid (thread 0)
+  int flags[4];              // [0] abort: a wait gave up (the launch writes NaN)
+  unsigned long long bar_base;  // layer counter at launch start / grid (thread 0)
+  int arrived;                  // layers this CTA has added to the counter (thread 0)
   int npieces, nseg1, nseg2, ncopies;
   int pq0[kMaxPieces], pn[kMaxPieces], pseg[kMaxPieces];
   uint32_t poff[kMaxPieces];  // piece: gate rows at codes1 + poff, up rows right after
@@ -274,8 +285,11 @@ struct DecodeOneshotArgs {
   int T, k;
   const void* const* ptrs;
   int E, H, I;
-  unsigned long long* bar;  // grid-barrier counter (workspace start)
-  float* hws;               // [P][I] SwiGLU intermediate
+  unsigned long long* bar;  // layer counter (workspace start)
+  // the logits exchanged between CTAs, [T][kLogitStride] tagged words (the
+  // value's bits in the low 32, the layer's tag in the high 32)
+  unsigned long long* xlog;
+  float* hws;  // [P][I] SwiGLU intermediate
   float* y;
   int32_t* status;
   // router, when the launch runs the whole layer (wr != NULL): x = RMS
@@ -299,4 +313,13 @@ struct DecodeOneshotArgs {
   // from y); 0 or 1 for one layer
   int layers;
 };
+// The counter, the tagged logits and h of a launch with T tokens in a
+// workspace of at least moe::os::oneshot_ws_bytes(T, k, I) bytes.
+inline void oneshot_set_workspace(DecodeOneshotArgs& oa, void* ws) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  oa.bar = reinterpret_cast<unsigned long long*>(b);
+  oa.xlog = reinterpret_cast<unsigned long long*>(b + moe::os::kHeaderBytes);
+  oa.hws = reinterpret_cast<float*>(oa.xlog + (size_t)oa.T * moe::os::kLogitStride);
+}
+
 int launch_decode_oneshot(const DecodeOneshotArgs& a, int fmt, int grid, void* stream);

@@ -149,8 +149,9 @@ __device__ __forceinline__ float topk_weight(int lane, int k, float my_l) {
 // their order are exactly those of a single-warp selection.  fin: NW * 32
 // keys of shared memory.  Every thread of the block (BAR < 0; the block
 // has NW warps), or of the first NW warps (named barrier BAR), calls it;
-// warp 0, lane r < k, ends with pick r.
-template <int NW, int BAR = -1>
+// warp 0, lane r < k, ends with pick r.  lrow is in global memory, read
+// through L2 (written by other CTAs), or in shared memory (SHARED).
+template <int NW, int BAR = -1, bool SHARED = false>
 __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsigned long long* fin, int& my_e,
                                            float& my_l) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,7 +161,9 @@ __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsi
   for (int m = 0; m < kPer; ++m) {
     const int e = warp * 32 + lane + 32 * NW * m;
     cand[m] = 0ull;
-    if (e < E) cand[m] = ((unsigned long long)ordered_key(__ldcg(lrow + e)) << 32) | (unsigned long long)(~(uint32_t)e);
+    if (e < E)
+      cand[m] = ((unsigned long long)ordered_key(SHARED ? lrow[e] : __ldcg(lrow + e)) << 32) |
+                (unsigned long long)(~(uint32_t)e);
   }
   if (warp < NW) {
     unsigned long long prev = ~0ull;
@@ -210,13 +213,13 @@ __device__ __forceinline__ void topk_block(const float* lrow, int E, int k, unsi
 // NW < k, it falls back to topk_block.  Keys are unique, so both routes give
 // the same picks in the same order.  fin: NW * 32 keys of shared memory
 // (at least 128); same calling rules as topk_block.
-template <int NW, int BAR = -1>
+template <int NW, int BAR = -1, bool SHARED = false>
 __device__ __forceinline__ void topk_block_fast(const float* lrow, int E, int k, unsigned long long* fin,
                                                 int& my_e, float& my_l) {
   static_assert(NW * 32 >= 128, "scratch");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (NW < k) {
-    topk_block<NW, BAR>(lrow, E, k, fin, my_e, my_l);
+    topk_block<NW, BAR, SHARED>(lrow, E, k, fin, my_e, my_l);
     return;
   }
   constexpr int kPer = (1024 + 32 * NW - 1) / (32 * NW);
@@ -226,7 +229,9 @@ __device__ __forceinline__ void topk_block_fast(const float* lrow, int E, int k,
   for (int m = 0; m < kPer; ++m) {
     const int e = warp * 32 + lane + 32 * NW * m;
     cand[m] = 0ull;
-    if (e < E) cand[m] = ((unsigned long long)ordered_key(__ldcg(lrow + e)) << 32) | (unsigned long long)(~(uint32_t)e);
+    if (e < E)
+      cand[m] = ((unsigned long long)ordered_key(SHARED ? lrow[e] : __ldcg(lrow + e)) << 32) |
+                (unsigned long long)(~(uint32_t)e);
     best = cand[m] > best ? cand[m] : best;
   }
   unsigned* cnt = reinterpret_cast<unsigned*>(fin + 96);
@@ -266,7 +271,7 @@ __device__ __forceinline__ void topk_block_fast(const float* lrow, int E, int k,
   const unsigned total = *cnt;
   if (total > 32u || tau == 0ull) {
     step_sync<BAR, NW * 32>();  // every thread has read the count before topk_block reuses fin
-    topk_block<NW, BAR>(lrow, E, k, fin, my_e, my_l);
+    topk_block<NW, BAR, SHARED>(lrow, E, k, fin, my_e, my_l);
     return;
   }
   if (warp == 0) {

@@ -139,13 +139,16 @@ int moe_rmsnorm_router_topk(const float* y_prev, int T, int H, double eps, uint1
                             int32_t* idx, float* weights, float* logits, void* stream);
 
 /* Workspace bytes moe_experts_decode needs for T tokens, k experts each:
- * 16,640 bytes of grid-barrier counters, then the FP32 SwiGLU intermediate
- * [T*k][I].  Zero-fill it before its first use.  Every call that completes
+ * a 16,640-byte header of counters, then the logits the CTAs of a one-shot
+ * launch exchange (1024 per token, each an 8-byte word of the value and a
+ * per-layer tag), then the FP32 SwiGLU intermediate [T*k][I] (the other
+ * decode paths keep theirs right after the header).  Zero-fill it before
+ * its first use.  Every call that completes
  * leaves the counters in a state the next call accepts, so one zeroed
  * workspace serves any number of calls, of any shape, on one stream; calls
  * that overlap in time need separate workspaces.  After a call that reported
  * MOE_DEV_TIMEOUT, zero it again.  For diagnosis, the 64-bit word at byte
- * 128 of the workspace then holds the first wait that gave up since the
+ * 192 of the workspace then holds the first wait that gave up since the
  * zero-fill: site << 56 | (layer + 1) << 32 | CTA index, with site 1 the
  * router rows' copy, 2 the gate/up scales, 3 a gate/up piece, 4 the down
  * rows, 5 and 6 the two grid barriers of a layer, 7 the barrier between

@@ -79,8 +79,10 @@ def test_argument_validation_before_any_cuda_call(lib):
                                   1 << 20, None, None) == 3
     assert lib.fp8_rowscale_gemv(one, one, one, 4, 24, one, None) == 3
     assert lib.fp4_pack_expert(one, one, vp(20), s, one, None) == 2
-    # counters header, then h [T*k][I]
-    assert moe.moe_experts_decode_workspace(1, 10, s) == 16640 + 10 * 640 * 4
+    # counters header, then 1024 tagged 8-byte logits per token, then FP32 h
+    # [T*k][I] (the other decode paths keep theirs right after the header)
+    assert moe.moe_experts_decode_workspace(1, 10, s) == 16640 + 1024 * 8 + 10 * 640 * 4
+    assert moe.moe_experts_decode_workspace(32, 10, s) == 16640 + 32 * 1024 * 8 + 32 * 10 * 640 * 4
 
 
 def test_wait_limit_hook_rejects_bad_values(lib):

@@ -33,7 +33,7 @@ def _per_layer(x0, wr, ptrs, s, k, bias=None, eps=1e-6):
 
 def _gave_up(ws):
     """The first wait that gave up, as recorded in the workspace header."""
-    v = int(ws[128:136].cpu().numpy().view(np.uint64)[0])
+    v = int(ws[192:200].cpu().numpy().view(np.uint64)[0])
     return {"site": v >> 56, "layer": ((v >> 32) & 0xFFFFFF) - 1, "block": v & 0xFFFFFFFF} if v else None
 
 

@@ -1185,6 +1185,25 @@ def run_profile_case(args):
             x = synth.activations(1, H, synth.seed_of(0, 50 + i, synth.T_X), device=dev)
             moe.moe_decode_layer(wr, None, K_TOP, ptrs, s, x=x, y=y, workspace=ws)
         torch.cuda.synchronize()
+    elif args.profile_case == "deepseek_call":
+        # the DeepSeek-shaped call (router over 384 MXFP4 experts, top-6, then
+        # the ring kernel's expert pass) over 16 distinct records (301 MB):
+        # expert e uses record e % 16
+        D = DeepSeekCalls
+        s = moe.shape(D.HD, D.ID, moe.FMT_MXFP4)
+        nE = 16
+        pool = torch.empty(nE, moe.moe_expert_record_bytes(s), dtype=torch.uint8, device=dev)
+        for e in range(nE):
+            g, up, d = synth.expert_weights(D.HD, D.ID, synth.expert_seed(D.WORKLOAD, 0, e), device=dev)
+            moe.fp4_pack_expert(g, up, d, s, record=pool[e])
+        ptrs = moe.pointer_table([pool[e % nE] for e in range(D.NE)])
+        ws = torch.zeros(moe.moe_experts_decode_workspace(1, D.KD, s), dtype=torch.uint8, device=dev)
+        for i in range(args.warmup + args.steps):
+            wr = synth.router_weights(D.NE, D.HD, synth.seed_of(D.WORKLOAD, i, synth.T_ROUTER), device=dev)
+            x = synth.activations(1, D.HD, synth.seed_of(D.WORKLOAD, i, synth.T_X), device=dev)
+            idx, w, _ = moe.moe_router_topk(x, wr, None, D.KD)
+            moe.moe_experts_decode(x, idx, w, ptrs, s, workspace=ws)
+        torch.cuda.synchronize()
     else:
         pl = PromptLayer(torch, moe, synth, dev)
         for _ in range(args.warmup + args.steps):
@@ -1204,7 +1223,7 @@ def main():
     ap.add_argument("--no-prompt", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the one-layer, DeepSeek-shaped and batched workloads")
     ap.add_argument("--cpu-seconds-other", type=float, default=6.0)
-    ap.add_argument("--profile-case", choices=("none", "decode_layer", "prompt_layer"), default="none",
+    ap.add_argument("--profile-case", choices=("none", "decode_layer", "prompt_layer", "deepseek_call"), default="none",
                     help="small fixed case for ncu captures (no JSON line)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

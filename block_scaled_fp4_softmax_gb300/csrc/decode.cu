@@ -246,10 +246,10 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(
 // ---------------------------------------------------------------------------
 namespace st {
 
-constexpr int kThreads = 512;      // warps 0-14 consume, warp 15 lanes 0-3 produce
+constexpr int kThreads = 512;      // warps 0-14 consume, warp 15 lanes 0-15 produce
 constexpr int kCWarps = 15;
 constexpr int kCThreads = kCWarps * 32;
-constexpr int kProdLanes = 4;
+constexpr int kProdLanes = 16;  // copies issued by 16 lanes: measured faster than 4
 constexpr int kMaxSlots = 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -282,20 +282,82 @@ __host__ __device__ inline Win window(size_t start, size_t len) {
   return w;
 }
 
-// Host and device agree on the chunk plan: a gate/up chunk is one row pair
-// (gate row | up row | gate scale window | up scale window); a down chunk is
-// one output row of one token for experts [j0, j0 + jn) (per expert: row of
-// codes | scale window).  The slot holds the larger of a gate/up chunk and
-// one expert row of down.
+// Host and device agree on the chunk plan.  A gate/up chunk is up to kRG
+// consecutive row pairs of one routed pair (gate rows | up rows | gate scale
+// window | up scale window); a down chunk is up to kRD consecutive output
+// rows of one token for experts [j0, j0 + jn) (per expert: rows of codes |
+// scale window).  A bulk copy carries several rows, so each of the few copies
+// an SM keeps in flight moves kilobytes rather than one row and a sliver of
+// scales.  The slot holds the larger of a gate/up chunk and one expert's down
+// part; jn experts' down parts fill it.
+constexpr int kRG = 4;  // row pairs per gate/up chunk
+constexpr int kRD = 4;  // output rows per down chunk
+static_assert(kRG == kRD, "a slot's empty barrier counts one arrival per row of either kind of chunk");
+__host__ __device__ inline int gu_scale_room(int H, int G) { return (kRG * (H / G) + 32 + 15) & ~15; }
+__host__ __device__ inline int dn_part_bytes(int I, int G) { return kRD * (I / 2) + ((kRD * (I / G) + 32 + 15) & ~15); }
 __host__ __device__ inline int plan_slot_bytes(int H, int I, int G) {
-  const int p1 = 2 * (H / 2) + 2 * (H / G + 32);
-  const int p2 = I / 2 + I / G + 32;
+  const int p1 = 2 * kRG * (H / 2) + 2 * gu_scale_room(H, G);
+  const int p2 = dn_part_bytes(I, G);
   const int s = p1 > p2 ? p1 : p2;
   return (s + 127) & ~127;
 }
 __host__ __device__ inline int plan_jn(int k, int I, int G, int slot_bytes) {
-  const int j = slot_bytes / (I / 2 + I / G + 32);
+  const int j = slot_bytes / dn_part_bytes(I, G);
   return j < 1 ? 1 : (j > k ? k : j);
+}
+
+// Gate/up chunk c of the row range [r0, r1) (rows r = p * I + i): the range
+// split at pair boundaries, each piece into runs of at most kRG rows.  Sets
+// the first row and the row count; false past the last chunk.
+__device__ __forceinline__ bool gu_chunk(int c, long long r0, long long r1, int I, long long& rs, int& nr) {
+  long long r = r0;
+  while (r < r1) {
+    const long long seg_end = min(r1, (r / I + 1) * (long long)I);
+    const long long n = (seg_end - r + kRG - 1) / kRG;
+    if (c < n) {
+      rs = r + (long long)c * kRG;
+      nr = (int)min((long long)kRG, seg_end - rs);
+      return true;
+    }
+    c -= (int)n;
+    r = seg_end;
+  }
+  return false;
+}
+__device__ __forceinline__ int gu_chunks(long long r0, long long r1, int I) {
+  int n = 0;
+  for (long long r = r0; r < r1;) {
+    const long long seg_end = min(r1, (r / I + 1) * (long long)I);
+    n += (int)((seg_end - r + kRG - 1) / kRG);
+    r = seg_end;
+  }
+  return n;
+}
+// The same for blocks of output rows of [q0, q1) (rows q = t * H + n), split
+// at token boundaries and into runs of at most kRD rows.
+__device__ __forceinline__ bool dn_block(int b, long long q0, long long q1, int H, long long& qs, int& nd) {
+  long long q = q0;
+  while (q < q1) {
+    const long long seg_end = min(q1, (q / H + 1) * (long long)H);
+    const long long n = (seg_end - q + kRD - 1) / kRD;
+    if (b < n) {
+      qs = q + (long long)b * kRD;
+      nd = (int)min((long long)kRD, seg_end - qs);
+      return true;
+    }
+    b -= (int)n;
+    q = seg_end;
+  }
+  return false;
+}
+__device__ __forceinline__ int dn_blocks(long long q0, long long q1, int H) {
+  int n = 0;
+  for (long long q = q0; q < q1;) {
+    const long long seg_end = min(q1, (q / H + 1) * (long long)H);
+    n += (int)((seg_end - q + kRD - 1) / kRD);
+    q = seg_end;
+  }
+  return n;
 }
 
 // FP16 x FP16 -> FP32 fused multiply-add (the product is exact in FP32).
@@ -413,13 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   const long long q0 = (long long)blockIdx.x * R2 / gridDim.x, q1 = (long long)(blockIdx.x + 1) * R2 / gridDim.x;
   const int jn = a.jn;
   const int cpr = (a.k + jn - 1) / jn;  // down chunks per output row
-  const int n1 = (int)(r1 - r0);        // gate/up chunks of this CTA
-  const int n2 = (int)(q1 - q0) * cpr;  // down chunks of this CTA
+  const int n1 = gu_chunks(r0, r1, a.I);  // gate/up chunks of this CTA
+  const int nb2 = dn_blocks(q0, q1, a.H);  // blocks of output rows
+  const int n2 = nb2 * cpr;                // down chunks of this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxSlots; ++s) {
       moe::tc::mbar_init(&full[s], 1);
-      moe::tc::mbar_init(&empty[s], 1);
+      moe::tc::mbar_init(&empty[s], kRG);  // one arrival per row of the chunk
       slot_fill[s] = -1;
     }
     flags[0] = 0;
@@ -476,39 +539,45 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
         if (!(ok = claim(c))) break;
         const int slot = c % S;
         const uint32_t base = moe::tc::smem_u32(ring + (size_t)slot * SB);
-        if (c < n1) {  // gate/up row pair
-          const long long r = r0 + c;
-          const int p = (int)(r / a.I), i = (int)(r - (long long)p * a.I);
+        if (c < n1) {  // gate/up: rows [i, i + nr) of pair p
+          long long rs = 0;
+          int nr = 0;
+          gu_chunk(c, r0, r1, a.I, rs, nr);
+          const int p = (int)(rs / a.I), i = (int)(rs - (long long)p * a.I);
           const uint8_t* rec = recs[p];
-          const uint32_t cb = (uint32_t)(a.H / 2);
-          const Win gw = window(o.gate_s + (size_t)i * (a.H / G), a.H / G);
-          const Win uw = window(o.up_s + (size_t)i * (a.H / G), a.H / G);
-          moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? 2 * cb + gw.bytes + uw.bytes : 0);
+          const uint32_t cb = (uint32_t)(a.H / 2), gb = (uint32_t)nr * cb;
+          const Win gw = window(o.gate_s + (size_t)i * (a.H / G), (size_t)nr * (a.H / G));
+          const Win uw = window(o.up_s + (size_t)i * (a.H / G), (size_t)nr * (a.H / G));
+          const uint32_t so = 2u * kRG * cb, room = (uint32_t)gu_scale_room(a.H, G);
+          moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? 2 * gb + gw.bytes + uw.bytes : 0);
           if (rec) {
-            moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i * cb, cb, &full[slot]);
-            moe::tc::bulk_g2s(base + cb, rec + o.up + (size_t)i * cb, cb, &full[slot]);
-            moe::tc::bulk_g2s(base + 2 * cb, rec + gw.lo, gw.bytes, &full[slot]);
-            moe::tc::bulk_g2s(base + 2 * cb + gw.bytes, rec + uw.lo, uw.bytes, &full[slot]);
+            moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i * cb, gb, &full[slot]);
+            moe::tc::bulk_g2s(base + kRG * cb, rec + o.up + (size_t)i * cb, gb, &full[slot]);
+            moe::tc::bulk_g2s(base + so, rec + gw.lo, gw.bytes, &full[slot]);
+            moe::tc::bulk_g2s(base + so + room, rec + uw.lo, uw.bytes, &full[slot]);
           }
-        } else {  // down: one output row, experts [j0, j1)
+        } else {  // down: output rows [n, n + nd) of token t, experts [j0, j1)
           const int c2 = c - n1;
-          const long long q = q0 + c2 / cpr;
-          const int t = (int)(q / a.H), n = (int)(q - (long long)t * a.H);
+          long long qs = 0;
+          int nd = 0;
+          dn_block(c2 / cpr, q0, q1, a.H, qs, nd);
+          const int t = (int)(qs / a.H), n = (int)(qs - (long long)t * a.H);
           const int j0 = (c2 % cpr) * jn, j1 = min(a.k, j0 + jn);
-          const uint32_t cb = (uint32_t)(a.I / 2);
-          const Win dw = window(o.down_s + (size_t)n * (a.I / G), a.I / G);
+          const uint32_t cb = (uint32_t)(a.I / 2), db = (uint32_t)nd * cb;
+          const Win dw = window(o.down_s + (size_t)n * (a.I / G), (size_t)nd * (a.I / G));
+          const uint32_t per = (uint32_t)dn_part_bytes(a.I, G);
           uint32_t total = 0;
           for (int j = j0; j < j1; ++j)
-            if (recs[t * a.k + j]) total += cb + dw.bytes;
+            if (recs[t * a.k + j]) total += db + dw.bytes;
           moe::tc::mbar_arrive_expect_tx(&full[slot], total);
           uint32_t off = 0;
           for (int j = j0; j < j1; ++j) {
             const uint8_t* rec = recs[t * a.k + j];
             if (rec) {
-              moe::tc::bulk_g2s(base + off, rec + o.down + (size_t)n * cb, cb, &full[slot]);
-              moe::tc::bulk_g2s(base + off + cb, rec + dw.lo, dw.bytes, &full[slot]);
+              moe::tc::bulk_g2s(base + off, rec + o.down + (size_t)n * cb, db, &full[slot]);
+              moe::tc::bulk_g2s(base + off + kRD * cb, rec + dw.lo, dw.bytes, &full[slot]);
             }
-            off += cb + dw.bytes;
+            off += per;
           }
         }
       }
@@ -538,20 +607,32 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
       }
       return true;
     };
-    auto release = [&](int chunk) {
+    // a chunk's slot is free once every row of it is done: the warp of each
+    // row arrives once, the warp of its last row also for the rows a ragged
+    // chunk lacks
+    auto release = [&](int chunk, int row, int rows) {
       __syncwarp();
-      if (lane == 0) moe::tc::mbar_arrive(&empty[chunk % S]);
+      if (lane == 0) moe::tc::mbar_arrive_n(&empty[chunk % S], row == rows - 1 ? (uint32_t)(kRG - rows + 1) : 1u);
     };
-    // gate/up + SwiGLU: chunk c (one row pair) -> warp c % 15
-    for (int c = warp; c < n1; c += kCWarps) {
+    // gate/up + SwiGLU: task (chunk c, row ri) -> warp (c kRG + ri) % 15, so
+    // the rows of one chunk (copied together) are computed by several warps
+    // at once.  Lane l takes units l, l + 32, ... of the row, in that order.
+    for (int task = warp; task < n1 * kRG; task += kCWarps) {
+      const int c = task / kRG, ri = task - c * kRG;
+      long long rs = 0;
+      int nr = 0;
+      gu_chunk(c, r0, r1, a.I, rs, nr);
+      if (ri >= nr) continue;
       const bool live = take(c);
-      const long long r = r0 + c;
-      const int p = (int)(r / a.I), i = (int)(r - (long long)p * a.I);
+      const int p = (int)(rs / a.I), i0 = (int)(rs - (long long)p * a.I);
       const uint8_t* rec = recs[p];
       const uint8_t* base = ring + (size_t)(c % S) * SB;
-      const uint32_t cb = (uint32_t)(a.H / 2);
-      const Win gw = window(o.gate_s + (size_t)i * (a.H / G), a.H / G);
-      const Win uw = window(o.up_s + (size_t)i * (a.H / G), a.H / G);
+      const uint32_t cb = (uint32_t)(a.H / 2), so = 2u * kRG * cb, room = (uint32_t)gu_scale_room(a.H, G);
+      const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)nr * (a.H / G));
+      const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)nr * (a.H / G));
+      const uint8_t* crow = base + (size_t)ri * cb;
+      const uint8_t* gsr = base + so + gw.delta + (size_t)ri * (a.H / G);
+      const uint8_t* usr = base + so + room + uw.delta + (size_t)ri * (a.H / G);
       const uint4* xt = act + (size_t)(p / a.k) * 4 * upr;
       float gs = 0.f, us = 0.f;
       if (live && rec) {
@@ -562,9 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
             if (u < 2 * UPR) {
               const bool is_up = u >= UPR;
               const int cix = is_up ? u - UPR : u;
-              const uint4 q = *reinterpret_cast<const uint4*>(base + (is_up ? cb : 0) + 16 * cix);
-              const uint8_t* sp = base + 2 * cb + (is_up ? gw.bytes + uw.delta : gw.delta) + sstep * cix;
-              const float d = unit_dot_h<FMT, UPR>(q, scale_bits<FMT>(sp), xt + cix, UPR);
+              const uint4 q = *reinterpret_cast<const uint4*>(crow + (is_up ? kRG * cb : 0u) + 16 * cix);
+              const float d = unit_dot_h<FMT, UPR>(q, scale_bits<FMT>((is_up ? usr : gsr) + sstep * cix), xt + cix, UPR);
               if (is_up) us += d;
               else gs += d;
             }
@@ -573,19 +653,18 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
           for (int u = lane; u < 2 * upr; u += 32) {
             const bool is_up = u >= upr;
             const int cix = is_up ? u - upr : u;
-            const uint4 q = *reinterpret_cast<const uint4*>(base + (is_up ? cb : 0) + 16 * cix);
-            const uint8_t* sp = base + 2 * cb + (is_up ? gw.bytes + uw.delta : gw.delta) + sstep * cix;
-            const float d = unit_dot_h<FMT, 0>(q, scale_bits<FMT>(sp), xt + cix, upr);
+            const uint4 q = *reinterpret_cast<const uint4*>(crow + (is_up ? kRG * cb : 0u) + 16 * cix);
+            const float d = unit_dot_h<FMT, 0>(q, scale_bits<FMT>((is_up ? usr : gsr) + sstep * cix), xt + cix, upr);
             if (is_up) us += d;
             else gs += d;
           }
         }
       }
-      release(c);
+      release(c, ri, nr);
       gs = moe::warp_sum(gs);
       us = moe::warp_sum(us);
       if (lane == 0)
-        a.hws[(size_t)p * a.I + i] =
+        a.hws[(size_t)p * a.I + i0 + ri] =
             (live && rec) ? gs / (1.0f + expf(-gs)) * us : __uint_as_float(0x7FC00000u);
     }
     // grid barrier among the consumer threads of every CTA
@@ -647,21 +726,37 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
         }
       }
       moe::tc::named_sync(1, kCThreads);
-      // down + weighted combine: output row rr of this CTA -> warp rr % 15,
-      // which walks its row's chunks (experts in ascending order)
-      for (int rr = warp; rr < (int)(q1 - q0); rr += kCWarps) {
-        const long long q = q0 + rr;
-        const int t = (int)(q / a.H), n = (int)(q - (long long)t * a.H);
-        float acc = 0.f;
+      // down + weighted combine: task (block bi of up to kRD output rows, kTR
+      // of its rows from rb on) -> warp (task) % 15, which walks the block's
+      // chunks (experts in ascending order).  Lane l takes the flattened
+      // (expert, unit) items l, l + 32, ... of the task's rows, in that
+      // order, each item's h loaded once for them.  One row per task: two
+      // (h shared) measured slower, the fewer tasks leaving warps idle.
+      constexpr int kTR = 1;  // rows per task
+      static_assert(kRD % kTR == 0, "row tasks tile a block");
+      for (int task = warp; task < nb2 * (kRD / kTR); task += kCWarps) {
+        const int bi = task / (kRD / kTR), rb = (task - bi * (kRD / kTR)) * kTR;
+        long long qs = 0;
+        int nd = 0;
+        dn_block(bi, q0, q1, a.H, qs, nd);
+        if (rb >= nd) continue;
+        const int nr = min(kTR, nd - rb);
+        // this task's arrivals on each chunk: its rows, and, for the task of
+        // the block's last row, the rows a ragged block lacks
+        const uint32_t arrivals = rb + kTR >= nd ? (uint32_t)(kRD - rb) : (uint32_t)kTR;
+        const int t = (int)(qs / a.H), n0 = (int)(qs - (long long)t * a.H);
+        float acc[kTR];
+#pragma unroll
+        for (int r = 0; r < kTR; ++r) acc[r] = 0.f;
         bool bad = false;
         for (int cc = 0; cc < cpr; ++cc) {
-          const int c = n1 + rr * cpr + cc;
+          const int c = n1 + bi * cpr + cc;
           const bool live = take(c);
           const uint8_t* base = ring + (size_t)(c % S) * SB;
           const int j0 = cc * jn, j1 = min(a.k, j0 + jn);
           const uint32_t cb = (uint32_t)(a.I / 2);
-          const Win dw = window(o.down_s + (size_t)n * (a.I / G), a.I / G);
-          const uint32_t per = cb + dw.bytes;  // bytes per expert in the slot
+          const Win dw = window(o.down_s + (size_t)n0 * (a.I / G), (size_t)nd * (a.I / G));
+          const uint32_t per = (uint32_t)dn_part_bytes(a.I, G);
           for (int j = j0; j < j1; ++j)
             if (!(live && recs[t * a.k + j])) bad = true;
           if (!bad) {
@@ -671,17 +766,35 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
               const int jj = f / updr, u = f - jj * updr;
               const int pj = t * a.k + j0 + jj;
               const uint8_t* eb = base + (size_t)jj * per;
-              const uint4 qv = *reinterpret_cast<const uint4*>(eb + 16 * u);
-              const uint8_t* sp = eb + cb + dw.delta + sstep * u;
+              const uint8_t* sp = eb + kRD * cb + dw.delta + (size_t)rb * (a.I / G) + sstep * u;
               const size_t col = (size_t)(pj - t_lo * a.k) * 4 * updr + u;
-              acc += wts[pj] * unit_dot_h2<FMT, UPDR>(qv, scale_bits<FMT>(sp), hhi + col, hlo + col, updr);
+              uint4 hh[4], hl[4];
+#pragma unroll
+              for (int wi = 0; wi < 4; ++wi) {
+                hh[wi] = hhi[col + (size_t)wi * updr];
+                hl[wi] = hlo[col + (size_t)wi * updr];
+              }
+              const float wt = wts[pj];
+#pragma unroll
+              for (int r = 0; r < kTR; ++r) {
+                if (r < nr)
+                  acc[r] += wt * unit_dot_h2<FMT, 1>(
+                                     *reinterpret_cast<const uint4*>(eb + (size_t)(rb + r) * cb + 16 * u),
+                                     scale_bits<FMT>(sp + (size_t)r * (a.I / G)), hh, hl, 1);
+              }
             }
           }
-          release(c);
+          __syncwarp();
+          if (lane == 0) moe::tc::mbar_arrive_n(&empty[c % S], arrivals);
         }
-        acc = moe::warp_sum(acc);
-        if (lane == 0)
-          a.y[(size_t)t * a.H + n] = (bad || *abort_flag) ? __uint_as_float(0x7FC00000u) : acc;
+#pragma unroll
+        for (int r = 0; r < kTR; ++r) {
+          if (r < nr) {
+            const float v = moe::warp_sum(acc[r]);
+            if (lane == 0)
+              a.y[(size_t)t * a.H + n0 + rb + r] = (bad || *abort_flag) ? __uint_as_float(0x7FC00000u) : v;
+          }
+        }
       }
     }
   }
@@ -721,8 +834,8 @@ int stream_smem_limit() { return moe::device_info().smem_optin; }
 
 int sm_count() { return moe::device_info().sms; }
 
-// The streaming kernel takes T*k <= 64 pairs when at least 16 ring slots fit
-// next to the activations.
+// The streaming kernel takes T*k <= 64 pairs when at least 4 ring slots (of
+// kRG row pairs each) fit next to the activations.
 int stream_slots(int T, int k, int H, int I, int fmt, int* slot_bytes) {
   const int sms = sm_count();
   if (sms <= 0 || (long long)T * k > 64) return 0;
@@ -732,7 +845,7 @@ int stream_slots(int T, int k, int H, int I, int fmt, int* slot_bytes) {
   const size_t fixed = st::smem_bytes(T, k, H, I, sms, 0, *slot_bytes) + 1024;
   if (fixed >= limit) return 0;
   const int slots = (int)std::min<size_t>(st::kMaxSlots, (limit - fixed) / *slot_bytes);
-  return slots >= 16 ? slots : 0;
+  return slots >= 4 ? slots : 0;
 }
 
 template <int FMT, int UPR, int UPDR>

@@ -68,6 +68,21 @@ def test_decode_mxfp4_deepseek_shape():
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("T", [4, 6])
+def test_decode_ring_multi_row_chunks(pool64, T):
+    """Shapes the one-shot plan does not take but the ring kernel does (T*k
+    <= 64): its chunks of several row pairs and blocks of several output rows
+    are cut at pair and token boundaries and end ragged."""
+    err, _ = _decode_vs_oracle(pool64, T, 10, seed=200 + T)
+    assert err <= TOL, err
+
+
+def test_decode_ring_mxfp4_two_tokens():
+    pool = Pool(12, 4096, 2880, 1, workload=3)
+    err, _ = _decode_vs_oracle(pool, 2, 6, seed=33)
+    assert err <= TOL, err
+
+
 def test_decode_small_shapes():
     pool = Pool(8, 128, 64, 0, workload=9)
     err, _ = _decode_vs_oracle(pool, 3, 4, seed=31)

@@ -234,11 +234,11 @@ __global__ void __launch_bounds__(kThreads) decode_down_kernel(
 // Raises a kernel's dynamic shared-memory limit once (the attribute call is
 // not repeated, so later launches can be captured in a CUDA graph).
 // ---------------------------------------------------------------------------
-// Streaming expert pass (T*k <= 64): one CTA per SM.  One producer thread
-// walks this CTA's share of the selected records -- first the gate/up rows,
-// then the down rows -- and moves it with 1-D TMA bulk copies into a ring of
-// shared-memory slots, so every byte the CTA needs is requested at kernel
-// entry and the HBM pipe stays full.  Fifteen consumer warps compute from
+// Streaming expert pass (T*k <= 512): one CTA per SM.  Producer lanes walk
+// this CTA's share of the selected records -- first the gate/up rows, then
+// the down rows -- and move it with 1-D TMA bulk copies of several rows each
+// into a ring of shared-memory slots, refilled as soon as a slot's rows are
+// done, so the HBM pipe stays full.  Fifteen consumer warps compute from
 // shared memory: gate/up + SwiGLU rows -> h (global scratch), one grid
 // barrier, then down rows against h and the weighted combine, accumulated per
 // output row in a fixed order (bit-reproducible).  Slots that hold down rows
@@ -251,6 +251,7 @@ constexpr int kCWarps = 15;
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kProdLanes = 16;  // copies issued by 16 lanes: measured faster than 4
 constexpr int kMaxSlots = 64;
+constexpr int kMaxPairs = 512;  // routed pairs (T*k) of one launch
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Args {
@@ -293,7 +294,7 @@ __host__ __device__ inline Win window(size_t start, size_t len) {
 constexpr int kRG = 4;  // row pairs per gate/up chunk
 constexpr int kRD = 4;  // output rows per down chunk
 static_assert(kRG == kRD, "a slot's empty barrier counts one arrival per row of either kind of chunk");
-__host__ __device__ inline int gu_scale_room(int H, int G) { return (kRG * (H / G) + 32 + 15) & ~15; }
+__host__ __device__ inline int gu_scale_room(int H, int G) { return (kRG * (H / G) + 64 + 15) & ~15; }
 __host__ __device__ inline int dn_part_bytes(int I, int G) { return kRD * (I / 2) + ((kRD * (I / G) + 32 + 15) & ~15); }
 __host__ __device__ inline int plan_slot_bytes(int H, int I, int G) {
   const int p1 = 2 * kRG * (H / 2) + 2 * gu_scale_room(H, G);
@@ -306,55 +307,45 @@ __host__ __device__ inline int plan_jn(int k, int I, int G, int slot_bytes) {
   return j < 1 ? 1 : (j > k ? k : j);
 }
 
-// Gate/up chunk c of the row range [r0, r1) (rows r = p * I + i): the range
-// split at pair boundaries, each piece into runs of at most kRG rows.  Sets
-// the first row and the row count; false past the last chunk.
-__device__ __forceinline__ bool gu_chunk(int c, long long r0, long long r1, int I, long long& rs, int& nr) {
-  long long r = r0;
-  while (r < r1) {
-    const long long seg_end = min(r1, (r / I + 1) * (long long)I);
-    const long long n = (seg_end - r + kRG - 1) / kRG;
-    if (c < n) {
-      rs = r + (long long)c * kRG;
-      nr = (int)min((long long)kRG, seg_end - rs);
-      return true;
-    }
-    c -= (int)n;
-    r = seg_end;
-  }
-  return false;
+// Gate/up chunk c of the CTA's row range [r0, r1) (row r = p * I + i): rows
+// [rs, rs + nr), rs = r0 + kRG c.  As kRG <= I it crosses at most one pair
+// boundary: piece 0 is rows [i0, i0 + n0) of pair p0, piece 1 (nr - n0 rows,
+// possibly none) rows from 0 of pair p0 + 1.  O(1), 32-bit.
+struct GuChunk {
+  int rs, nr, p0, i0, n0;
+};
+__device__ __forceinline__ GuChunk gu_chunk(int c, int r0, int r1, int I) {
+  GuChunk g;
+  g.rs = r0 + c * kRG;
+  g.nr = min(kRG, r1 - g.rs);
+  g.p0 = g.rs / I;
+  g.i0 = g.rs - g.p0 * I;
+  g.n0 = min(g.nr, I - g.i0);
+  return g;
 }
-__device__ __forceinline__ int gu_chunks(long long r0, long long r1, int I) {
-  int n = 0;
-  for (long long r = r0; r < r1;) {
-    const long long seg_end = min(r1, (r / I + 1) * (long long)I);
-    n += (int)((seg_end - r + kRG - 1) / kRG);
-    r = seg_end;
-  }
-  return n;
-}
-// The same for blocks of output rows of [q0, q1) (rows q = t * H + n), split
-// at token boundaries and into runs of at most kRD rows.
-__device__ __forceinline__ bool dn_block(int b, long long q0, long long q1, int H, long long& qs, int& nd) {
-  long long q = q0;
+__host__ __device__ inline int gu_chunks(int r0, int r1) { return (r1 - r0 + kRG - 1) / kRG; }
+// Blocks of output rows of [q0, q1) (row q = t * H + n), split at token
+// boundaries and into runs of at most kRD rows; a CTA's rows span few tokens.
+__device__ __forceinline__ bool dn_block(int b, int q0, int q1, int H, int& qs, int& nd) {
+  int q = q0;
   while (q < q1) {
-    const long long seg_end = min(q1, (q / H + 1) * (long long)H);
-    const long long n = (seg_end - q + kRD - 1) / kRD;
+    const int seg_end = min(q1, (q / H + 1) * H);
+    const int n = (seg_end - q + kRD - 1) / kRD;
     if (b < n) {
-      qs = q + (long long)b * kRD;
-      nd = (int)min((long long)kRD, seg_end - qs);
+      qs = q + b * kRD;
+      nd = min(kRD, seg_end - qs);
       return true;
     }
-    b -= (int)n;
+    b -= n;
     q = seg_end;
   }
   return false;
 }
-__device__ __forceinline__ int dn_blocks(long long q0, long long q1, int H) {
+__device__ __forceinline__ int dn_blocks(int q0, int q1, int H) {
   int n = 0;
-  for (long long q = q0; q < q1;) {
-    const long long seg_end = min(q1, (q / H + 1) * (long long)H);
-    n += (int)((seg_end - q + kRD - 1) / kRD);
+  for (int q = q0; q < q1;) {
+    const int seg_end = min(q1, (q / H + 1) * H);
+    n += (seg_end - q + kRD - 1) / kRD;
     q = seg_end;
   }
   return n;
@@ -453,9 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   uint8_t* ring = smem;                                                   // S x SB
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * SB);
   uint64_t* empty = full + kMaxSlots;
-  const uint8_t** recs = reinterpret_cast<const uint8_t**>(empty + kMaxSlots);  // [64]
-  float* wts = reinterpret_cast<float*>(recs + 64);                              // [64]
-  int* flags = reinterpret_cast<int*>(wts + 64);  // [0] abort, [1] barrier ok
+  const int P = a.T * a.k, Pr = (P + 15) & ~15;
+  const uint8_t** recs = reinterpret_cast<const uint8_t**>(empty + kMaxSlots);  // [Pr]
+  float* wts = reinterpret_cast<float*>(recs + Pr);                              // [Pr]
+  int* flags = reinterpret_cast<int*>(wts + Pr);  // [0] abort, [1] barrier ok
   // slot_fill[s]: the last chunk a producer started in slot s.  A barrier's
   // parity is only meaningful once the slot is on the right fill: consumers
   // first wait for slot_fill == chunk, producers for slot_fill == chunk - S.
@@ -469,13 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int G = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   constexpr int sstep = FMT == MOE_FMT_NVFP4 ? 2 : 1;
-  const int P = a.T * a.k;
   const long long R1 = (long long)P * a.I, R2 = (long long)a.T * a.H;
-  const long long r0 = (long long)blockIdx.x * R1 / gridDim.x, r1 = (long long)(blockIdx.x + 1) * R1 / gridDim.x;
-  const long long q0 = (long long)blockIdx.x * R2 / gridDim.x, q1 = (long long)(blockIdx.x + 1) * R2 / gridDim.x;
+  // row ranges of this CTA (32-bit: T*k*I and T*H stay below 2^23 here)
+  const int r0 = (int)((long long)blockIdx.x * R1 / gridDim.x), r1 = (int)((long long)(blockIdx.x + 1) * R1 / gridDim.x);
+  const int q0 = (int)((long long)blockIdx.x * R2 / gridDim.x), q1 = (int)((long long)(blockIdx.x + 1) * R2 / gridDim.x);
   const int jn = a.jn;
   const int cpr = (a.k + jn - 1) / jn;  // down chunks per output row
-  const int n1 = gu_chunks(r0, r1, a.I);  // gate/up chunks of this CTA
+  const int n1 = gu_chunks(r0, r1);        // gate/up chunks of this CTA
   const int nb2 = dn_blocks(q0, q1, a.H);  // blocks of output rows
   const int n2 = nb2 * cpr;                // down chunks of this CTA
 
@@ -490,15 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
     moe::tc::mbar_fence_init();
   }
   moe::pdl_wait();
-  if (threadIdx.x < P) {
-    recs[threadIdx.x] = checked_record(a.idx[threadIdx.x], a.E, a.ptrs,
-                                       blockIdx.x == 0 ? a.status : nullptr);
-    wts[threadIdx.x] = a.w[threadIdx.x];
+  for (int p = threadIdx.x; p < P; p += kThreads) {
+    recs[p] = checked_record(a.idx[p], a.E, a.ptrs, blockIdx.x == 0 ? a.status : nullptr);
+    wts[p] = a.w[p];
   }
-  // x of every token as FP16 quads [t][4][H/32] (8 values per uint4)
-  for (int h0 = threadIdx.x * 8; h0 < a.T * a.H; h0 += kThreads * 8) {
+  // x of the tokens of this CTA's gate/up rows, [xt0, xt1], as FP16 quads
+  // [t - xt0][4][H/32] (8 values per uint4)
+  const int xt0 = r1 > r0 ? (r0 / a.I) / a.k : 0;
+  const int xt1 = r1 > r0 ? ((r1 - 1) / a.I) / a.k : -1;
+  for (int h0 = threadIdx.x * 8; h0 < (xt1 - xt0 + 1) * a.H; h0 += kThreads * 8) {
     const int t = h0 / a.H, hh = h0 - t * a.H;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + h0));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)xt0 * a.H + h0));
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
     uint32_t o4[4];
 #pragma unroll
@@ -539,29 +533,39 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
         if (!(ok = claim(c))) break;
         const int slot = c % S;
         const uint32_t base = moe::tc::smem_u32(ring + (size_t)slot * SB);
-        if (c < n1) {  // gate/up: rows [i, i + nr) of pair p
-          long long rs = 0;
-          int nr = 0;
-          gu_chunk(c, r0, r1, a.I, rs, nr);
-          const int p = (int)(rs / a.I), i = (int)(rs - (long long)p * a.I);
-          const uint8_t* rec = recs[p];
-          const uint32_t cb = (uint32_t)(a.H / 2), gb = (uint32_t)nr * cb;
-          const Win gw = window(o.gate_s + (size_t)i * (a.H / G), (size_t)nr * (a.H / G));
-          const Win uw = window(o.up_s + (size_t)i * (a.H / G), (size_t)nr * (a.H / G));
-          const uint32_t so = 2u * kRG * cb, room = (uint32_t)gu_scale_room(a.H, G);
-          moe::tc::mbar_arrive_expect_tx(&full[slot], rec ? 2 * gb + gw.bytes + uw.bytes : 0);
-          if (rec) {
-            moe::tc::bulk_g2s(base, rec + o.gate + (size_t)i * cb, gb, &full[slot]);
-            moe::tc::bulk_g2s(base + kRG * cb, rec + o.up + (size_t)i * cb, gb, &full[slot]);
-            moe::tc::bulk_g2s(base + so, rec + gw.lo, gw.bytes, &full[slot]);
-            moe::tc::bulk_g2s(base + so + room, rec + uw.lo, uw.bytes, &full[slot]);
+        if (c < n1) {  // gate/up: rows [rs, rs + nr), one or two pieces (one per pair)
+          const GuChunk gc = gu_chunk(c, r0, r1, a.I);
+          const uint32_t cb = (uint32_t)(a.H / 2), so = 2u * kRG * cb, room = (uint32_t)gu_scale_room(a.H, G);
+          Win gw[2], uw[2];
+          uint32_t total = 0;
+#pragma unroll
+          for (int pc = 0; pc < 2; ++pc) {
+            const int n = pc == 0 ? gc.n0 : gc.nr - gc.n0, i = pc == 0 ? gc.i0 : 0;
+            gw[pc] = window(o.gate_s + (size_t)i * (a.H / G), (size_t)n * (a.H / G));
+            uw[pc] = window(o.up_s + (size_t)i * (a.H / G), (size_t)n * (a.H / G));
+            if (n > 0 && recs[gc.p0 + pc]) total += 2u * n * cb + gw[pc].bytes + uw[pc].bytes;
+          }
+          moe::tc::mbar_arrive_expect_tx(&full[slot], total);
+          uint32_t gso = 0, uso = 0;
+#pragma unroll
+          for (int pc = 0; pc < 2; ++pc) {
+            const int n = pc == 0 ? gc.n0 : gc.nr - gc.n0, i = pc == 0 ? gc.i0 : 0, roff = pc == 0 ? 0 : gc.n0;
+            const uint8_t* rec = n > 0 ? recs[gc.p0 + pc] : nullptr;
+            if (rec) {
+              const uint32_t gb = (uint32_t)n * cb;
+              moe::tc::bulk_g2s(base + roff * cb, rec + o.gate + (size_t)i * cb, gb, &full[slot]);
+              moe::tc::bulk_g2s(base + kRG * cb + roff * cb, rec + o.up + (size_t)i * cb, gb, &full[slot]);
+              moe::tc::bulk_g2s(base + so + gso, rec + gw[pc].lo, gw[pc].bytes, &full[slot]);
+              moe::tc::bulk_g2s(base + so + room + uso, rec + uw[pc].lo, uw[pc].bytes, &full[slot]);
+            }
+            gso += gw[pc].bytes;
+            uso += uw[pc].bytes;
           }
         } else {  // down: output rows [n, n + nd) of token t, experts [j0, j1)
           const int c2 = c - n1;
-          long long qs = 0;
-          int nd = 0;
+          int qs = 0, nd = 0;
           dn_block(c2 / cpr, q0, q1, a.H, qs, nd);
-          const int t = (int)(qs / a.H), n = (int)(qs - (long long)t * a.H);
+          const int t = qs / a.H, n = qs - t * a.H;
           const int j0 = (c2 % cpr) * jn, j1 = min(a.k, j0 + jn);
           const uint32_t cb = (uint32_t)(a.I / 2), db = (uint32_t)nd * cb;
           const Win dw = window(o.down_s + (size_t)n * (a.I / G), (size_t)nd * (a.I / G));
@@ -619,21 +623,27 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
     // at once.  Lane l takes units l, l + 32, ... of the row, in that order.
     for (int task = warp; task < n1 * kRG; task += kCWarps) {
       const int c = task / kRG, ri = task - c * kRG;
-      long long rs = 0;
-      int nr = 0;
-      gu_chunk(c, r0, r1, a.I, rs, nr);
-      if (ri >= nr) continue;
+      const GuChunk gc = gu_chunk(c, r0, r1, a.I);
+      if (ri >= gc.nr) continue;
       const bool live = take(c);
-      const int p = (int)(rs / a.I), i0 = (int)(rs - (long long)p * a.I);
+      const int pc = ri < gc.n0 ? 0 : 1;
+      const int p = gc.p0 + pc, i = pc == 0 ? gc.i0 + ri : ri - gc.n0;
       const uint8_t* rec = recs[p];
       const uint8_t* base = ring + (size_t)(c % S) * SB;
       const uint32_t cb = (uint32_t)(a.H / 2), so = 2u * kRG * cb, room = (uint32_t)gu_scale_room(a.H, G);
-      const Win gw = window(o.gate_s + (size_t)i0 * (a.H / G), (size_t)nr * (a.H / G));
-      const Win uw = window(o.up_s + (size_t)i0 * (a.H / G), (size_t)nr * (a.H / G));
+      // the row's scales: piece 0's windows first, then piece 1's
+      const Win gw0 = window(o.gate_s + (size_t)gc.i0 * (a.H / G), (size_t)gc.n0 * (a.H / G));
+      const Win uw0 = window(o.up_s + (size_t)gc.i0 * (a.H / G), (size_t)gc.n0 * (a.H / G));
+      uint32_t gso = gw0.delta, uso = uw0.delta;
+      if (pc == 1) {
+        gso = gw0.bytes + window(o.gate_s, (size_t)(gc.nr - gc.n0) * (a.H / G)).delta;
+        uso = uw0.bytes + window(o.up_s, (size_t)(gc.nr - gc.n0) * (a.H / G)).delta;
+      }
+      const int rr = pc == 0 ? ri : ri - gc.n0;  // row within its piece
       const uint8_t* crow = base + (size_t)ri * cb;
-      const uint8_t* gsr = base + so + gw.delta + (size_t)ri * (a.H / G);
-      const uint8_t* usr = base + so + room + uw.delta + (size_t)ri * (a.H / G);
-      const uint4* xt = act + (size_t)(p / a.k) * 4 * upr;
+      const uint8_t* gsr = base + so + gso + (size_t)rr * (a.H / G);
+      const uint8_t* usr = base + so + room + uso + (size_t)rr * (a.H / G);
+      const uint4* xt = act + (size_t)(p / a.k - xt0) * 4 * upr;
       float gs = 0.f, us = 0.f;
       if (live && rec) {
         if constexpr (UPR > 0) {
@@ -660,12 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
           }
         }
       }
-      release(c, ri, nr);
+      release(c, ri, gc.nr);
       gs = moe::warp_sum(gs);
       us = moe::warp_sum(us);
       if (lane == 0)
-        a.hws[(size_t)p * a.I + i0 + ri] =
-            (live && rec) ? gs / (1.0f + expf(-gs)) * us : __uint_as_float(0x7FC00000u);
+        a.hws[(size_t)p * a.I + i] = (live && rec) ? gs / (1.0f + expf(-gs)) * us : __uint_as_float(0x7FC00000u);
     }
     // grid barrier among the consumer threads of every CTA
     moe::tc::named_sync(1, kCThreads);
@@ -736,15 +745,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
       static_assert(kRD % kTR == 0, "row tasks tile a block");
       for (int task = warp; task < nb2 * (kRD / kTR); task += kCWarps) {
         const int bi = task / (kRD / kTR), rb = (task - bi * (kRD / kTR)) * kTR;
-        long long qs = 0;
-        int nd = 0;
+        int qs = 0, nd = 0;
         dn_block(bi, q0, q1, a.H, qs, nd);
         if (rb >= nd) continue;
         const int nr = min(kTR, nd - rb);
         // this task's arrivals on each chunk: its rows, and, for the task of
         // the block's last row, the rows a ragged block lacks
         const uint32_t arrivals = rb + kTR >= nd ? (uint32_t)(kRD - rb) : (uint32_t)kTR;
-        const int t = (int)(qs / a.H), n0 = (int)(qs - (long long)t * a.H);
+        const int t = qs / a.H, n0 = qs - t * a.H;
         float acc[kTR];
 #pragma unroll
         for (int r = 0; r < kTR; ++r) acc[r] = 0.f;
@@ -804,11 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a) {
 // Shared memory for `slots` ring slots plus the activation region: x as FP16
 // quads (T*H halves) in phase 1, h as FP16 hi + lo quads in phase 2.
 inline size_t smem_bytes(int T, int k, int H, int I, int sms, int slots, int slot_bytes) {
-  const long long R2 = (long long)T * H;
-  const long long rows = (R2 + sms - 1) / sms + 1;
-  const long long ntok = std::min<long long>(T, rows / H + 2);
-  const size_t act = std::max<size_t>((size_t)T * H * 2, (size_t)ntok * k * I * 4);
-  return (size_t)slots * slot_bytes + 2 * kMaxSlots * 8 + 64 * 8 + 64 * 4 + 16 + kMaxSlots * 4 + act;
+  // tokens of one CTA's gate/up rows (x) and of its output rows (h)
+  const long long rows1 = (long long)T * k * I / sms + 1;
+  const long long nx = std::min<long long>(T, (rows1 / I + 2) / k + 2);
+  const long long rows2 = (long long)T * H / sms + 1;
+  const long long ntok = std::min<long long>(T, rows2 / H + 2);
+  const size_t act = std::max<size_t>((size_t)nx * H * 2, (size_t)ntok * k * I * 4);
+  const size_t pr = ((size_t)T * k + 15) & ~(size_t)15;
+  return (size_t)slots * slot_bytes + 2 * kMaxSlots * 8 + pr * 8 + pr * 4 + 16 + kMaxSlots * 4 + act;
 }
 
 }  // namespace st
@@ -834,11 +845,11 @@ int stream_smem_limit() { return moe::device_info().smem_optin; }
 
 int sm_count() { return moe::device_info().sms; }
 
-// The streaming kernel takes T*k <= 64 pairs when at least 4 ring slots (of
+// The streaming kernel takes T*k <= 512 pairs when at least 4 ring slots (of
 // kRG row pairs each) fit next to the activations.
 int stream_slots(int T, int k, int H, int I, int fmt, int* slot_bytes) {
   const int sms = sm_count();
-  if (sms <= 0 || (long long)T * k > 64) return 0;
+  if (sms <= 0 || (long long)T * k > st::kMaxPairs) return 0;
   const int G = fmt == MOE_FMT_NVFP4 ? 16 : 32;
   *slot_bytes = st::plan_slot_bytes(H, I, G);
   const size_t limit = (size_t)stream_smem_limit();

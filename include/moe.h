@@ -157,9 +157,11 @@ size_t moe_experts_decode_workspace(int T, int k, moe_expert_shape s);
 
 /* Decode path: the experts of T tokens (T*k small, GEMV shaped), HBM bound
  * (first page, "The engine", item 4: the single-token NVFP4 SwiGLU expert
- * kernel).  For T*k <= 64 (and T*H, T*k*I within 24K floats) this is one
- * persistent kernel with a grid barrier between gate/up and down; larger
- * calls use two kernels.  Results are bit-identical between repeated calls.
+ * kernel).  Small calls (the selected rows fit in shared memory) run one
+ * persistent kernel that copies every row at entry; up to T*k = 512 pairs a
+ * persistent kernel streams the rows through a shared-memory ring; both have
+ * a grid barrier between gate/up and down.  Larger calls use two kernels.
+ * Results are bit-identical between repeated calls.
  * x_bf16 [T x H]; idx, weights [T x k] as moe_router_topk writes them.
  * expert_ptrs: device array of E device pointers, one record per expert;
  *   entries may point anywhere (arbitrary slots), 16-B aligned; an entry may

@@ -540,8 +540,9 @@ class BatchedStack:
                 "unique_experts_per_layer": round(uniq / LAYERS, 1), "expert_bytes_per_step": exp_bytes,
                 "expert_gbs": round(exp_bytes / sec / 1e9, 1),
                 "l2": "inputs larger than L2 (~0.66 GB of distinct records per layer)",
-                "launches_per_step": LAYERS * 5, "dev_status": int(self.st.item()),
-                "roofline": _roofline(nbytes, sec, "whole step (router kernels + two-kernel expert pass), "
+                # per layer: RMS chaining (layers 1-47), logits, top-k, the ring kernel's expert pass
+                "launches_per_step": LAYERS * 4 - 1, "dev_status": int(self.st.item()),
+                "roofline": _roofline(nbytes, sec, "whole step (router kernels + ring-kernel expert pass), "
                                       "unique-record bytes", "one 48-layer step")}
 
 

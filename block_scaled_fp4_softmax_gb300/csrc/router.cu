@@ -8,6 +8,7 @@
 // index ever travels to the host.
 #include "common.cuh"
 #include "router_math.cuh"
+#include "tcgen05.cuh"
 
 namespace {
 
@@ -84,6 +85,113 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 #pragma unroll
       for (int b = 0; b < EW; ++b) {
         const int t = t0 + a, e = e0 + b;
+        if (t < T && e < E) {
+          float v = acc[a][b];
+          if (bias) v = __fadd_rn(v, bias[e]);
+          logits[(size_t)t * E + e] = v;
+        }
+      }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Logits for many tokens, the same order as router_logits_kernel: a CTA owns
+// 32 tokens x 2 WE experts and walks H in K-steps of 256 elements (32 chunks
+// of 8), staging both BF16 tiles in shared memory with cp.async, double
+// buffered.  Warp w owns tokens 8 (w >> 1) .. +8 and experts WE (w & 1) ..
+// +WE; in K-step ks its lane j takes chunk 32 ks + j of every row, so lane j
+// still walks chunks j, j + 32, ... in ascending order with one FMA per
+// element, and the 32 lane sums meet in the same xor butterfly.  The FMAs take
+// the BF16 halves as they are (fma.rn.f32.bf16: both factors are exact in
+// FP32, so this is the FP32 FMA of the converted values).  Needs H % 256 == 0.
+// ---------------------------------------------------------------------------
+constexpr int kRtTok = 32, kRtK = 256, kRtWTok = 8;
+template <int WE>
+constexpr int rt_stage_bytes() { return (kRtTok + 2 * WE) * kRtK * 2; }
+
+__device__ __forceinline__ float fma_bf16(uint32_t a_lo16, uint32_t b_lo16, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;"
+      : "=f"(d)
+      : "h"((uint16_t)(a_lo16 & 0xFFFFu)), "h"((uint16_t)(b_lo16 & 0xFFFFu)), "f"(c));
+  return d;
+}
+
+template <int WE>
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias,
+    int T, int H, int E, float* __restrict__ logits) {
+  constexpr int kExp = 2 * WE, kStage = rt_stage_bytes<WE>();
+  extern __shared__ __align__(128) uint8_t rsm[];
+  moe::pdl_launch_dependents();
+  moe::pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t_cta = blockIdx.x * kRtTok, e_cta = blockIdx.y * kExp;
+  const int ta = (warp >> 1) * kRtWTok, ea = (warp & 1) * WE;  // the warp's rows in the tile
+  const int nks = H / kRtK;
+  // staging: lane j copies the 16-byte piece j of tile rows warp, warp + 8,
+  // ...: x rows 0..31 (clamped to T - 1), then W_r rows (clamped to E - 1)
+  constexpr int kRows = kRtTok + kExp, kPer = kRows / 8;
+  const uint16_t* src[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int r = warp + 8 * j;
+    src[j] = (r < kRtTok ? x + (size_t)min(t_cta + r, T - 1) * H : wr + (size_t)min(e_cta + r - kRtTok, E - 1) * H) +
+             8 * lane;
+  }
+  const uint32_t dst0 = moe::tc::smem_u32(rsm) + (uint32_t)(warp * kRtK + 8 * lane) * 2u;
+  auto stage = [&](int ks, int buf) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      moe::tc::cp_async16(dst0 + (uint32_t)(buf * kStage + j * 8 * kRtK * 2), src[j] + (size_t)ks * kRtK, 16u);
+    moe::tc::cp_async_commit();
+  };
+  float acc[kRtWTok][WE];
+#pragma unroll
+  for (int a = 0; a < kRtWTok; ++a)
+#pragma unroll
+    for (int b = 0; b < WE; ++b) acc[a][b] = 0.0f;
+  stage(0, 0);
+  for (int ks = 0; ks < nks; ++ks) {
+    if (ks + 1 < nks) {
+      stage(ks + 1, (ks + 1) & 1);
+      moe::tc::cp_async_wait<1>();
+    } else {
+      moe::tc::cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(rsm + (ks & 1) * kStage);
+    const uint16_t* ws = xs + kRtTok * kRtK;
+    uint4 wv[WE];
+#pragma unroll
+    for (int b = 0; b < WE; ++b) wv[b] = *reinterpret_cast<const uint4*>(ws + (ea + b) * kRtK + 8 * lane);
+#pragma unroll
+    for (int a = 0; a < kRtWTok; ++a) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(xs + (ta + a) * kRtK + 8 * lane);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t xw = (&xv.x)[i >> 1] >> (16 * (i & 1));
+#pragma unroll
+        for (int b = 0; b < WE; ++b) acc[a][b] = fma_bf16(xw, (&wv[b].x)[i >> 1] >> (16 * (i & 1)), acc[a][b]);
+      }
+    }
+    __syncthreads();  // the buffer is refilled two K-steps on
+  }
+#pragma unroll
+  for (int a = 0; a < kRtWTok; ++a)
+#pragma unroll
+    for (int b = 0; b < WE; ++b) {
+      float v = acc[a][b];
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
+      acc[a][b] = v;
+    }
+  if (lane == 0) {
+#pragma unroll
+    for (int a = 0; a < kRtWTok; ++a)
+#pragma unroll
+      for (int b = 0; b < WE; ++b) {
+        const int t = t_cta + ta + a, e = e_cta + ea + b;
         if (t < T && e < E) {
           float v = acc[a][b];
           if (bias) v = __fadd_rn(v, bias[e]);
@@ -267,10 +375,16 @@ extern "C" int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, 
     const long long warps = (long long)T * E;
     rc = moe::launch_pdl(router_logits_kernel<1, 1>, dim3((unsigned)((warps * 32 + threads - 1) / threads)),
                          dim3(threads), 0, st, x_bf16, wr_bf16, bias, T, H, E, logits);
-  } else {
+  } else if (T < 64 || H % kRtK != 0) {
     const long long warps = (long long)((T + 3) / 4) * ((E + 3) / 4);
     rc = moe::launch_pdl(router_logits_kernel<4, 4>, dim3((unsigned)((warps * 32 + threads - 1) / threads)),
                          dim3(threads), 0, st, x_bf16, wr_bf16, bias, T, H, E, logits);
+  } else {
+    // many tokens: shared-memory tiles of 32 tokens x 8 experts, 2 x 20 KB
+    constexpr int WE = 4;
+    rc = moe::launch_pdl(router_logits_tiled_kernel<WE>, dim3((unsigned)((T + kRtTok - 1) / kRtTok),
+                                                              (unsigned)((E + 2 * WE - 1) / (2 * WE))),
+                         dim3(256), 2 * rt_stage_bytes<WE>(), st, x_bf16, wr_bf16, bias, T, H, E, logits);
   }
   if (rc != MOE_OK) return rc;
   return launch_topk(logits, T, E, k, idx, weights, st);

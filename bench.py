@@ -592,13 +592,15 @@ def measure_host_tier(torch, moe, synth, device, calls: int = 40):
 
 def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
     """FP8 row-scaled GEMV on the two proposed shapes; GB/s of W + x + y per
-    call, L2 flushed between calls."""
+    call: single calls with the L2 flushed before each, and back-to-back calls
+    on distinct matrices (more bytes than the L2 holds) replayed from a CUDA
+    graph, as a model's consecutive matrices would run."""
     out = {}
     flush = torch.ones(512 << 18, dtype=torch.int32, device=device)   # read sweep evicts the L2
     flush_out = torch.zeros((), dtype=torch.int64, device=device)
     for M, K in ((8192, 2560), (2560, 4096)):
         # enough distinct matrices that consecutive calls never share L2 lines
-        n = max(2, (256 << 20) // (M * K) + 1)
+        n = max(16, (256 << 20) // (M * K) + 1)
         ws = [synth.expert_matrix((M, K), seed=M + K + i, device=device).to(torch.float8_e4m3fn)
               .view(torch.uint8) for i in range(n)]
         s = synth.uniform((M,), seed=M, lo=0.5, hi=2.0, device=device)
@@ -618,7 +620,24 @@ def measure_fp8_gemv(torch, moe, synth, device, reps: int = 20):
             tot += a.elapsed_time(b)
         us = tot / reps * 1e3
         nbytes = M * K + M * 4 + K * 2 + M * 4
-        out[f"{M}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                moe.fp8_rowscale_gemv(ws[i], s, x, y)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _gpu_spacer(torch)
+        a.record()
+        for _ in range(5):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        gus = a.elapsed_time(b) / (5 * n) * 1e3
+        out[f"{M}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                           "graph_us": round(gus, 2), "graph_gbs": round(nbytes / (gus * 1e-6) / 1e9, 1),
+                           "graph_launches": n}
+        del g, ws
     return out
 
 

@@ -132,6 +132,17 @@ inline bool grant_smem(K kernel, size_t bytes, SmemGrant& g, int threads = 0) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// BF16 x BF16 + FP32 with one rounding, on the low halves of the words: both
+// factors are exact in FP32, so the result is the FP32 FMA of the converted
+// values, without converting them first.
+__device__ __forceinline__ float fma_bf16(uint32_t a_lo16, uint32_t b_lo16, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;"
+      : "=f"(d)
+      : "h"((uint16_t)(a_lo16 & 0xFFFFu)), "h"((uint16_t)(b_lo16 & 0xFFFFu)), "f"(c));
+  return d;
+}
+
 // Two E4M3 bytes (low byte = first) -> two floats, via the hardware convert.
 __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_bytes) {
   uint32_t h2;

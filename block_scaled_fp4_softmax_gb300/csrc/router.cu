@@ -59,14 +59,9 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
     for (int i = 0; i < 8; ++i) {
 #pragma unroll
       for (int a = 0; a < TT; ++a) {
-        const uint32_t xw = (&xv[a].x)[i >> 1];
-        const float xf = moe::bf16_bits_to_f32((i & 1) ? (xw >> 16) : (xw & 0xFFFFu));
+        const uint32_t xw = (&xv[a].x)[i >> 1] >> (16 * (i & 1));
 #pragma unroll
-        for (int b = 0; b < EW; ++b) {
-          const uint32_t ww = (&wv[b].x)[i >> 1];
-          const float wf = moe::bf16_bits_to_f32((i & 1) ? (ww >> 16) : (ww & 0xFFFFu));
-          acc[a][b] = __fmaf_rn(xf, wf, acc[a][b]);
-        }
+        for (int b = 0; b < EW; ++b) acc[a][b] = moe::fma_bf16(xw, (&wv[b].x)[i >> 1] >> (16 * (i & 1)), acc[a][b]);
       }
     }
   }
@@ -108,14 +103,6 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 constexpr int kRtTok = 32, kRtK = 256, kRtWTok = 8;
 template <int WE>
 constexpr int rt_stage_bytes() { return (kRtTok + 2 * WE) * kRtK * 2; }
-
-__device__ __forceinline__ float fma_bf16(uint32_t a_lo16, uint32_t b_lo16, float c) {
-  float d;
-  asm("fma.rn.f32.bf16 %0, %1, %2, %3;"
-      : "=f"(d)
-      : "h"((uint16_t)(a_lo16 & 0xFFFFu)), "h"((uint16_t)(b_lo16 & 0xFFFFu)), "f"(c));
-  return d;
-}
 
 template <int WE>
 __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
@@ -172,7 +159,7 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
       for (int i = 0; i < 8; ++i) {
         const uint32_t xw = (&xv.x)[i >> 1] >> (16 * (i & 1));
 #pragma unroll
-        for (int b = 0; b < WE; ++b) acc[a][b] = fma_bf16(xw, (&wv[b].x)[i >> 1] >> (16 * (i & 1)), acc[a][b]);
+        for (int b = 0; b < WE; ++b) acc[a][b] = moe::fma_bf16(xw, (&wv[b].x)[i >> 1] >> (16 * (i & 1)), acc[a][b]);
       }
     }
     __syncthreads();  // the buffer is refilled two K-steps on

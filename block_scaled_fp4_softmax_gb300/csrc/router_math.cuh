@@ -99,9 +99,7 @@ __device__ __forceinline__ float logit_dot(const uint16_t* x_row, const uint16_t
         const uint32_t ww[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float xf = bf16_bits_to_f32((i & 1) ? (xw[i >> 1] >> 16) : (xw[i >> 1] & 0xFFFFu));
-          const float wf = bf16_bits_to_f32((i & 1) ? (ww[i >> 1] >> 16) : (ww[i >> 1] & 0xFFFFu));
-          acc = __fmaf_rn(xf, wf, acc);
+          acc = fma_bf16(xw[i >> 1] >> (16 * (i & 1)), ww[i >> 1] >> (16 * (i & 1)), acc);
         }
       }
     }

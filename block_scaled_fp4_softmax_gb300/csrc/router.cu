@@ -92,15 +92,15 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 // ---------------------------------------------------------------------------
 // Logits for many tokens, the same order as router_logits_kernel: a CTA owns
 // 32 tokens x 2 WE experts and walks H in K-steps of 256 elements (32 chunks
-// of 8), staging both BF16 tiles in shared memory with cp.async, double
-// buffered.  Warp w owns tokens 8 (w >> 1) .. +8 and experts WE (w & 1) ..
+// of 8), staging both BF16 tiles in shared memory with cp.async, three
+// buffers deep.  Warp w owns tokens 8 (w >> 1) .. +8 and experts WE (w & 1) ..
 // +WE; in K-step ks its lane j takes chunk 32 ks + j of every row, so lane j
 // still walks chunks j, j + 32, ... in ascending order with one FMA per
 // element, and the 32 lane sums meet in the same xor butterfly.  The FMAs take
 // the BF16 halves as they are (fma.rn.f32.bf16: both factors are exact in
 // FP32, so this is the FP32 FMA of the converted values).  Needs H % 256 == 0.
 // ---------------------------------------------------------------------------
-constexpr int kRtTok = 32, kRtK = 256, kRtWTok = 8;
+constexpr int kRtTok = 32, kRtK = 256, kRtWTok = 8, kRtStages = 3;
 template <int WE>
 constexpr int rt_stage_bytes() { return (kRtTok + 2 * WE) * kRtK * 2; }
 
@@ -138,16 +138,17 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
   for (int a = 0; a < kRtWTok; ++a)
 #pragma unroll
     for (int b = 0; b < WE; ++b) acc[a][b] = 0.0f;
+  // three buffers: K-steps ks + 1 and ks + 2 are in flight while ks is
+  // summed; one barrier per K-step both publishes buffer ks and retires the
+  // buffer that K-step ks + 2 then refills (last read in K-step ks - 1)
   stage(0, 0);
+  if (nks > 1) stage(1, 1);
   for (int ks = 0; ks < nks; ++ks) {
-    if (ks + 1 < nks) {
-      stage(ks + 1, (ks + 1) & 1);
-      moe::tc::cp_async_wait<1>();
-    } else {
-      moe::tc::cp_async_wait<0>();
-    }
+    if (ks + 1 < nks) moe::tc::cp_async_wait<1>();
+    else moe::tc::cp_async_wait<0>();
     __syncthreads();
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(rsm + (ks & 1) * kStage);
+    if (ks + 2 < nks) stage(ks + 2, (ks + 2) % kRtStages);
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(rsm + (ks % kRtStages) * kStage);
     const uint16_t* ws = xs + kRtTok * kRtK;
     uint4 wv[WE];
 #pragma unroll
@@ -162,7 +163,6 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
         for (int b = 0; b < WE; ++b) acc[a][b] = moe::fma_bf16(xw, (&wv[b].x)[i >> 1] >> (16 * (i & 1)), acc[a][b]);
       }
     }
-    __syncthreads();  // the buffer is refilled two K-steps on
   }
 #pragma unroll
   for (int a = 0; a < kRtWTok; ++a)
@@ -367,11 +367,14 @@ extern "C" int moe_router_topk(const uint16_t* x_bf16, const uint16_t* wr_bf16, 
     rc = moe::launch_pdl(router_logits_kernel<4, 4>, dim3((unsigned)((warps * 32 + threads - 1) / threads)),
                          dim3(threads), 0, st, x_bf16, wr_bf16, bias, T, H, E, logits);
   } else {
-    // many tokens: shared-memory tiles of 32 tokens x 8 experts, 2 x 20 KB
+    // many tokens: shared-memory tiles of 32 tokens x 8 experts, 3 x 20 KB
     constexpr int WE = 4;
+    static moe::SmemGrant granted;
+    if (!moe::grant_smem(router_logits_tiled_kernel<WE>, kRtStages * rt_stage_bytes<WE>(), granted))
+      return MOE_ERR_CUDA;
     rc = moe::launch_pdl(router_logits_tiled_kernel<WE>, dim3((unsigned)((T + kRtTok - 1) / kRtTok),
                                                               (unsigned)((E + 2 * WE - 1) / (2 * WE))),
-                         dim3(256), 2 * rt_stage_bytes<WE>(), st, x_bf16, wr_bf16, bias, T, H, E, logits);
+                         dim3(256), kRtStages * rt_stage_bytes<WE>(), st, x_bf16, wr_bf16, bias, T, H, E, logits);
   }
   if (rc != MOE_OK) return rc;
   return launch_topk(logits, T, E, k, idx, weights, st);

@@ -313,7 +313,12 @@ int moe_experts_grouped(const uint16_t* x_bf16, const int32_t* idx, const float*
  * stored in FP8 with one scale per row; "The engine", item 4: their own GEMV
  * kernel).  w_e4m3 [M x K] E4M3FN bytes, row_scale [M] FP32, x_bf16 [K];
  * y[m] = row_scale[m] * sum_k e4m3(w[m,k]) * x[k], FP32 accumulation.
- * K % 16 == 0; w and x 16-B aligned. */
+ * K % 16 == 0; w and x 16-B aligned.
+ * For K <= 4096 the launch is a programmatic dependent launch that reads w
+ * before it waits for the previous kernel of the stream (x and row_scale only
+ * after): w is a weight that no kernel of the stream writes in the call's
+ * immediate past, as for model parameters; a caller that has just produced w
+ * on the same stream synchronises (or records an event) first. */
 int fp8_rowscale_gemv(const uint8_t* w_e4m3, const float* row_scale, const uint16_t* x_bf16,
                       int M, int K, float* y, void* stream);
 

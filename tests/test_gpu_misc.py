@@ -73,3 +73,37 @@ def test_fp8_gemv(M, K):
     want = O.fp8_rowscale_gemv(w8.numpy(), s.numpy(), bits(x))
     err = O.rel_l2(y.cpu().numpy(), want)
     assert err <= 1e-5, err
+
+
+def test_fp8_gemv_chained_after_the_kernel_that_writes_x():
+    """The GEMV reads its weights before waiting on the previous kernel of the
+    stream and x only after: x produced by the kernel right before it (the RMS
+    normalisation, launched on the same stream) must be the x it uses, across
+    a chain of back-to-back calls captured in a graph."""
+    M, K = 4096, 2560
+    W = synth.expert_matrix((M, K), seed=77)
+    w8 = W.to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+    s = synth.uniform((M,), seed=78, lo=0.5, hi=2.0).cuda()
+    ys = [torch.randn(1, K, generator=torch.Generator().manual_seed(80 + i)) * 0.05 for i in range(4)]
+    yd = [y.cuda() for y in ys]
+    x = torch.empty(1, K, dtype=torch.bfloat16, device="cuda")
+    outs = [torch.empty(M, dtype=torch.float32, device="cuda") for _ in ys]
+    g = torch.cuda.CUDAGraph()
+    moe.moe_rmsnorm_bf16(yd[0], 1e-6, x=x)
+    moe.fp8_rowscale_gemv(w8, s, x[0], outs[0])
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for i in range(len(ys)):
+            moe.moe_rmsnorm_bf16(yd[i], 1e-6, x=x)
+            moe.fp8_rowscale_gemv(w8, s, x[0], outs[i])
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    w_np = w8.cpu().numpy()
+    for i, y in enumerate(ys):
+        xb = O.rmsnorm_bf16(y.numpy(), 1e-6)
+        want = O.fp8_rowscale_gemv(w_np, s.cpu().numpy(), xb[0])
+        err = O.rel_l2(outs[i].cpu().numpy(), want)
+        assert err <= 1e-5, (i, err)
+

@@ -1181,8 +1181,9 @@ def run_reference(args):
 
 def run_profile_case(args):
     """A small case of one kernel family for ncu: one decode layer (a 512-expert
-    router over a 64-record pool, 177 MB of records, larger than L2), or the
-    prompt layer."""
+    router over a 64-record pool, 177 MB of records, larger than L2), one
+    DeepSeek-shaped call, one 32-token batched-decode call over a 64-record
+    pool, FP8 GEMVs on distinct matrices, or the prompt layer."""
     import torch
 
     from block_scaled_fp4_softmax_gb300 import build, moe, synth
@@ -1224,6 +1225,36 @@ def run_profile_case(args):
             idx, w, _ = moe.moe_router_topk(x, wr, None, D.KD)
             moe.moe_experts_decode(x, idx, w, ptrs, s, workspace=ws)
         torch.cuda.synchronize()
+    elif args.profile_case == "batched_call":
+        # one layer of the batched decode: 32 tokens routed by a 512-expert
+        # router over 64 distinct records (177 MB, larger than L2; expert e
+        # uses record e % 64), then the ring kernel's expert pass
+        s = moe.shape(H, I, moe.FMT_NVFP4)
+        nE, T = 64, 32
+        pool = torch.empty(nE, moe.moe_expert_record_bytes(s), dtype=torch.uint8, device=dev)
+        for e in range(nE):
+            g, up, d = synth.expert_weights(H, I, synth.expert_seed(0, 0, e), device=dev)
+            moe.fp4_pack_expert(g, up, d, s, record=pool[e])
+        ptrs = moe.pointer_table([pool[e % nE] for e in range(E)])
+        wr = synth.router_weights(E, H, synth.seed_of(0, 0, synth.T_ROUTER), device=dev)
+        ws = torch.zeros(moe.moe_experts_decode_workspace(T, K_TOP, s), dtype=torch.uint8, device=dev)
+        y = torch.empty(T, H, dtype=torch.float32, device=dev)
+        for i in range(args.warmup + args.steps):
+            x = synth.activations(T, H, synth.seed_of(0, 70 + i, synth.T_X), device=dev)
+            idx, w, _ = moe.moe_router_topk(x, wr, None, K_TOP)
+            moe.moe_experts_decode(x, idx, w, ptrs, s, y, workspace=ws)
+        torch.cuda.synchronize()
+    elif args.profile_case == "fp8_gemv":
+        # 8192 x 2560 E4M3 GEMVs on 8 distinct matrices (168 MB, larger than L2)
+        M, K, n = 8192, 2560, 8
+        ws_ = [synth.expert_matrix((M, K), seed=M + K + i, device=dev).to(torch.float8_e4m3fn).view(torch.uint8)
+               for i in range(n)]
+        sc = synth.uniform((M,), seed=M, lo=0.5, hi=2.0, device=dev)
+        x = synth.activations(1, K, seed=K, device=dev)[0]
+        y = torch.empty(M, dtype=torch.float32, device=dev)
+        for i in range(args.warmup + args.steps):
+            moe.fp8_rowscale_gemv(ws_[i % n], sc, x, y)
+        torch.cuda.synchronize()
     else:
         pl = PromptLayer(torch, moe, synth, dev)
         for _ in range(args.warmup + args.steps):
@@ -1243,7 +1274,8 @@ def main():
     ap.add_argument("--no-prompt", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the one-layer, DeepSeek-shaped and batched workloads")
     ap.add_argument("--cpu-seconds-other", type=float, default=6.0)
-    ap.add_argument("--profile-case", choices=("none", "decode_layer", "prompt_layer", "deepseek_call"), default="none",
+    ap.add_argument("--profile-case", choices=("none", "decode_layer", "prompt_layer", "deepseek_call", "batched_call",
+                                               "fp8_gemv"), default="none",
                     help="small fixed case for ncu captures (no JSON line)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

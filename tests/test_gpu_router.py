@@ -52,6 +52,23 @@ def test_router_exact(T, E, H, k):
     _check(*out, k)
 
 
+# Many-token shapes: T >= 64 with H a multiple of 256 take the shared-memory
+# tiled kernel (32 tokens x 8 experts per CTA, K-steps of 256 through a
+# three-buffer ring); just below either threshold the warp-per-logit kernel.
+@pytest.mark.parametrize("T,E,H,k,biased", [
+    (64, 8, 256, 4, False),       # the threshold; one K-step; one expert tile
+    (97, 65, 512, 10, False),     # ragged token and expert tiles; two K-steps
+    (130, 33, 768, 3, True),      # three K-steps (one full turn of the ring), bias
+    (300, 512, 2560, 10, True),   # ten K-steps: the ring wraps three times
+    (63, 64, 2560, 10, False),    # one token short of the tiled kernel
+    (80, 64, 320, 10, False),     # H not a multiple of 256
+])
+def test_router_many_tokens_exact(T, E, H, k, biased):
+    bias = synth.zipf_bias(E, seed=T + E) if biased else None
+    out = _run(T, E, H, k, seed=7 * T + E, bias=bias)
+    _check(*out, k)
+
+
 def test_router_prompt_sampled_rows_with_zipf_bias():
     T, E, H, k = 2451, 512, 2560, 10
     bias = synth.zipf_bias(E, seed=2003)

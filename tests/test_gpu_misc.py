@@ -59,10 +59,11 @@ def test_rmsnorm_bitexact(T, H):
     assert np.array_equal(got, want), f"{np.count_nonzero(got != want)} differ"
 
 
-# one or two rows per warp (odd M leaves a warp with one), ragged units per
+# one or two rows per warp (odd M leaves a warp with one), one to eight
+# 16-byte units per lane (every instance of the row kernel), ragged units per
 # lane, and rows longer than 4096 elements (the chunked kernel)
 @pytest.mark.parametrize("M,K", [(8192, 2560), (2560, 4096), (1000, 16), (37, 272), (4097, 2560), (65, 1040),
-                                 (3, 8192)])
+                                 (3, 8192), (33, 1024), (34, 2048), (35, 3072), (36, 3584)])
 def test_fp8_gemv(M, K):
     rng = np.random.default_rng(M + K)
     W = synth.expert_matrix((M, K), seed=M * 7 + K)

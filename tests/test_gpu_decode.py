@@ -83,6 +83,14 @@ def test_decode_ring_mxfp4_two_tokens():
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("T,k", [(51, 10), (64, 8), (52, 10), (130, 4)])
+def test_decode_ring_limit_and_two_kernel_path(pool64, T, k):
+    """T*k = 510 and 512 take the ring kernel (its pair table holds at most 512
+    pairs); 520 takes the two-kernel path on HBM records, with k = 10 and 4."""
+    err, _ = _decode_vs_oracle(pool64, T, k, seed=300 + T)
+    assert err <= TOL, err
+
+
 def test_decode_small_shapes():
     pool = Pool(8, 128, 64, 0, workload=9)
     err, _ = _decode_vs_oracle(pool, 3, 4, seed=31)

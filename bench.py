@@ -651,10 +651,16 @@ def max_over_ranks(value: float, dist=None, device="cpu") -> float:
     return float(t.item())
 
 
-def _hash_sources():
+# the sources the one-shot decode kernel is compiled from: a DRAM capture
+# stays valid while these files are unchanged
+ONESHOT_SOURCES = ("common.cuh", "decode_math.cuh", "decode_oneshot.cu", "decode_oneshot.h", "router_math.cuh",
+                   "tcgen05.cuh")
+
+
+def _hash_sources(names=ONESHOT_SOURCES):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_scaled_fp4_softmax_gb300", "csrc")
-    for n in sorted(os.listdir(d)):
+    for n in sorted(names):
         with open(os.path.join(d, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
@@ -662,7 +668,7 @@ def _hash_sources():
 
 def _traffic_from_profiles(kernel_key: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources."""
+    the current sources of the kernel (the files of ONESHOT_SOURCES)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
